@@ -1,0 +1,197 @@
+"""CPU oracle for the paged-KV attention step -- TEST INFRASTRUCTURE ONLY.
+
+Thin ctypes wrappers around ``pa_oracle.c`` (plain C, fp64).  Only the tests,
+``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg import this
+package; the CUDA library and its Python binding never do.
+
+Parity status of each function (how it is pinned, in ``tests/test_oracle.py``):
+
+* ``prepare_inputs`` -- pinned by the pages' printed worked examples
+  (``tests/golden/``), hand-derived exercise answers, invariants and a brute
+  force against a separately written pure-Python restatement.
+* ``cache_write`` -- pinned by bit equality against a direct per-slot copy,
+  untouched-slot preservation and write-then-gather round trips.
+* ``attention`` -- pinned by closed forms (one visible key, K = 0, constant V,
+  one dominant key), a pure-Python ``math.fsum`` brute force on tiny inputs,
+  NumPy dense causal attention on the unpaged K/V, and invariances (physical
+  block permutation, request order, GQA vs. replicated MHA, chunked vs. full
+  prefill).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPES = {"bf16": 0, "fp16": 1}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pa_oracle.c`` into ``libpa_oracle.so`` (gcc, strict IEEE)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # PA_ORACLE_LIB points the wrappers at another build of the same
+            # source (the mutation tests use it to load deliberately broken
+            # copies); by default the library is built next to this file.
+            path = os.environ.get("PA_ORACLE_LIB") or build()
+            lib = ctypes.CDLL(path)
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            u16p = ctypes.c_void_p
+            lib.oracle_prepare_inputs.restype = ctypes.c_int
+            lib.oracle_prepare_inputs.argtypes = [
+                i32p, i32p, i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, i32p, i32p, i32p, i32p, ctypes.c_int32,
+                i32p, i32p]
+            lib.oracle_cache_write.restype = ctypes.c_int
+            lib.oracle_cache_write.argtypes = [
+                u16p, u16p, ctypes.c_int64, u16p, u16p, i32p, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
+            lib.oracle_attention.restype = ctypes.c_int
+            lib.oracle_attention.argtypes = [
+                u16p, u16p, u16p, i32p, ctypes.c_int32, i32p, i32p, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int32,
+                ctypes.POINTER(ctypes.c_double), i32p, ctypes.c_int32, ctypes.c_int32]
+            lib.oracle_num_cpus.restype = ctypes.c_int
+            lib.oracle_num_cpus.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p32(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _bits(a) -> np.ndarray:
+    """16-bit element patterns of a bf16/fp16 torch tensor or a uint16 array."""
+    if isinstance(a, np.ndarray):
+        if a.dtype == np.float16:
+            return np.ascontiguousarray(a).view(np.uint16)
+        return np.ascontiguousarray(a.astype(np.uint16, copy=False))
+    import torch  # local: torch only as a carrier of bf16 bit patterns
+    t = a.detach().to("cpu").contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def num_cpus() -> int:
+    return int(_load().oracle_num_cpus())
+
+
+def prepare_inputs(num_scheduled_tokens, num_computed_tokens, block_table, block_size,
+                   num_tokens, num_blocks, qsl_capacity=None, check=True):
+    """Index tensors of one step.  Returns a dict of int32 arrays:
+    req_indices, positions, slot_mapping [T]; query_start_loc [qsl_capacity];
+    seq_lens, logits_indices [R]; and ``status`` (0 when the inputs are valid)."""
+    lib = _load()
+    nst, nct = _i32(num_scheduled_tokens), _i32(num_computed_tokens)
+    bt = _i32(block_table)
+    r = nst.shape[0]
+    bt = bt.reshape(r, -1) if r else bt.reshape(0, max(1, bt.size))
+    mb = bt.shape[1]
+    cap = r + 1 if qsl_capacity is None else int(qsl_capacity)
+    out = {k: np.full(max(num_tokens, 0), -7, np.int32)
+           for k in ("req_indices", "positions", "slot_mapping")}
+    out["query_start_loc"] = np.full(max(cap, 1), -7, np.int32)
+    out["seq_lens"] = np.full(r, -7, np.int32)
+    out["logits_indices"] = np.full(r, -7, np.int32)
+    rc = lib.oracle_prepare_inputs(
+        _p32(nst), _p32(nct), _p32(bt), r, mb, int(block_size), int(num_tokens),
+        int(num_blocks), _p32(out["req_indices"]), _p32(out["positions"]),
+        _p32(out["slot_mapping"]), _p32(out["query_start_loc"]), cap,
+        _p32(out["seq_lens"]), _p32(out["logits_indices"]))
+    out["status"] = int(rc)
+    if check and rc != 0:
+        raise OracleError(f"oracle_prepare_inputs rejected the inputs ({rc})")
+    return out
+
+
+def cache_write(key, value, key_cache, value_cache, slot_mapping, num_kv_heads, head_dim,
+                block_size, num_blocks, kv_token_stride=None, check=True):
+    """Return (key_cache', value_cache', status) as uint16 arrays shaped like the
+    input caches: the pools after each token's K/V was copied to its slot."""
+    lib = _load()
+    kb, vb = _bits(key), _bits(value)
+    stride = num_kv_heads * head_dim if kv_token_stride is None else int(kv_token_stride)
+    kcb = _bits(key_cache).copy()
+    vcb = _bits(value_cache).copy()
+    slots = _i32(slot_mapping)
+    t = slots.shape[0]
+    if kb.size < (t - 1) * stride + num_kv_heads * head_dim if t else False:
+        raise OracleError("key buffer too small for the stride")
+    rc = lib.oracle_cache_write(kb.ctypes.data, vb.ctypes.data, stride, kcb.ctypes.data,
+                                vcb.ctypes.data, _p32(slots), t, int(num_kv_heads),
+                                int(head_dim), int(block_size), int(num_blocks))
+    if check and rc != 0:
+        raise OracleError(f"oracle_cache_write rejected the inputs ({rc})")
+    return kcb, vcb, int(rc)
+
+
+def attention(q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
+              num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+              tokens=None, num_threads=0):
+    """fp64 attention output [T, Hq, D].  With ``tokens`` (ascending flat token
+    indices) only those rows are computed; the others are NaN."""
+    lib = _load()
+    qb = _bits(q)
+    kcb, vcb = _bits(key_cache), _bits(value_cache)
+    qsl, sl = _i32(query_start_loc), _i32(seq_lens)
+    r = sl.shape[0]
+    bt = _i32(block_table).reshape(r, -1) if r else _i32(block_table).reshape(0, 1)
+    t = int(qsl[r]) if r else 0
+    out = np.full((t, num_q_heads, head_dim), np.nan, np.float64)
+    sel = None if tokens is None else _i32(np.sort(np.asarray(tokens)))
+    rc = lib.oracle_attention(
+        qb.ctypes.data, kcb.ctypes.data, vcb.ctypes.data, _p32(bt), bt.shape[1], _p32(qsl),
+        _p32(sl), r, t, int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+        int(num_blocks), float(scale), DTYPES[dtype],
+        out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+        None if sel is None else _p32(sel), 0 if sel is None else sel.shape[0],
+        int(num_threads))
+    if rc != 0:
+        raise OracleError(f"oracle_attention rejected the inputs ({rc})")
+    return out
+
+
+def step(w, vals, qsl_capacity=None, tokens=None, num_threads=0):
+    """The whole step for a workload from ``workloads``: index build, cache
+    write, attention.  Returns (indices dict, key_cache', value_cache', out)."""
+    idx = prepare_inputs(w.num_scheduled_tokens, w.num_computed_tokens, w.block_table,
+                         w.block_size, w.num_tokens, w.num_blocks, qsl_capacity)
+    kc, vc, _ = cache_write(vals["key"], vals["value"], vals["key_cache"],
+                            vals["value_cache"], idx["slot_mapping"], w.num_kv_heads,
+                            w.head_dim, w.block_size, w.num_blocks)
+    out = attention(vals["q"], kc, vc, w.block_table, idx["query_start_loc"][: w.num_reqs + 1],
+                    idx["seq_lens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
+                    w.block_size, w.num_blocks, w.scale, w.dtype, tokens, num_threads)
+    return idx, kc, vc, out

@@ -1,0 +1,286 @@
+"""Seeded synthetic workloads for one paged-KV attention step.
+
+This module builds inputs only: how many tokens each request schedules and
+has already computed, where each request's cache blocks sit in the pool, and
+random Q/K/V values.  It holds none of the step's own arithmetic (the index
+build, the cache write, the attention); the CUDA path's tests, the benchmark
+and the oracle all take their inputs from here.
+
+Recipe (the same for every named workload):
+
+* Request lengths come from a NumPy PCG64 generator seeded with ``seed``.
+  A decode request has one scheduled token and ``num_computed_tokens =
+  context - 1``, so its context length includes the new token.
+* Physical blocks: a seeded random permutation of the pool; requests take
+  their blocks in order from the shuffled list (shared blocks are taken
+  once and referenced by several tables).  Table entries past a request's
+  last block are -1, so a stray read of one is detectable.
+* The pool holds ``ceil(1.1 * blocks needed)`` blocks (the tiny workload:
+  exactly 16).
+* Values: every element of q, the new tokens' key/value and the whole cache
+  pool is N(0, 1) drawn by a seeded ``torch.Generator`` on the requested
+  device, rounded to bf16 / fp16 (round to nearest even).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+BLOCK_SIZE = 16
+
+_TORCH_DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+@dataclasses.dataclass
+class Workload:
+    """One step's shapes and index inputs (host arrays)."""
+
+    name: str
+    num_scheduled_tokens: np.ndarray  # int32 [R], tokens each request runs this step
+    num_computed_tokens: np.ndarray   # int32 [R], tokens already in the cache
+    block_table: np.ndarray           # int32 [R, MB] physical block ids, -1 padded
+    num_blocks: int                   # physical blocks in the pool
+    block_size: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    dtype: str                        # "bf16" | "fp16"
+    unique_blocks: int = 0            # distinct physical blocks referenced by the tables
+
+    @property
+    def num_reqs(self) -> int:
+        return int(self.num_scheduled_tokens.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.num_scheduled_tokens.sum())
+
+    @property
+    def max_blocks_per_req(self) -> int:
+        return int(self.block_table.shape[1])
+
+    @property
+    def context_lens(self) -> np.ndarray:
+        """Context length each request was drawn with (history + this step)."""
+        return (self.num_computed_tokens.astype(np.int64)
+                + self.num_scheduled_tokens.astype(np.int64))
+
+    @property
+    def max_query_len(self) -> int:
+        return int(self.num_scheduled_tokens.max()) if self.num_reqs else 0
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_reqs else 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _TORCH_DTYPES[self.dtype]
+
+    def kv_read_bytes(self) -> int:
+        """Bytes of K and V context every request's attention reads (logical)."""
+        elt = 2
+        return int(self.context_lens.sum()) * 2 * self.num_kv_heads * self.head_dim * elt
+
+    def kv_unique_bytes(self) -> int:
+        """Bytes of K and V in the distinct blocks the tables reference."""
+        elt = 2
+        return (self.unique_blocks * self.block_size * 2 * self.num_kv_heads
+                * self.head_dim * elt)
+
+
+def _blocks_for(context_len: int, block_size: int) -> int:
+    return -(-int(context_len) // block_size)
+
+
+def _pool_size(needed: int) -> int:
+    return int(math.ceil(needed * 1.1))
+
+
+def _tables(rows: list[list[int]], width: int | None = None) -> np.ndarray:
+    width = max(len(r) for r in rows) if width is None else width
+    bt = np.full((len(rows), max(width, 1)), -1, dtype=np.int32)
+    for i, r in enumerate(rows):
+        bt[i, : len(r)] = r
+    return bt
+
+
+def _private_tables(rng: np.random.Generator, ctx: np.ndarray, block_size: int,
+                    num_blocks: int | None = None):
+    need = [_blocks_for(c, block_size) for c in ctx]
+    nb = _pool_size(sum(need)) if num_blocks is None else num_blocks
+    perm = rng.permutation(nb)
+    rows, k = [], 0
+    for n in need:
+        rows.append([int(b) for b in perm[k : k + n]])
+        k += n
+    return _tables(rows), nb, sum(need)
+
+
+def _make(name, nst, nct, rng, hq, hkv, d, dtype, num_blocks=None) -> Workload:
+    nst = np.asarray(nst, dtype=np.int32)
+    nct = np.asarray(nct, dtype=np.int32)
+    bt, nb, uniq = _private_tables(rng, nct.astype(np.int64) + nst, BLOCK_SIZE, num_blocks)
+    return Workload(name, nst, nct, bt, nb, BLOCK_SIZE, hq, hkv, d, dtype, uniq)
+
+
+# ---------------------------------------------------------------------------
+# The five named workloads
+# ---------------------------------------------------------------------------
+
+def tiny(seed: int = 0) -> Workload:
+    """3 requests, [2,5,3] scheduled at [17,0,40] computed; 4 q / 2 kv heads,
+    head_dim 64, a 16-block pool."""
+    rng = np.random.default_rng(seed)
+    return _make("tiny-3req-[2,5,3]", [2, 5, 3], [17, 0, 40], rng, 4, 2, 64, "bf16",
+                 num_blocks=16)
+
+
+def decode_batch(seed: int = 1) -> Workload:
+    """256 single-token decodes, context ~ U[128, 4096]; 32 q / 8 kv heads, D 128."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(128, 4096, size=256, endpoint=True)
+    return _make("decode-256x[128,4096]-gqa32/8-d128", np.ones(256, np.int32), ctx - 1,
+                 rng, 32, 8, 128, "bf16")
+
+
+def mixed_step(seed: int = 2) -> Workload:
+    """One 5000-token prompt chunk at 2048 computed, then 200 single-token decodes
+    with context ~ U[256, 8192]; 32 q / 8 kv heads, D 128."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(256, 8192, size=200, endpoint=True)
+    nst = np.concatenate([[5000], np.ones(200, np.int64)])
+    nct = np.concatenate([[2048], ctx - 1])
+    return _make("mixed-5000@2048+200x[256,8192]-gqa32/8-d128", nst, nct, rng,
+                 32, 8, 128, "bf16")
+
+
+def mha_decode(seed: int = 3) -> Workload:
+    """30 single-token decodes at context 2048; 40 q = 40 kv heads, D 128, fp16."""
+    rng = np.random.default_rng(seed)
+    return _make("mha-30x2048-h40-d128-fp16", np.ones(30, np.int32),
+                 np.full(30, 2047, np.int32), rng, 40, 40, 128, "fp16")
+
+
+def shared_prefix(seed: int = 4) -> Workload:
+    """64 sequences sharing the physical blocks of a 1024-token prefix, each
+    followed by P ~ U[0,31] full private blocks and u ~ U[0,15] more context
+    tokens, with the new token at position 1024 + 16P + u in its own private
+    block; plus 4 requests at context 32768.  32 q / 8 kv heads, D 128."""
+    rng = np.random.default_rng(seed)
+    bs = BLOCK_SIZE
+    prefix_blocks = 1024 // bs
+    p = rng.integers(0, 31, size=64, endpoint=True)
+    u = rng.integers(0, 15, size=64, endpoint=True)
+    nct_short = 1024 + bs * p + u
+    long_ctx = np.full(4, 32768)
+    private_need = [int(pi) + 1 for pi in p] + [_blocks_for(c, bs) for c in long_ctx]
+    needed = prefix_blocks + sum(private_need)
+    nb = _pool_size(needed)
+    perm = rng.permutation(nb)
+    shared = [int(b) for b in perm[:prefix_blocks]]
+    k = prefix_blocks
+    rows = []
+    for i, n in enumerate(private_need):
+        own = [int(b) for b in perm[k : k + n]]
+        k += n
+        rows.append(shared + own if i < 64 else own)
+    nst = np.ones(68, np.int32)
+    nct = np.concatenate([nct_short, long_ctx - 1]).astype(np.int32)
+    return Workload("shared-prefix-64x(1024+priv)+4x32768-gqa32/8-d128", nst, nct,
+                    _tables(rows), nb, bs, 32, 8, 128, "bf16", needed)
+
+
+NAMED = {
+    "tiny": tiny,
+    "decode": decode_batch,
+    "mixed": mixed_step,
+    "mha": mha_decode,
+    "shared_prefix": shared_prefix,
+}
+
+
+def named(name: str, seed: int | None = None) -> Workload:
+    fn = NAMED[name]
+    return fn() if seed is None else fn(seed)
+
+
+# ---------------------------------------------------------------------------
+# Small random workloads for parity sweeps
+# ---------------------------------------------------------------------------
+
+def random_case(seed: int, *, max_reqs: int = 6, max_new: int = 40,
+                max_computed: int = 300, head_dim: int | None = None,
+                dtype: str | None = None, group: int | None = None,
+                num_kv_heads: int | None = None, long_prefill: int = 0) -> Workload:
+    """A random small step: 1..max_reqs requests mixing decodes (1 token) and
+    chunks (2..max_new tokens) at random computed offsets.  ``long_prefill``
+    adds one request of that many scheduled tokens."""
+    rng = np.random.default_rng(seed)
+    r = int(rng.integers(1, max_reqs, endpoint=True))
+    kinds = rng.random(r) < 0.5
+    nst = np.where(kinds, 1, rng.integers(2, max(3, max_new + 1), size=r))
+    nct = rng.integers(0, max_computed, size=r, endpoint=True)
+    if long_prefill:
+        nst = np.concatenate([nst, [long_prefill]])
+        nct = np.concatenate([nct, [int(rng.integers(0, max_computed + 1))]])
+    hkv = int(num_kv_heads or rng.choice([1, 2, 4]))
+    g = int(group or rng.choice([1, 2, 4, 8]))
+    d = int(head_dim or rng.choice([64, 128]))
+    dt = dtype or str(rng.choice(["bf16", "fp16"]))
+    return _make(f"random-{seed}", nst, nct, rng, hkv * g, hkv, d, dt)
+
+
+# ---------------------------------------------------------------------------
+# Values
+# ---------------------------------------------------------------------------
+
+def _randn(shape, gen: torch.Generator, device, dtype, chunk_elems: int = 1 << 27):
+    """N(0,1) in fp32 rounded to ``dtype``; generated in chunks along dim 0 so
+    the fp32 temporary stays bounded."""
+    out = torch.empty(shape, dtype=dtype, device=device)
+    flat = out.view(shape[0], -1)
+    row = flat.shape[1] if flat.dim() == 2 else 1
+    step = max(1, chunk_elems // max(row, 1))
+    for i in range(0, shape[0], step):
+        j = min(shape[0], i + step)
+        flat[i:j] = torch.randn((j - i, row), generator=gen, device=device,
+                                dtype=torch.float32).to(dtype)
+    return out
+
+
+def make_values(w: Workload, seed: int = 0, device="cpu", fused_qkv: bool = False):
+    """Q, the new tokens' K/V and a filled cache pool for workload ``w``.
+
+    Returns a dict of tensors on ``device``: ``q [T,Hq,D]``, ``key``/``value``
+    ``[T,Hkv,D]`` and ``key_cache``/``value_cache`` ``[NB,bs,Hkv,D]``.  With
+    ``fused_qkv`` the three projections are views of one ``[T,(Hq+2Hkv)*D]``
+    tensor, so ``key``/``value`` have token stride ``(Hq+2Hkv)*D``."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(seed))
+    dt = w.torch_dtype
+    t, hq, hkv, d = w.num_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
+    out = {}
+    if fused_qkv:
+        qkv = _randn((max(t, 1), (hq + 2 * hkv) * d), gen, dev, dt)[:t]
+        out["q"] = qkv[:, : hq * d].view(t, hq, d)
+        out["key"] = qkv[:, hq * d : (hq + hkv) * d].view(t, hkv, d)
+        out["value"] = qkv[:, (hq + hkv) * d :].view(t, hkv, d)
+        out["qkv"] = qkv
+    else:
+        out["q"] = _randn((max(t, 1), hq, d), gen, dev, dt)[:t]
+        out["key"] = _randn((max(t, 1), hkv, d), gen, dev, dt)[:t]
+        out["value"] = _randn((max(t, 1), hkv, d), gen, dev, dt)[:t]
+    shape = (w.num_blocks, w.block_size, hkv, d)
+    out["key_cache"] = _randn(shape, gen, dev, dt)
+    out["value_cache"] = _randn(shape, gen, dev, dt)
+    return out
