@@ -1,0 +1,228 @@
+/*
+ * pa.h -- C ABI of the paged-KV attention step for GB300 (sm_103a).
+ *
+ * One engine step's attention over a flattened, variable-length batch that
+ * mixes prompt chunks and single-token decodes, against a paged KV cache:
+ *
+ *   pa_prepare_inputs  the per-step index tensors (request of each token,
+ *                      positions, query_start_loc, seq_lens, slot_mapping,
+ *                      logits_indices);
+ *   pa_cache_write     each new token's K and V copied to its cache slot;
+ *   pa_attention       causal grouped-query attention of every token over
+ *                      its own request's context, read through the block
+ *                      table.
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller allocates and owns every buffer.  The library
+ *     allocates nothing per call; its only device state is one status word
+ *     per device (a file-scope device variable).
+ *   - Pointers named "device" are CUDA device pointers (any memory a kernel
+ *     can dereference); sizes and scalars are host values.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  The
+ *     return value reports host-side argument checks and launch errors only:
+ *       PA_OK               queued;
+ *       PA_ERR_INVALID      an argument is malformed; nothing was launched;
+ *       PA_ERR_UNSUPPORTED  well-formed but outside what the kernels handle
+ *                           (e.g. head_dim not 64/128); nothing launched;
+ *       PA_ERR_CUDA         a CUDA runtime call failed.
+ *     Checks that need the data (a request with zero scheduled tokens, a
+ *     block id outside the pool, a logical block past the table's width, a
+ *     slot outside the pool, a wait inside a kernel that ran out) are made
+ *     by the kernels, which skip the offending item and record the failure
+ *     in the device status word; pa_get_status() reads and clears it.  A
+ *     failed check never turns into an out-of-bounds access.
+ *   - Ordering: calls on one stream run in order, so pa_cache_write followed
+ *     by pa_attention on the same stream reads the freshly written K/V.
+ *   - Index tensors are int32.  Q/K/V/output elements are bf16 or fp16.
+ *   - KV cache layout: separate K and V pools, each contiguous
+ *     [num_blocks][block_size][num_kv_heads][head_dim]; element
+ *     (slot, h, d) of a pool is at ((slot * num_kv_heads) + h) * head_dim + d
+ *     with slot = physical_block * block_size + offset.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so the header needs
+ * no CUDA include. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,
+    PA_ERR_CUDA = 2,
+    PA_ERR_UNSUPPORTED = 3,
+    PA_ERR_DEVICE_CHECK = 4,
+    PA_ERR_TIMEOUT = 5,
+    PA_ERR_WORKSPACE = 6
+} pa_status;
+
+typedef enum { PA_BF16 = 0, PA_FP16 = 1 } pa_dtype;
+
+/* Bits of the detail word returned by pa_get_status(). */
+enum {
+    PA_CHECK_EMPTY_REQUEST = 1u << 0,  /* num_scheduled_tokens[r] <= 0 */
+    PA_CHECK_TOKEN_COUNT = 1u << 1,    /* sum(num_scheduled_tokens) != num_tokens,
+                                          or query_start_loc[num_reqs] != num_tokens */
+    PA_CHECK_BLOCK_ID = 1u << 2,       /* block_table entry outside [0, num_blocks) */
+    PA_CHECK_LOGICAL_BLOCK = 1u << 3,  /* position / block_size >= max_blocks_per_req */
+    PA_CHECK_SLOT = 1u << 4,           /* slot_mapping entry >= num_blocks * block_size */
+    PA_CHECK_SEQ_LEN = 1u << 5,        /* seq_lens[r] < query length, qsl decreasing, or
+                                          a context wider than the table */
+    PA_CHECK_TIMEOUT = 1u << 6         /* a bounded wait inside a kernel ran out */
+};
+
+/*
+ * pa_prepare_inputs -- the step's index tensors.
+ *
+ * Defined by "Building the Batch", sections "How they are computed" and
+ * "Reading and writing the KV cache" (and its Go program), and by "vLLM's
+ * Model Runner", section "The two things this method returns":
+ *   query_start_loc[0] = 0, query_start_loc[r+1] = query_start_loc[r] + nst[r];
+ *   entries past num_reqs, up to qsl_capacity, hold num_tokens (so the
+ *   array never decreases);
+ *   for token t of request r at offset i (t = query_start_loc[r] + i):
+ *     req_indices[t]  = r
+ *     positions[t]    = num_computed_tokens[r] + i
+ *     slot_mapping[t] = block_table[r][pos / block_size] * block_size
+ *                       + pos % block_size
+ *   seq_lens[r]       = num_computed_tokens[r] + num_scheduled_tokens[r]
+ *   logits_indices[r] = query_start_loc[r+1] - 1
+ *
+ * Arguments (all device pointers are int32):
+ *   num_scheduled_tokens [num_reqs]   tokens each request runs this step (>= 1)
+ *   num_computed_tokens  [num_reqs]   tokens already in the cache (>= 0)
+ *   block_table [num_reqs][max_blocks_per_req] row-major physical block ids
+ *   block_size           tokens per cache block (> 0)
+ *   num_tokens           T = sum(num_scheduled_tokens), known to the host
+ *   num_blocks           physical blocks in the pool (ids are checked against it)
+ *   req_indices, positions, slot_mapping   outputs [num_tokens]
+ *   query_start_loc      output [qsl_capacity], qsl_capacity >= num_reqs + 1
+ *   seq_lens, logits_indices               outputs [num_reqs]
+ * Errors: PA_ERR_INVALID for negative sizes, a NULL buffer with a non-zero
+ * size, qsl_capacity < num_reqs + 1, or num_blocks * block_size >= 2^31;
+ * PA_ERR_UNSUPPORTED for more than 50,000 requests.
+ * Data checks (status word): PA_CHECK_EMPTY_REQUEST, PA_CHECK_TOKEN_COUNT,
+ * PA_CHECK_LOGICAL_BLOCK, PA_CHECK_BLOCK_ID; a token whose block fails a
+ * check gets slot_mapping = -1.
+ */
+pa_status pa_prepare_inputs(const int32_t *num_scheduled_tokens,
+                            const int32_t *num_computed_tokens,
+                            const int32_t *block_table, int32_t num_reqs,
+                            int32_t max_blocks_per_req, int32_t block_size,
+                            int32_t num_tokens, int32_t num_blocks,
+                            int32_t *req_indices, int32_t *positions,
+                            int32_t *slot_mapping, int32_t *query_start_loc,
+                            int32_t qsl_capacity, int32_t *seq_lens,
+                            int32_t *logits_indices, pa_stream_t stream);
+
+/*
+ * pa_cache_write -- scatter the step's new K and V into the cache.
+ *
+ * Defined by "Inside vLLM: Following One Request", the section on the write
+ * op (reshape_and_cache_flash): for token i, its key and value vectors are
+ * copied to slot slot_mapping[i].  A bit copy: no conversion, no scaling.
+ *
+ * Arguments:
+ *   key, value        device [num_tokens][num_kv_heads][head_dim] elements,
+ *                     token rows kv_token_stride elements apart (>= Hkv*D;
+ *                     lets K and V be views of a fused QKV projection)
+ *   key_cache, value_cache  device pools, layout above
+ *   slot_mapping      device int32 [num_tokens]; a negative slot means the
+ *                     token writes nothing (a padding row)
+ *   block_size, num_blocks  pool geometry (slots = num_blocks * block_size)
+ *   dtype             element type of all four buffers
+ * Errors: PA_ERR_INVALID for non-positive head counts/sizes, NULL buffers
+ * with num_tokens > 0, or kv_token_stride < num_kv_heads * head_dim.
+ * Data check: PA_CHECK_SLOT (that token is skipped).
+ */
+pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_stride,
+                         void *key_cache, void *value_cache,
+                         const int32_t *slot_mapping, int32_t num_tokens,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, pa_dtype dtype, pa_stream_t stream);
+
+/*
+ * pa_attention_workspace_size -- bytes of workspace that let pa_attention
+ * split every request's context into its preferred number of partitions.
+ * Any smaller workspace (including 0) is still correct: the kernel then uses
+ * longer partitions so the partial results fit (less parallelism for long
+ * contexts).  Arguments are host-known bounds of the step.
+ */
+size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens,
+                                   int32_t max_query_len, int32_t max_seq_len,
+                                   int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim);
+
+/*
+ * pa_attention -- paged causal grouped-query attention for the flat batch.
+ *
+ * Defined by "How vLLM Works Internally", section "How the Kernel Works"
+ * (look up the block table, fetch K from the scattered blocks, scores,
+ * softmax, weighted sum of V; the two-pass variant reduces partial softmax
+ * results across partitions) and "Inside vLLM: Following One Request", the
+ * read path (cu_seqlens_q = query_start_loc, seqused_k = seq_lens,
+ * physical block = block_table[logical block]).  For token t of request r
+ * at offset i, with n = query_start_loc[r+1] - query_start_loc[r] and
+ * position p = seq_lens[r] - n + i, and q head h reading kv head
+ * g = h / (num_q_heads / num_kv_heads):
+ *     out[t][h] = sum_{j <= p} softmax_j(scale * q[t][h] . K_r[j][g]) V_r[j][g]
+ * where K_r[j] is the cache entry at block_table[r][j / block_size],
+ * offset j % block_size.  Accumulation is fp32; the output is rounded once
+ * to the element type.
+ *
+ * Arguments:
+ *   q             device [num_tokens][num_q_heads][head_dim], contiguous
+ *   key_cache, value_cache  device pools (layout above), already holding
+ *                 this step's K/V (pa_cache_write first, same stream)
+ *   block_table   device int32 [num_reqs][max_blocks_per_req]
+ *   query_start_loc device int32 [num_reqs + 1]; seq_lens device int32 [num_reqs]
+ *   max_query_len, max_seq_len  host upper bounds of q length / seq_lens
+ *   head_dim      64 or 128; block_size 16; num_q_heads % num_kv_heads == 0
+ *   scale         softmax scale (usually 1/sqrt(head_dim))
+ *   out           device [num_tokens][num_q_heads][head_dim]
+ *   workspace     device scratch of workspace_bytes (256-byte aligned when
+ *                 non-zero); contents need no initialisation and are
+ *                 overwritten.  Calls that share a workspace must not
+ *                 overlap on the GPU.
+ * Errors: PA_ERR_INVALID (NULL buffers, bad sizes, misaligned buffers),
+ * PA_ERR_UNSUPPORTED (head_dim, block_size, head ratio, a pool too large for
+ * 32-bit slots).  Data checks: PA_CHECK_SEQ_LEN, PA_CHECK_BLOCK_ID (the
+ * request is skipped, or its block replaced by block 0), PA_CHECK_TIMEOUT.
+ */
+pa_status pa_attention(const void *q, const void *key_cache, const void *value_cache,
+                       const int32_t *block_table, int32_t max_blocks_per_req,
+                       const int32_t *query_start_loc, const int32_t *seq_lens,
+                       int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                       int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                       float scale, pa_dtype dtype, void *out, void *workspace,
+                       size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_get_status -- synchronise `stream`, then read and clear the current
+ * device's status word.  Returns PA_OK when no kernel check failed since the
+ * last call, PA_ERR_TIMEOUT when a bounded wait ran out, PA_ERR_DEVICE_CHECK
+ * for any other failed check, PA_ERR_CUDA if the synchronisation failed.
+ * When `detail` is non-NULL it receives the PA_CHECK_* bits.
+ */
+pa_status pa_get_status(pa_stream_t stream, uint32_t *detail);
+
+/* A static, human-readable name for a status code. */
+const char *pa_status_string(pa_status s);
+
+/* Number of the library's kernel launches queued by this thread since the
+ * last call to this function (returns and resets the count). */
+uint64_t pa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

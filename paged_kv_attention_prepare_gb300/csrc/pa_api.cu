@@ -1,0 +1,219 @@
+// The C ABI (include/pa.h): host-side argument checks, the per-device status
+// word, TMA descriptor encoding, and dispatch to the kernels.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pa_internal.cuh"
+
+// The one piece of device state the library keeps: a word of PA_CHECK_* bits
+// that kernels OR into when a data-dependent check fails.
+static __device__ unsigned int g_pa_status;
+
+namespace pa {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int *g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+thread_local uint64_t t_launches = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+unsigned int *status_word() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pa_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+void note_launch(int n) { t_launches += (uint64_t)n; }
+
+int num_sms() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv, int D,
+                     int box_rows) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return false;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_slots};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(pool), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+pa_status pa_prepare_inputs(const int32_t *num_scheduled_tokens, const int32_t *num_computed_tokens,
+                            const int32_t *block_table, int32_t num_reqs,
+                            int32_t max_blocks_per_req, int32_t block_size, int32_t num_tokens,
+                            int32_t num_blocks, int32_t *req_indices, int32_t *positions,
+                            int32_t *slot_mapping, int32_t *query_start_loc, int32_t qsl_capacity,
+                            int32_t *seq_lens, int32_t *logits_indices, pa_stream_t stream) {
+    if (num_reqs < 0 || num_tokens < 0 || block_size <= 0 || num_blocks < 0 ||
+        max_blocks_per_req < 0 || qsl_capacity < num_reqs + 1)
+        return PA_ERR_INVALID;
+    if (!query_start_loc) return PA_ERR_INVALID;
+    if (num_reqs > 0 && (!num_scheduled_tokens || !num_computed_tokens || !seq_lens ||
+                         !logits_indices || (max_blocks_per_req > 0 && !block_table)))
+        return PA_ERR_INVALID;
+    if (num_tokens > 0 && (!req_indices || !positions || !slot_mapping)) return PA_ERR_INVALID;
+    if ((int64_t)num_blocks * block_size >= (int64_t)INT32_MAX) return PA_ERR_INVALID;
+    return launch_prepare(num_scheduled_tokens, num_computed_tokens, block_table, num_reqs,
+                          max_blocks_per_req, block_size, num_tokens, num_blocks, req_indices,
+                          positions, slot_mapping, query_start_loc, qsl_capacity, seq_lens,
+                          logits_indices, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_stride,
+                         void *key_cache, void *value_cache, const int32_t *slot_mapping,
+                         int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                         pa_stream_t stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || (dtype != PA_BF16 && dtype != PA_FP16))
+        return PA_ERR_INVALID;
+    if (kv_token_stride < (int64_t)num_kv_heads * head_dim) return PA_ERR_INVALID;
+    if (num_tokens > 0 && (!key || !value || !key_cache || !value_cache || !slot_mapping))
+        return PA_ERR_INVALID;
+    if ((int64_t)num_kv_heads * head_dim > INT32_MAX / 2) return PA_ERR_UNSUPPORTED;
+    return launch_cache_write(key, value, kv_token_stride, key_cache, value_cache, slot_mapping,
+                              num_tokens, num_kv_heads * head_dim,
+                              (int64_t)num_blocks * block_size,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                                   int32_t max_seq_len, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim) {
+    if (num_reqs <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    return decode_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len, num_q_heads,
+                                 num_kv_heads, head_dim);
+}
+
+pa_status pa_attention(const void *q, const void *key_cache, const void *value_cache,
+                       const int32_t *block_table, int32_t max_blocks_per_req,
+                       const int32_t *query_start_loc, const int32_t *seq_lens, int32_t num_reqs,
+                       int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, int32_t num_blocks, float scale, pa_dtype dtype,
+                       void *out, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0 ||
+        num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || max_blocks_per_req < 0 || (dtype != PA_BF16 && dtype != PA_FP16))
+        return PA_ERR_INVALID;
+    if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return PA_ERR_INVALID;
+    if (num_tokens == 0 || num_reqs == 0) return PA_OK;
+    if (!q || !key_cache || !value_cache || !block_table || !query_start_loc || !seq_lens || !out)
+        return PA_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(key_cache, 16) ||
+        !aligned(value_cache, 16))
+        return PA_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size != 16) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * block_size >= (int64_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (num_blocks == 0 || max_blocks_per_req == 0) return PA_ERR_INVALID;
+    AttnArgs a;
+    a.q = q;
+    a.kc = key_cache;
+    a.vc = value_cache;
+    a.bt = block_table;
+    a.MB = max_blocks_per_req;
+    a.qsl = query_start_loc;
+    a.seq_lens = seq_lens;
+    a.R = num_reqs;
+    a.T = num_tokens;
+    a.max_q = max_query_len;
+    a.max_seq = max_seq_len;
+    a.Hq = num_q_heads;
+    a.Hkv = num_kv_heads;
+    a.D = head_dim;
+    a.bs = block_size;
+    a.NB = num_blocks;
+    a.scale = scale;
+    a.dtype = dtype;
+    a.out = out;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_get_status(pa_stream_t stream, uint32_t *detail) {
+    if (detail) *detail = 0;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_pa_status, sizeof v) != cudaSuccess) return PA_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_pa_status, &zero, sizeof zero) != cudaSuccess) return PA_ERR_CUDA;
+    if (detail) *detail = v;
+    if (!v) return PA_OK;
+    return (v & PA_CHECK_TIMEOUT) ? PA_ERR_TIMEOUT : PA_ERR_DEVICE_CHECK;
+}
+
+const char *pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID: return "invalid argument";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or type";
+        case PA_ERR_DEVICE_CHECK: return "a device-side data check failed";
+        case PA_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+        case PA_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+uint64_t pa_launch_count(void) {
+    const uint64_t n = t_launches;
+    t_launches = 0;
+    return n;
+}
+
+}  // extern "C"

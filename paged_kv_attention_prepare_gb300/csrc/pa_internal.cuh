@@ -1,0 +1,181 @@
+// Internal helpers shared by the library's translation units: launch
+// plumbing, the status-word bits, and thin inline-PTX wrappers for mbarriers,
+// TMA bulk-tensor copies and bounded waits on sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+// Device address of this device's status word (set up once per device).
+unsigned int *status_word();
+// Count one kernel launch queued by the calling thread.
+void note_launch(int n = 1);
+int num_sms();
+
+pa_status launch_prepare(const int32_t *nst, const int32_t *nct, const int32_t *bt,
+                         int32_t R, int32_t MB, int32_t bs, int32_t T, int32_t NB,
+                         int32_t *req, int32_t *pos, int32_t *slot, int32_t *qsl,
+                         int32_t qsl_cap, int32_t *seq_lens, int32_t *logits,
+                         cudaStream_t stream);
+
+pa_status launch_cache_write(const void *key, const void *value, int64_t stride_elems,
+                             void *kc, void *vc, const int32_t *slots, int32_t T,
+                             int32_t row_elems, int64_t num_slots, cudaStream_t stream);
+
+struct AttnArgs {
+    const void *q;
+    const void *kc, *vc;
+    const int32_t *bt;
+    int32_t MB;
+    const int32_t *qsl, *seq_lens;
+    int32_t R, T, max_q, max_seq, Hq, Hkv, D, bs, NB;
+    float scale;
+    pa_dtype dtype;
+    void *out;
+    void *ws;
+    size_t ws_bytes;
+};
+
+size_t decode_workspace_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq,
+                             int32_t Hq, int32_t Hkv, int32_t D);
+pa_status launch_decode(const AttnArgs &a, cudaStream_t stream);
+
+// Encode a 3-D TMA map over one pool viewed as [NB*bs][Hkv][D] elements with a
+// box of D x 1 kv head x `box_rows` slots.
+bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv, int D,
+                     int box_rows);
+
+// ---------------------------------------------------------------------------
+// Device side
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void flag(unsigned int *status, unsigned int bit) {
+    atomicOr(status, bit);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Upper bound for any single wait inside a kernel.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after the
+// time limit (the caller records the timeout and winds down).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// 3-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Element traits: packed 16-bit elements -> floats, and two floats -> a
+// packed pair rounded to nearest even.
+template <typename T> struct Elt;
+
+template <> struct Elt<__nv_bfloat16> {
+    __device__ __forceinline__ static void unpack2(uint32_t w, float &a, float &b) {
+        a = __uint_as_float(w << 16);
+        b = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ __forceinline__ static uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+template <> struct Elt<__half> {
+    __device__ __forceinline__ static void unpack2(uint32_t w, float &a, float &b) {
+        __half2 h = *reinterpret_cast<const __half2 *>(&w);
+        float2 x = __half22float2(h);
+        a = x.x;
+        b = x.y;
+    }
+    __device__ __forceinline__ static uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+}  // namespace pa
+
+#define PA_TRY_CUDA(expr)                                  \
+    do {                                                   \
+        cudaError_t e_ = (expr);                           \
+        if (e_ != cudaSuccess) return PA_ERR_CUDA;         \
+    } while (0)
