@@ -1,0 +1,191 @@
+"""Paged-KV attention step for GB300: Python binding of ``libpa.so``.
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+their dtype, device and layout, and passes raw pointers, sizes and the
+stream to the C ABI in ``include/pa.h``.  Every step runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback, and using the package
+without the built library raises immediately.
+
+Functions carry the C names: ``pa_prepare_inputs``, ``pa_cache_write``,
+``pa_attention_workspace_size``, ``pa_attention``, ``pa_get_status``,
+``pa_launch_count``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_CUDA, PA_ERR_UNSUPPORTED = 0, 1, 2, 3
+PA_ERR_DEVICE_CHECK, PA_ERR_TIMEOUT, PA_ERR_WORKSPACE = 4, 5, 6
+PA_BF16, PA_FP16 = 0, 1
+
+CHECK_BITS = {
+    "empty_request": 1 << 0, "token_count": 1 << 1, "block_id": 1 << 2,
+    "logical_block": 1 << 3, "slot": 1 << 4, "seq_len": 1 << 5, "timeout": 1 << 6,
+}
+
+_DTYPES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
+_lock = threading.Lock()
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_status_string(status)} ({status})")
+
+
+def build(force: bool = False) -> str:
+    """Compile ``libpa.so`` (nvcc, sm_103a) next to this file."""
+    from .builder import build as _build
+    return _build(force=force)
+
+
+def lib():
+    """The loaded ``libpa.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -m paged_kv_attention_prepare_gb300.builder)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            L.pa_prepare_inputs.restype = ctypes.c_int
+            L.pa_prepare_inputs.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                            i32, vp, vp, vp]
+            L.pa_cache_write.restype = ctypes.c_int
+            L.pa_cache_write.argtypes = [vp, vp, i64, vp, vp, vp, i32, i32, i32, i32, i32,
+                                         ctypes.c_int, vp]
+            L.pa_attention_workspace_size.restype = sz
+            L.pa_attention_workspace_size.argtypes = [i32] * 7
+            L.pa_attention.restype = ctypes.c_int
+            L.pa_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+                                       i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, vp, sz, vp]
+            L.pa_get_status.restype = ctypes.c_int
+            L.pa_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+            L.pa_status_string.restype = ctypes.c_char_p
+            L.pa_status_string.argtypes = [ctypes.c_int]
+            L.pa_launch_count.restype = ctypes.c_uint64
+            L.pa_launch_count.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _status_string(s: int) -> str:
+    try:
+        return lib().pa_status_string(int(s)).decode()
+    except Exception:  # pragma: no cover - only while reporting another error
+        return "status"
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, contiguous=True):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc: int, what: str):
+    if rc != PA_OK:
+        raise PAError(rc, what)
+
+
+def pa_prepare_inputs(num_scheduled_tokens, num_computed_tokens, block_table, block_size,
+                      num_tokens, num_blocks, req_indices, positions, slot_mapping,
+                      query_start_loc, seq_lens, logits_indices, stream=None):
+    """Index tensors of one step into caller-allocated int32 CUDA tensors."""
+    i32 = torch.int32
+    R = num_scheduled_tokens.shape[0]
+    rc = lib().pa_prepare_inputs(
+        _dev(num_scheduled_tokens, "num_scheduled_tokens", i32),
+        _dev(num_computed_tokens, "num_computed_tokens", i32),
+        _dev(block_table, "block_table", i32), R, block_table.shape[1] if R else 0,
+        int(block_size), int(num_tokens), int(num_blocks),
+        _dev(req_indices, "req_indices", i32), _dev(positions, "positions", i32),
+        _dev(slot_mapping, "slot_mapping", i32), _dev(query_start_loc, "query_start_loc", i32),
+        query_start_loc.shape[0], _dev(seq_lens, "seq_lens", i32),
+        _dev(logits_indices, "logits_indices", i32), _stream(stream))
+    _check(rc, "pa_prepare_inputs")
+
+
+def pa_cache_write(key, value, key_cache, value_cache, slot_mapping, num_blocks=None,
+                   stream=None):
+    """Scatter key/value [T, Hkv, D] (token stride may exceed Hkv*D) into the
+    [NB, bs, Hkv, D] pools at slot_mapping."""
+    T, hkv, d = key.shape
+    if key.stride(1) != d or key.stride(2) != 1 or value.stride() != key.stride():
+        raise ValueError("key/value rows must be [Hkv, D]-contiguous with equal strides")
+    dt = _DTYPES.get(key.dtype)
+    if dt is None or value.dtype != key.dtype or key_cache.dtype != key.dtype:
+        raise TypeError("key, value and caches must share a bf16/fp16 dtype")
+    nb, bs = key_cache.shape[0], key_cache.shape[1]
+    rc = lib().pa_cache_write(
+        _dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
+        int(key.stride(0)) if T else hkv * d, _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(slot_mapping, "slot_mapping", torch.int32), T,
+        hkv, d, bs, nb if num_blocks is None else int(num_blocks), dt, _stream(stream))
+    _check(rc, "pa_cache_write")
+
+
+def pa_attention_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len, num_q_heads,
+                                num_kv_heads, head_dim) -> int:
+    return int(lib().pa_attention_workspace_size(num_reqs, num_tokens, max_query_len,
+                                                 max_seq_len, num_q_heads, num_kv_heads,
+                                                 head_dim))
+
+
+def pa_attention(q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
+                 max_query_len, max_seq_len, scale, out, workspace=None, stream=None):
+    """Paged causal GQA attention: q [T, Hq, D] -> out [T, Hq, D]."""
+    T, hq, d = q.shape
+    nb, bs, hkv, _ = key_cache.shape
+    R = seq_lens.shape[0]
+    dt = _DTYPES.get(q.dtype)
+    if dt is None or key_cache.dtype != q.dtype or out.dtype != q.dtype:
+        raise TypeError("q, caches and out must share a bf16/fp16 dtype")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None and workspace.numel() > 0:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().pa_attention(
+        _dev(q, "q"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _dev(query_start_loc, "query_start_loc", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), R, T, int(max_query_len), int(max_seq_len),
+        hq, hkv, d, bs, nb, float(scale), dt, _dev(out, "out"), ws_ptr, ws_bytes,
+        _stream(stream))
+    _check(rc, "pa_attention")
+
+
+def pa_get_status(stream=None):
+    """(status, detail bits): synchronises the stream, reads and clears the
+    device status word."""
+    detail = ctypes.c_uint32(0)
+    rc = lib().pa_get_status(_stream(stream), ctypes.byref(detail))
+    return int(rc), int(detail.value)
+
+
+def pa_launch_count() -> int:
+    return int(lib().pa_launch_count())
+
+
+def check_bits(detail: int) -> set:
+    return {k for k, b in CHECK_BITS.items() if detail & b}

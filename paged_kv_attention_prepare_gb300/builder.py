@@ -4,7 +4,7 @@ Translation units compile in parallel; the link is a plain shared-library
 link (no relocatable device code).  Re-running is a no-op while the library
 is newer than every source and header.
 
-    python -m paged_kv_attention_prepare_gb300.build [--force] [--ptxas-info]
+    python -m paged_kv_attention_prepare_gb300.builder [--force] [--ptxas-info]
 """
 
 from __future__ import annotations

@@ -98,9 +98,11 @@ struct Walker {
         nsplit = 0;
         items = 0;
         if (r < p->R) {
-            n = p->qsl[r + 1] - p->qsl[r];
+            const int a = p->qsl[r], b = p->qsl[r + 1];
+            n = b - a;
             L = p->seq_lens[r];
-            const bool sane = n >= 0 && L >= n && (L + kPage - 1) / kPage <= p->MB;
+            const bool sane = a >= 0 && b <= p->T && n >= 0 && L >= n &&
+                              (L + kPage - 1) / kPage <= p->MB;
             if (!sane) flag(p->status, PA_CHECK_SEQ_LEN);
             if (sane && n >= 1 && n <= p->tau) {
                 nchunks = (n * p->G + RPI - 1) / RPI;
@@ -261,9 +263,12 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         for (int k = 0; k < kCandidates; ++k) local[k] = 0;
         if (p.p_min < kSingle) {
             for (int r = tid; r < p.R; r += kThreads) {
-                const int n = p.qsl[r + 1] - p.qsl[r];
+                const int a = p.qsl[r], b = p.qsl[r + 1];
+                const int n = b - a;
                 const int L = p.seq_lens[r];
-                if (n < 1 || n > p.tau || L < n || (L + kPage - 1) / kPage > p.MB) continue;
+                if (a < 0 || b > p.T || n < 1 || n > p.tau || L < n ||
+                    (L + kPage - 1) / kPage > p.MB)
+                    continue;
                 const long long per = (long long)p.Hkv * ((n * p.G + RPI - 1) / RPI);
 #pragma unroll
                 for (int k = 0; k < kCandidates; ++k) {

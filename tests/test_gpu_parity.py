@@ -1,0 +1,271 @@
+"""CUDA path vs. the oracle, through the C ABI.
+
+Indices and cache contents must match bit for bit; attention within the
+stated bound: max |gpu - oracle| <= 1e-2 (bf16/fp16 output, fp32
+accumulation, oracle in fp64)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_prepare_gb300 as pa
+import workloads
+from gpu_step import run_step, to_dev
+from helpers import golden, to_bits
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+IDX_KEYS = ("req_indices", "positions", "slot_mapping", "query_start_loc", "seq_lens",
+            "logits_indices")
+
+
+@pytest.fixture(autouse=True)
+def clean_status():
+    pa.pa_get_status()
+    yield
+
+
+def _oracle_step(w, vals, tokens=None, qsl_capacity=None):
+    host = {k: v.cpu() for k, v in vals.items()}
+    return oracle.step(w, host, qsl_capacity=qsl_capacity, tokens=tokens)
+
+
+def _check_indices(res, idx):
+    for k in IDX_KEYS:
+        np.testing.assert_array_equal(res[k], idx[k], err_msg=k)
+
+
+def _check_attention(res, ref, tokens=None):
+    got = res["out"].float().cpu().numpy().astype(np.float64)
+    if tokens is not None:
+        got, ref = got[tokens], ref[tokens]
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max() if got.size else 0.0
+    assert err <= ATOL, f"max abs error {err}"
+    return err
+
+
+# ---------------------------------------------------------------------------
+# Small workloads: everything compared in full
+# ---------------------------------------------------------------------------
+
+def test_tiny_step_full_parity():
+    w = workloads.tiny()
+    vals = workloads.make_values(w, 0)
+    res = run_step(w, vals, qsl_capacity=8)
+    idx, kc, vc, ref = _oracle_step(w, vals, qsl_capacity=8)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_indices(res, idx)
+    np.testing.assert_array_equal(to_bits(res["key_cache"]), kc)
+    np.testing.assert_array_equal(to_bits(res["value_cache"]), vc)
+    _check_attention(res, ref)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_small_steps(seed):
+    kw = dict(max_computed=1500 if seed % 3 else 200)
+    if seed % 4 == 1:
+        kw["long_prefill"] = 70
+    w = workloads.random_case(seed, **kw)
+    vals = workloads.make_values(w, seed, fused_qkv=bool(seed % 2))
+    res = run_step(w, vals)
+    host = {k: v.cpu() for k, v in vals.items()}
+    host["key"] = host["key"].contiguous()
+    host["value"] = host["value"].contiguous()
+    idx, kc, vc, ref = oracle.step(w, host)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_indices(res, idx)
+    np.testing.assert_array_equal(to_bits(res["key_cache"]), kc)
+    np.testing.assert_array_equal(to_bits(res["value_cache"]), vc)
+    _check_attention(res, ref)
+
+
+@pytest.mark.parametrize("ws", ["none", "tiny", "default"])
+def test_partition_choice_does_not_change_result(ws):
+    # Long contexts: the kernel picks its partition length from the workspace
+    # it is given (no workspace: one partition per request).
+    w = workloads.random_case(77, max_reqs=5, max_computed=3000, head_dim=128, dtype="bf16",
+                              group=4, num_kv_heads=2)
+    vals = workloads.make_values(w, 77)
+    nbytes = {"none": 0, "tiny": 64 * 1024, "default": None}[ws]
+    res = run_step(w, vals, workspace_bytes=nbytes)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    _check_attention(res, ref)
+
+
+@pytest.mark.parametrize("d,dtype,group", [(64, "bf16", 1), (64, "fp16", 8), (128, "fp16", 2),
+                                           (128, "bf16", 8), (128, "bf16", 3)])
+def test_head_shapes(d, dtype, group):
+    w = workloads.random_case(300 + d + group, max_reqs=4, max_computed=700, head_dim=d,
+                              dtype=dtype, group=group, num_kv_heads=2, long_prefill=21)
+    vals = workloads.make_values(w, 5)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    _check_attention(res, ref)
+
+
+def test_golden_examples_on_gpu():
+    # The pages' worked index examples, block size 4, through the CUDA kernel.
+    for name in ("prep_go_program_bs4.json", "block_table_nano_vllm_bs4.json"):
+        g = golden(name)["inputs"]
+        nst = np.asarray(g["num_scheduled_tokens"], np.int32)
+        nct = np.asarray(g["num_computed_tokens"], np.int32)
+        bt = np.asarray(g["block_table"], np.int32)
+        t = int(nst.sum())
+        want = oracle.prepare_inputs(nst, nct, bt, g["block_size"], t, g["num_blocks"])
+        outs = [torch.empty(n, dtype=torch.int32, device="cuda")
+                for n in (t, t, t, len(nst) + 1, len(nst), len(nst))]
+        pa.pa_prepare_inputs(to_dev(nst), to_dev(nct), to_dev(bt), g["block_size"], t,
+                             g["num_blocks"], *outs)
+        for k, o in zip(IDX_KEYS, outs):
+            np.testing.assert_array_equal(o.cpu().numpy(), want[k], err_msg=f"{name}:{k}")
+    for c in golden("prep_exercises.json")["cases"]:
+        nst = np.asarray(c["num_scheduled_tokens"], np.int32)
+        t = int(nst.sum())
+        outs = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (t, t, t, 2, 1, 1)]
+        pa.pa_prepare_inputs(to_dev(nst), to_dev(np.asarray(c["num_computed_tokens"], np.int32)),
+                             to_dev(np.asarray(c["block_table"], np.int32)), c["block_size"], t,
+                             c["num_blocks"], *outs)
+        assert outs[2].cpu().tolist() == c["slot_mapping_by_hand"]
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: indices and written rows in full, attention sampled
+# ---------------------------------------------------------------------------
+
+def _sample_tokens(w, k, seed):
+    rng = np.random.default_rng(seed)
+    starts = np.concatenate([[0], np.cumsum(w.num_scheduled_tokens)])
+    picks = {int(starts[0]), int(starts[-1] - 1)}
+    picks |= set(rng.choice(w.num_tokens, size=min(k, w.num_tokens), replace=False).tolist())
+    # every request boundary kind: longest context, shortest, multi-token chunk ends
+    ctx = w.context_lens
+    for r in (int(np.argmax(ctx)), int(np.argmin(ctx)), int(np.argmax(w.num_scheduled_tokens))):
+        picks.add(int(starts[r + 1] - 1))
+        picks.add(int(starts[r]))
+    return np.array(sorted(picks), np.int32)
+
+
+@pytest.mark.parametrize("name", ["decode", "mixed", "mha", "shared_prefix"])
+def test_full_size_workloads(name):
+    w = workloads.named(name)
+    vals = workloads.make_values(w, 1, device="cuda")
+    res = run_step(w, vals)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    tokens = _sample_tokens(w, 24, 3)
+    idx, kc, vc, ref = _oracle_step(w, vals, tokens=tokens)
+    _check_indices(res, idx)
+    # written rows bit-exact; a sample of the untouched pool unchanged
+    kb, vb = to_bits(res["key_cache"]), to_bits(res["value_cache"])
+    slots = idx["slot_mapping"]
+    flat = lambda a: a.reshape(-1, w.num_kv_heads, w.head_dim)
+    np.testing.assert_array_equal(flat(kb)[slots], flat(kc)[slots])
+    np.testing.assert_array_equal(flat(vb)[slots], flat(vc)[slots])
+    rng = np.random.default_rng(0)
+    blocks = rng.choice(w.num_blocks, size=min(256, w.num_blocks), replace=False)
+    np.testing.assert_array_equal(kb[blocks], kc[blocks])
+    np.testing.assert_array_equal(vb[blocks], vc[blocks])
+    _check_attention(res, ref, tokens)
+    del vals, res
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# Edge cases and device-side checks (host-made bad inputs; every access stays
+# in bounds because the kernels check before they read)
+# ---------------------------------------------------------------------------
+
+def test_empty_step_is_a_no_op():
+    e = torch.empty(0, dtype=torch.int32, device="cuda")
+    qsl = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    pa.pa_prepare_inputs(e, e, torch.empty(0, 1, dtype=torch.int32, device="cuda"), 16, 0, 4,
+                         e, e, e, qsl, e, e)
+    assert qsl.cpu().tolist() == [0, 0, 0, 0]
+    q = torch.empty(0, 4, 64, dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16, device="cuda")
+    kv = torch.empty(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    pa.pa_cache_write(kv, kv, pool, pool.clone(), e)
+    pa.pa_attention(q, pool, pool, torch.zeros(0, 1, dtype=torch.int32, device="cuda"), qsl[:1],
+                    e, 0, 0, 0.125, q)
+    assert pa.pa_get_status() == (pa.PA_OK, 0)
+
+
+def test_negative_slot_skips_and_out_of_pool_slot_is_flagged():
+    pool = torch.zeros(2, 16, 1, 64, dtype=torch.float16, device="cuda")
+    key = torch.ones(3, 1, 64, dtype=torch.float16, device="cuda")
+    slots = torch.tensor([-1, 5, 32], dtype=torch.int32, device="cuda")
+    kc, vc = pool.clone(), pool.clone()
+    pa.pa_cache_write(key, key, kc, vc, slots)
+    st, detail = pa.pa_get_status()
+    assert st == pa.PA_ERR_DEVICE_CHECK and pa.check_bits(detail) == {"slot"}
+    flat = kc.view(-1, 64)
+    assert (flat[5] == 1).all() and (flat[:5] == 0).all() and (flat[6:] == 0).all()
+
+
+@pytest.mark.parametrize("bad", ["block_id", "empty_request", "token_count", "logical_block"])
+def test_prep_device_checks(bad):
+    nst = np.array([2, 3], np.int32)
+    nct = np.array([5, 0], np.int32)
+    bt = np.array([[0, 1], [2, -1]], np.int32)
+    t = 5
+    if bad == "block_id":
+        bt[1, 0] = 9
+    elif bad == "empty_request":
+        nst[0], t = 0, 3
+    elif bad == "token_count":
+        t = 7
+    elif bad == "logical_block":
+        nct[0] = 40
+    outs = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (t, t, t, 3, 2, 2)]
+    pa.pa_prepare_inputs(to_dev(nst), to_dev(nct), to_dev(bt), 16, t, 4, *outs)
+    st, detail = pa.pa_get_status()
+    assert st == pa.PA_ERR_DEVICE_CHECK
+    assert bad in pa.check_bits(detail)
+
+
+def test_attention_flags_bad_block_and_bad_lengths():
+    w = workloads.random_case(3, max_reqs=3, max_computed=100, head_dim=64)
+    vals = workloads.make_values(w, 3)
+    res = run_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    q = vals["q"].cuda()
+    bt = to_dev(w.block_table.copy())
+    bt[0, 0] = w.num_blocks + 5                      # outside the pool
+    o = torch.empty_like(q)
+    qsl = torch.from_numpy(res["query_start_loc"]).cuda()
+    sl = torch.from_numpy(res["seq_lens"]).cuda()
+    pa.pa_attention(q, res["key_cache"], res["value_cache"], bt, qsl, sl, w.max_query_len,
+                    w.max_seq_len, w.scale, o)
+    st, detail = pa.pa_get_status()
+    assert st == pa.PA_ERR_DEVICE_CHECK and "block_id" in pa.check_bits(detail)
+    sl_bad = sl.clone()
+    sl_bad[0] = w.max_blocks_per_req * 16 + 1          # wider than its table
+    pa.pa_attention(q, res["key_cache"], res["value_cache"], to_dev(w.block_table), qsl, sl_bad,
+                    w.max_query_len, w.max_seq_len + 32, w.scale, o)
+    st, detail = pa.pa_get_status()
+    assert st == pa.PA_ERR_DEVICE_CHECK and "seq_len" in pa.check_bits(detail)
+
+
+def test_host_side_rejections():
+    q = torch.zeros(2, 4, 96, dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros(4, 16, 2, 96, dtype=torch.bfloat16, device="cuda")
+    i = torch.zeros(2, dtype=torch.int32, device="cuda")
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_attention(q, pool, pool, torch.zeros(2, 1, dtype=torch.int32, device="cuda"),
+                        torch.tensor([0, 1, 2], dtype=torch.int32, device="cuda"), i, 1, 1,
+                        0.1, q)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+    with pytest.raises(TypeError):
+        pa.pa_attention(q.cpu(), pool, pool, i, i, i, 1, 1, 0.1, q)
+
+
+def test_launch_count():
+    w = workloads.tiny()
+    vals = workloads.make_values(w, 0)
+    pa.pa_launch_count()
+    run_step(w, vals)
+    assert pa.pa_launch_count() >= 3

@@ -1,0 +1,97 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/pa.h declares, and its host-side checks reject bad arguments before
+any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_attention_prepare_gb300 as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("pa_prepare_inputs", "pa_cache_write", "pa_attention",
+              "pa_attention_workspace_size", "pa_get_status", "pa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(pa.build())
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    for s in range(7):
+        assert pa.lib().pa_status_string(s)
+
+
+FAKE = ctypes.c_void_p(0x100000)  # never dereferenced: the checks return first
+
+
+def test_attention_rejects_unsupported_head_dim():
+    L = pa.lib()
+    rc = L.pa_attention(FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 2, 1, 16, 4, 2, 96, 16, 8,
+                        0.1, pa.PA_BF16, FAKE, None, 0, None)
+    assert rc == pa.PA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("case", ["block_size", "ratio", "null", "ws_align", "neg"])
+def test_attention_rejects_bad_arguments(case):
+    L = pa.lib()
+    args = dict(bs=16, hq=4, hkv=2, q=FAKE, ws=None, wsb=0, R=2)
+    if case == "block_size":
+        args["bs"] = 32
+    elif case == "ratio":
+        args["hq"] = 5
+    elif case == "null":
+        args["q"] = None
+    elif case == "ws_align":
+        args["ws"], args["wsb"] = ctypes.c_void_p(0x100004), 64
+    elif case == "neg":
+        args["R"] = -1
+    rc = L.pa_attention(args["q"], FAKE, FAKE, FAKE, 4, FAKE, FAKE, args["R"], 2, 1, 16,
+                        args["hq"], args["hkv"], 64, args["bs"], 8, 0.1, pa.PA_BF16, FAKE,
+                        args["ws"], args["wsb"], None)
+    expect = pa.PA_ERR_UNSUPPORTED if case in ("block_size", "ratio") else pa.PA_ERR_INVALID
+    assert rc == expect
+
+
+def test_prepare_rejects_small_qsl_capacity_and_huge_pool():
+    L = pa.lib()
+    assert L.pa_prepare_inputs(FAKE, FAKE, FAKE, 3, 2, 16, 5, 8, FAKE, FAKE, FAKE, FAKE, 3,
+                               FAKE, FAKE, None) == pa.PA_ERR_INVALID
+    assert L.pa_prepare_inputs(FAKE, FAKE, FAKE, 3, 2, 16, 5, 1 << 28, FAKE, FAKE, FAKE, FAKE,
+                               4, FAKE, FAKE, None) == pa.PA_ERR_INVALID
+
+
+def test_cache_write_rejects_short_stride_and_bad_dtype():
+    L = pa.lib()
+    assert L.pa_cache_write(FAKE, FAKE, 100, FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, pa.PA_BF16,
+                            None) == pa.PA_ERR_INVALID
+    assert L.pa_cache_write(FAKE, FAKE, 128, FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, 7,
+                            None) == pa.PA_ERR_INVALID
+
+
+def test_workspace_size_grows_with_context():
+    small = pa.pa_attention_workspace_size(256, 256, 1, 512, 32, 8, 128)
+    big = pa.pa_attention_workspace_size(256, 256, 1, 4096, 32, 8, 128)
+    assert 0 < small < big
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    t = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(TypeError):
+        pa.pa_prepare_inputs(t, t, t.view(4, 1), 16, 4, 4, t, t, t, t, t, t)
