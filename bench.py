@@ -1,0 +1,411 @@
+"""Benchmark of one paged-KV attention step (index build + cache write +
+paged attention) on synthetic workloads shaped like the pages' examples.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints one JSON line.  A step is the whole path over one batch: the three
+C-ABI calls on inputs already resident in HBM.  The L2 is flushed (a 256 MB
+write) between timed steps, outside the timed events.  ``e2e`` repeats the
+step through the same public calls with the step's inputs copied from pinned
+host memory and the output copied back inside the timed region.
+
+Under torchrun every rank runs an independent replica (its own pool and
+requests, seeded by rank): the path has no exchange step.  Timing is the max
+over ranks; ``value`` is the tokens all ranks processed per second.
+
+``--impl reference`` times the CPU oracle (the reference arm here) on a
+bounded sample of the same workload, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged-attn step tokens/s"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=sorted(workloads.NAMED))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def kv_bytes(w) -> tuple[int, int]:
+    """Algorithmic bytes of one attention call: K/V context read (logical and
+    unique-physical), plus q read, out write and the block-table entries."""
+    elt = 2
+    extra = (w.num_tokens * w.num_q_heads * w.head_dim * elt * 2
+             + int(np.ceil(w.context_lens / w.block_size).sum()) * 4)
+    logical = w.kv_read_bytes() + extra
+    unique = w.kv_unique_bytes() + extra
+    return logical, unique
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("decode.cu", "pa_internal.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_attention_prepare_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from a committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"paged_decode_kernel_{workload}.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not hm or hm.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline, and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, vals_host, seconds: float):
+    """Time the oracle on a bounded sample: the full index build and cache
+    write, and attention for a growing random subset of tokens until about
+    ``seconds`` of CPU work.  Returns (tokens/s for the whole step, threads,
+    description)."""
+    import oracle
+    nthreads = oracle.num_cpus()
+    t0 = time.perf_counter()
+    idx = oracle.prepare_inputs(w.num_scheduled_tokens, w.num_computed_tokens, w.block_table,
+                                w.block_size, w.num_tokens, w.num_blocks)
+    t1 = time.perf_counter()
+    kc, vc, _ = oracle.cache_write(vals_host["key"], vals_host["value"], vals_host["key_cache"],
+                                   vals_host["value_cache"], idx["slot_mapping"], w.num_kv_heads,
+                                   w.head_dim, w.block_size, w.num_blocks)
+    t2 = time.perf_counter()
+    rng = np.random.default_rng(0)
+    n, spent, done = max(1, nthreads), 0.0, 0
+    order = rng.permutation(w.num_tokens)
+    while done < w.num_tokens and spent < seconds:
+        take = np.sort(order[done:done + n])
+        a = time.perf_counter()
+        oracle.attention(vals_host["q"], kc, vc, w.block_table, idx["query_start_loc"],
+                         idx["seq_lens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
+                         w.block_size, w.num_blocks, w.scale, w.dtype, tokens=take,
+                         num_threads=nthreads)
+        spent += time.perf_counter() - a
+        done += len(take)
+        n = min(n * 2, w.num_tokens - done) if spent < seconds / 4 else n
+    per_token = spent / done
+    step_s = (t1 - t0) + (t2 - t1) + per_token * w.num_tokens
+    desc = (f"index build + cache write on all {w.num_tokens} tokens; attention on {done} "
+            f"random tokens ({spent:.1f} s), scaled to the step's {w.num_tokens} tokens")
+    return w.num_tokens / step_s, nthreads, desc
+
+
+def host_values(vals):
+    return {k: v.detach().cpu() for k, v in vals.items()}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.named(args.workload)
+    vals = host_values(workloads.make_values(w, 1, device="cpu"))
+    budget = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, vals, budget / 4)
+    vals_s, threads, desc = [], 0, ""
+    for _ in range(args.steps):
+        v, threads, desc = oracle_sample(w, vals, budget)
+        vals_s.append(v)
+    value = float(np.median(vals_s))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.num_tokens / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "num_reqs": w.num_reqs, "num_tokens": w.num_tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# The CUDA path
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from paged_kv_attention_prepare_gb300.builder import build
+    build()
+    import paged_kv_attention_prepare_gb300 as pa
+
+    dev = torch.device("cuda", local)
+    w = workloads.named(args.workload, None if rank == 0 else 1000 + rank)
+    vals = workloads.make_values(w, 1 + rank, device=dev)
+    i32 = torch.int32
+    R, T = w.num_reqs, w.num_tokens
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    nst, nct, bt = up(w.num_scheduled_tokens), up(w.num_computed_tokens), up(w.block_table)
+    req, pos, slot = (torch.empty(T, dtype=i32, device=dev) for _ in range(3))
+    qsl = torch.empty(R + 1, dtype=i32, device=dev)
+    sl, li = torch.empty(R, dtype=i32, device=dev), torch.empty(R, dtype=i32, device=dev)
+    q, key, value = vals["q"], vals["key"], vals["value"]
+    kc, vc = vals["key_cache"], vals["value_cache"]
+    out = torch.empty_like(q)
+    ws_bytes = pa.pa_attention_workspace_size(R, T, w.max_query_len, w.max_seq_len,
+                                              w.num_q_heads, w.num_kv_heads, w.head_dim)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(nst=nst, nct=nct, bt=bt, q=q, key=key, value=value):
+        pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot, qsl,
+                             sl, li)
+        pa.pa_cache_write(key, value, kc, vc, slot)
+        a0.record(stream)
+        pa.pa_attention(q, kc, vc, bt, qsl, sl, w.max_query_len, w.max_seq_len, w.scale, out, ws)
+        a1.record(stream)
+
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    status, detail = pa.pa_get_status()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device checks failed during warm-up: {pa.check_bits(detail)}")
+
+    # ---- timed region: device-resident inputs
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    pa.pa_launch_count()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            s0, s1, b0, b1 = ev[k]
+            s0.record(stream)
+            a0, a1 = b0, b1
+            step()
+            s1.record(stream)
+        torch.cuda.synchronize()
+    launches = pa.pa_launch_count()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    attn_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    total_ms = float(np.sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T / (ms_per_step / 1e3)
+
+    # ---- end to end: inputs from pinned host memory, output back to host
+    host_in = {"nst": w.num_scheduled_tokens, "nct": w.num_computed_tokens, "bt": w.block_table}
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host_in.items()}
+    for k in ("q", "key", "value"):
+        pinned[k] = vals[k].cpu().contiguous().pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in pinned.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k in pinned:
+            dev_in[k].copy_(pinned[k], non_blocking=True)
+        step(dev_in["nst"], dev_in["nct"], dev_in["bt"], dev_in["q"], dev_in["key"],
+             dev_in["value"])
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(args.warmup, 1)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        e2e_ev[k][0].record(stream)
+        e2e_step()
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.sum([a.elapsed_time(b) for a, b in e2e_ev]))
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        dist.barrier()
+    status, detail = pa.pa_get_status()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device checks failed: {pa.check_bits(detail)}")
+
+    # ---- roofline of the attention call (decode kernel + merge pass)
+    logical, unique = kv_bytes(w)
+    attn_avg_s = float(np.mean(attn_ms)) / 1e3
+    alg = unique if args.workload == "shared_prefix" else logical
+    peak, peak_kind = load_peaks()
+    achieved = alg / attn_avg_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                "kernel": "pa_attention (paged_decode_kernel + merge_kernel)",
+                "algorithmic_bytes_per_launch": alg, "avg_launch_us": attn_avg_s * 1e6,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "frac_of_8TBps": achieved / 8000.0}
+    if args.workload == "shared_prefix":
+        roofline["effective_logical_GBps"] = logical / attn_avg_s / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, threads, desc = oracle_sample(w, host_values(vals), args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "num_reqs": R, "num_tokens": T,
+                       "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                       "head_dim": w.head_dim, "block_size": w.block_size,
+                       "kv_bytes": w.kv_read_bytes(), "parallelism": f"replicas x{world}",
+                       "l2": "flushed between steps (256 MB write outside the timed events)"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": int(launches),
+            "clocks": clocks.summary(),
+            "attn_us_per_step": float(np.mean(attn_ms)) * 1e3,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
