@@ -206,6 +206,40 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
                        size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_attention_noalloc -- pa_attention for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory when they call in -- an engine that has
+ * given nearly all free HBM to its KV-cache pool, a decode loop where
+ * cudaMalloc/cudaFree would synchronise the device, or a host program that
+ * reaches this library through the C ABI with no device allocator of its
+ * own.  Same inputs, outputs and results as pa_attention; the workspace is
+ * a fixed PA_NOALLOC_SCRATCH_BYTES array in the library's own device memory
+ * (every GPU that loads the library holds it until the process exits), and
+ * the call itself allocates nothing.
+ *   - Limit: num_reqs <= PA_NOALLOC_MAX_REQS, else PA_ERR_WORKSPACE and
+ *     nothing is launched.  Long contexts are still handled: with less
+ *     scratch than pa_attention_workspace_size() asks for, the kernel uses
+ *     longer KV partitions.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; nothing needs clearing (each call writes what it
+ *     reads), but calls that overlap on the GPU (different streams, or
+ *     threads without ordering) race on it and must be serialised.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define PA_NOALLOC_MAX_REQS 65536
+pa_status pa_attention_noalloc(const void *q, const void *key_cache, const void *value_cache,
+                               const int32_t *block_table, int32_t max_blocks_per_req,
+                               const int32_t *query_start_loc, const int32_t *seq_lens,
+                               int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                               int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                               float scale, pa_dtype dtype, void *out, pa_stream_t stream);
+
+/*
  * pa_get_status -- synchronise `stream`, then read and clear the current
  * device's status word.  Returns PA_OK when no kernel check failed since the
  * last call, PA_ERR_TIMEOUT when a bounded wait ran out, PA_ERR_DEVICE_CHECK

@@ -7,8 +7,8 @@ CUDA kernels; there is no CPU or PyTorch fallback, and using the package
 without the built library raises immediately.
 
 Functions carry the C names: ``pa_prepare_inputs``, ``pa_cache_write``,
-``pa_attention_workspace_size``, ``pa_attention``, ``pa_get_status``,
-``pa_launch_count``.
+``pa_attention_workspace_size``, ``pa_attention``, ``pa_attention_noalloc``,
+``pa_get_status``, ``pa_launch_count``.
 """
 
 from __future__ import annotations
@@ -70,6 +70,10 @@ def lib():
             L.pa_attention.restype = ctypes.c_int
             L.pa_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                        i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, vp, sz, vp]
+            L.pa_attention_noalloc.restype = ctypes.c_int
+            L.pa_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                               i32, i32, i32, i32, i32, ctypes.c_float,
+                                               ctypes.c_int, vp, vp]
             L.pa_get_status.restype = ctypes.c_int
             L.pa_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             L.pa_status_string.restype = ctypes.c_char_p
@@ -173,6 +177,32 @@ def pa_attention(q, key_cache, value_cache, block_table, query_start_loc, seq_le
         hq, hkv, d, bs, nb, float(scale), dt, _dev(out, "out"), ws_ptr, ws_bytes,
         _stream(stream))
     _check(rc, "pa_attention")
+
+
+def pa_attention_noalloc(q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
+                         max_query_len, max_seq_len, scale, out, stream=None):
+    """pa_attention without a caller workspace: for callers that cannot
+    allocate device memory at call time.  The library's own fixed device
+    array (PA_NOALLOC_SCRATCH_BYTES per GPU) serves as scratch; calls on one
+    device must not overlap on the GPU.  Make the first call on a device
+    before any stream capture (it looks up the array's address)."""
+    T, hq, d = q.shape
+    nb, bs, hkv, _ = key_cache.shape
+    R = seq_lens.shape[0]
+    dt = _DTYPES.get(q.dtype)
+    if dt is None or key_cache.dtype != q.dtype or out.dtype != q.dtype:
+        raise TypeError("q, caches and out must share a bf16/fp16 dtype")
+    rc = lib().pa_attention_noalloc(
+        _dev(q, "q"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_table, "block_table", torch.int32), block_table.shape[1],
+        _dev(query_start_loc, "query_start_loc", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), R, T, int(max_query_len), int(max_seq_len),
+        hq, hkv, d, bs, nb, float(scale), dt, _dev(out, "out"), _stream(stream))
+    _check(rc, "pa_attention_noalloc")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+NOALLOC_MAX_REQS = 65536
 
 
 def pa_get_status(stream=None):
