@@ -10,14 +10,15 @@
 //     (query token, q head of group g) pair, so each K/V page is read once
 //     for all Hq/Hkv heads that share it and for all query tokens of a short
 //     chunk.  Rows per item (RPI) is a template parameter.
-//   * Persistent CTAs (3 per SM).  Every warp walks the request list itself
+//   * Persistent CTAs (3 per SM; 2 for 8-row items, which need more registers).  Every warp walks the request list itself
 //     (a warp-wide scan over 32 requests at a time) to map its CTA's next
 //     item index to (r, g, chunk, partition), so no work list is stored and
 //     no planning launch is needed.
 //   * One producer warp issues 3-D TMA copies of one 16-token page of one kv
-//     head (box D x 1 x 16) into a 12-stage shared-memory ring, driven by the
-//     block table; four consumer warps compute.  mbarriers: full (TMA bytes)
-//     and empty (one arrive per consumer warp).  Every wait is bounded.
+//     head (box D x 1 x 16) into a 16-stage shared-memory ring, driven by the
+//     block table, in the order K0 V0 K1 V1 ...; four consumer warps take the
+//     (K, V) page pairs round-robin.  mbarriers: full (TMA bytes) and empty
+//     (one arrive by the owning warp).  Every wait is bounded.
 //   * Keys are processed in chunks of 256 (16 pages): all K pages of the
 //     chunk -> scores in shared memory -> exact chunk max/sum, combined
 //     online across chunks -> all V pages of the chunk.  QK: one warp per
@@ -39,7 +40,14 @@ constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kCtasPerSm = 3;
-constexpr int kStages = 12;
+constexpr int kStages = 16;
+// Page pairs (K, V) are dealt round-robin to the consumer warps.  With
+// (kStages / 2) a multiple of the warp count, pair n always lands on stages
+// 2n mod kStages and 2n+1 mod kStages owned by warp n mod 4 alone, so every
+// round of a stage is consumed by the same warp in order: a warp can never run
+// a whole ring round ahead on a stage (where mbarrier parity could not tell
+// the rounds apart).
+static_assert((kStages / 2) % kConsumerWarps == 0, "stages must split evenly among warps");
 constexpr int kPage = 16;         // tokens per cache block
 constexpr int kChunkPages = 16;   // pages per softmax chunk
 constexpr int kChunkKeys = kPage * kChunkPages;
@@ -65,15 +73,23 @@ struct Params {
     unsigned int *status;
 };
 
+// Compile-time shape of the consumer work for head_dim D and RPI rows.
 template <int D, int RPI>
-struct Smem {
+struct Cfg {
+    // QK: LPT lanes share one key; each holds DQ dims of q for every row.
+    static constexpr int LPT = (D == 128 && RPI >= 4) ? 16 : 8;
+    static constexpr int TPP = 32 / LPT;           // keys per pass of a warp
+    static constexpr int NPASS = kPage / TPP;      // passes per page
+    static constexpr int CPL = D / 8 / LPT;        // 16-byte chunks per lane per key row
+    static constexpr int DQ = CPL * 8;             // q dims per lane
+    // PV: lanes over dims.
+    static constexpr int DPL = D / 32;
     static constexpr int kPageBytes = kPage * D * 2;
-    static constexpr int kScores = RPI * kChunkKeys;             // floats
-    static constexpr int kRed = kConsumerWarps * RPI * D;        // floats
-    static constexpr int kUnion = kScores > kRed ? kScores : kRed;
     static constexpr int kStageBytes = kStages * kPageBytes;
-    static constexpr int kBytes = kStageBytes + kUnion * 4 + 3 * RPI * 4 + 2 * kStages * 8 +
-                                  kCandidates * 8 + 16 + 128;  // + alignment slack
+    static constexpr int kPbuf = kPage * RPI + RPI;   // per warp: p[key][row], alpha[row]
+    static constexpr int kComb = RPI * (D + 2);       // per warp: acc[row][D], m[row], l[row]
+    static constexpr int kBytes = kStageBytes + kConsumerWarps * (kPbuf + kComb) * 4 +
+                                  (2 * kStages + 2) * 8 + kCandidates * 8 + 256;
 };
 
 // Per-warp walk over the request list: maps a global item index to its
@@ -180,21 +196,23 @@ __device__ __forceinline__ void item_keys(const Params &p, const typename Walker
     const int last_row = min((it.chunk + 1) * RPI, it.n * p.G) - 1;
     const int max_pos = it.L - it.n + last_row / p.G;
     k0 = it.split * part;
-    k1 = min(min(k0 + part, it.L), max_pos + 1);
+    // A chunk of a long prompt can end before this partition starts: the item
+    // is then empty (k1 == k0), never negative, so page counts stay >= 0.
+    k1 = max(k0, min(min(k0 + part, it.L), max_pos + 1));
 }
 
-// Reduce v[RPI] across the 32 lanes so that each row's full sum ends in the
-// lanes whose low (5 - log2 RPI) bits are zero; returns the row the lane holds
-// in v[0].  Each halving step trades half of the rows with the partner lane,
-// so RPI rows cost RPI - 1 + (5 - log2 RPI) shuffles instead of 5 * RPI.
-template <int RPI>
-__device__ __forceinline__ int reduce_scatter(float (&v)[RPI], int lane) {
+// Reduce v[RPI] across the LPT lanes of a key group so that each row's full
+// sum ends in v[0] of the lanes whose low log2(LPT/RPI) bits are zero; returns
+// the row the lane holds.  Each halving step trades half of the rows with the
+// partner lane, so RPI rows cost RPI - 1 + log2(LPT/RPI) shuffles.
+template <int RPI, int LPT>
+__device__ __forceinline__ int reduce_scatter(float (&v)[RPI], int j) {
     int row = 0;
 #pragma unroll
     for (int step = 0; (1 << step) < RPI; ++step) {
         const int half = RPI >> (step + 1);
-        const int mask = 16 >> step;
-        const bool upper = lane & mask;
+        const int mask = (LPT / 2) >> step;
+        const bool upper = j & mask;
 #pragma unroll
         for (int i = 0; i < half; ++i) {
             const float send = upper ? v[i] : v[i + half];
@@ -204,40 +222,45 @@ __device__ __forceinline__ int reduce_scatter(float (&v)[RPI], int lane) {
         if (upper) row += half;
     }
 #pragma unroll
-    for (int m = 32 / RPI / 2; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+    for (int m = LPT / RPI / 2; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
     return row;
 }
 
-// Load this lane's DPL elements of a 16-bit row as floats.
-template <typename T, int DPL>
-__device__ __forceinline__ void load_lane(const void *row, int lane, float (&f)[DPL]) {
-    if constexpr (DPL == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(static_cast<const char *>(row) + lane * 8);
-        Elt<T>::unpack2(raw.x, f[0], f[1]);
-        Elt<T>::unpack2(raw.y, f[2], f[3]);
-    } else {
-        const uint32_t raw = *reinterpret_cast<const uint32_t *>(static_cast<const char *>(row) + lane * 4);
-        Elt<T>::unpack2(raw, f[0], f[1]);
-    }
+// Unpack a word of two 16-bit elements into a float pair (element order kept).
+template <typename T>
+__device__ __forceinline__ float2 unpack_pair(uint32_t w) {
+    float2 f;
+    Elt<T>::unpack2(w, f.x, f.y);
+    return f;
+}
+
+// Bounded barrier among the consumer warps (an mbarrier with one arrival per
+// warp): a warp that timed out elsewhere cannot leave the others waiting.
+__device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &parity, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, parity);
+    parity ^= 1;
+    return ok;
 }
 
 template <typename T, int D, int RPI>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, RPI == 8 ? 2 : kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ Params p) {
-    using S = Smem<D, RPI>;
-    constexpr int DPL = D / 32;  // dims per lane
+    using C = Cfg<D, RPI>;
+    constexpr int LPT = C::LPT, TPP = C::TPP, NPASS = C::NPASS, CPL = C::CPL, DQ = C::DQ;
+    constexpr int DPL = C::DPL;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     unsigned char *stages = base;
-    float *uni = reinterpret_cast<float *>(base + S::kStageBytes);
-    float *row_m = uni + S::kUnion;
-    float *row_l = row_m + RPI;
-    float *row_a = row_l + RPI;
+    float *pbuf = reinterpret_cast<float *>(base + C::kStageBytes);
+    float *comb = pbuf + kConsumerWarps * C::kPbuf;
     uint64_t *full = reinterpret_cast<uint64_t *>(
-        (reinterpret_cast<uintptr_t>(row_a + RPI) + 7) & ~uintptr_t(7));
+        (reinterpret_cast<uintptr_t>(comb + kConsumerWarps * C::kComb) + 7) & ~uintptr_t(7));
     uint64_t *empty = full + kStages;
-    unsigned long long *cand = reinterpret_cast<unsigned long long *>(empty + kStages);
+    uint64_t *cbar = empty + kStages;
+    unsigned long long *cand = reinterpret_cast<unsigned long long *>(cbar + 2);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -245,8 +268,9 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], 1);
         }
+        mbar_init(cbar, kConsumerWarps);
         fence_mbar_init();
     }
     if (warp == kConsumerWarps && lane == 0) {
@@ -309,43 +333,45 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
     if (warp == kConsumerWarps) {
         // =================== producer warp ===================
+        // Ring order: K page 0, V page 0, K page 1, V page 1, ... of each item.
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x) {
             int k0, k1;
             item_keys<RPI>(p, it, part, k0, k1);
-            const int32_t *row = p.bt + (long long)it.r * p.MB;
-            for (int c0 = k0; ok && c0 < k1; c0 += kChunkKeys) {
-                const int npages = (min(c0 + kChunkKeys, k1) - c0 + kPage - 1) / kPage;
+            const int npages = (k1 - k0 + kPage - 1) / kPage;
+            const int32_t *row = p.bt + (long long)it.r * p.MB + k0 / kPage;
+            for (int g0 = 0; ok && g0 < npages; g0 += 32) {
                 int blk = 0;
-                if (lane < npages) {
-                    blk = row[c0 / kPage + lane];
+                if (g0 + lane < npages) {
+                    blk = row[g0 + lane];
                     if (blk < 0 || blk >= p.NB) {
                         flag(p.status, PA_CHECK_BLOCK_ID);
                         blk = 0;
                     }
                 }
-                for (int kv = 0; ok && kv < 2; ++kv) {
-                    for (int pg = 0; pg < npages; ++pg) {
-                        const int b = __shfl_sync(0xffffffffu, blk, pg);
+                const int n = min(32, npages - g0);
+                for (int pg = 0; ok && pg < n; ++pg) {
+                    const int b = __shfl_sync(0xffffffffu, blk, pg);
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
                         if (lane == 0) {
                             if (!mbar_wait(&empty[stage], phase ^ 1)) {
                                 flag(p.status, PA_CHECK_TIMEOUT);
                                 ok = false;
                             } else {
-                                mbar_arrive_expect_tx(&full[stage], S::kPageBytes);
-                                tma_load_3d(stages + stage * S::kPageBytes, kv ? &p.tmV : &p.tmK,
+                                mbar_arrive_expect_tx(&full[stage], C::kPageBytes);
+                                tma_load_3d(stages + stage * C::kPageBytes, kv ? &p.tmV : &p.tmK,
                                             &full[stage], 0, it.g, b * kPage);
                             }
                         }
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) break;
                         if (++stage == kStages) {
                             stage = 0;
                             phase ^= 1;
                         }
                     }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
                 }
             }
         }
@@ -367,193 +393,248 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     }
 
     // =================== consumer warps ===================
+    // Warp w takes the page pairs whose running index (over all items of this
+    // CTA) is w mod 4, and keeps its own online-softmax state for its rows;
+    // the four states are combined once per item.
     const T *q = reinterpret_cast<const T *>(p.q);
-    int stage = 0;
-    uint32_t phase = 0;
+    const int j = lane % LPT;        // lane within its key group
+    const int tq = lane / LPT;       // key group: keys tq, tq + TPP, ... of a page
+    const int dup = j & (LPT / RPI - 1);
+    int myrow = 0;                   // the row whose score this lane ends up holding
+#pragma unroll
+    for (int step = 0; (1 << step) < RPI; ++step)
+        if (j & ((LPT / 2) >> step)) myrow += RPI >> (step + 1);
+    float *pb = pbuf + warp * C::kPbuf;
+    float *cw = comb + warp * C::kComb;
+    long long pair_base = 0;         // page pairs of earlier items
+    uint32_t cpar = 0;
     bool ok = true;
     for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x) {
         int k0, k1;
         item_keys<RPI>(p, it, part, k0, k1);
+        const int npages = (k1 - k0 + kPage - 1) / kPage;
         const int qstart = p.qsl[it.r];
         const int nrows = it.n * p.G;
         const int pos0 = it.L - it.n;  // position of the request's first query token
+        int lim;                       // last key this lane's row may see
+        {
+            const int rr = it.chunk * RPI + myrow;
+            lim = rr < nrows ? min(pos0 + rr / p.G, k1 - 1) : -1;
+        }
 
-        // Q rows of this item, this lane's dims, pre-scaled by scale*log2(e).
-        float qr[RPI][DPL];
+        // q rows of this item, this lane's QK dims, pre-scaled by scale*log2(e).
+        float2 qv[RPI][DQ / 2];
 #pragma unroll
-        for (int j = 0; j < RPI; ++j) {
-            const int rr = it.chunk * RPI + j;
+        for (int r = 0; r < RPI; ++r) {
+            const int rr = it.chunk * RPI + r;
             if (rr < nrows) {
-                const int h = it.g * p.G + rr % p.G;
-                load_lane<T, DPL>(q + ((long long)(qstart + rr / p.G) * p.Hq + h) * D, lane, qr[j]);
+                const T *qrow = q + ((long long)(qstart + rr / p.G) * p.Hq + it.g * p.G + rr % p.G) * D;
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) qr[j][d] *= p.qscale;
+                for (int c = 0; c < CPL; ++c) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (j + c * LPT) * 8);
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float2 f = unpack_pair<T>(w4[e]);
+                        qv[r][c * 4 + e] = make_float2(f.x * p.qscale, f.y * p.qscale);
+                    }
+                }
             } else {
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) qr[j][d] = 0.f;
+                for (int e = 0; e < DQ / 2; ++e) qv[r][e] = make_float2(0.f, 0.f);
             }
         }
-        float acc[RPI][DPL];
+        float2 acc[RPI][DPL / 2];
 #pragma unroll
-        for (int j = 0; j < RPI; ++j)
+        for (int r = 0; r < RPI; ++r)
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) acc[j][d] = 0.f;
-        if (tid < RPI) {
-            row_m[tid] = -INFINITY;
-            row_l[tid] = 0.f;
-        }
+            for (int e = 0; e < DPL / 2; ++e) acc[r][e] = make_float2(0.f, 0.f);
+        float m_run = -INFINITY, l_run = 0.f;
 
-        for (int c0 = k0; ok && c0 < k1; c0 += kChunkKeys) {
-            const int nkeys = min(c0 + kChunkKeys, k1) - c0;
-            const int npages = (nkeys + kPage - 1) / kPage;
-            // ---- scores for the chunk's keys
-            for (int pg = 0; pg < npages; ++pg) {
-                if (!mbar_wait(&full[stage], phase)) {
-                    flag(p.status, PA_CHECK_TIMEOUT);
-                    ok = false;
-                    break;
+        for (int pg = (int)((warp - pair_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
+             pg < npages; pg += kConsumerWarps) {
+            const long long n2 = 2 * (pair_base + pg);
+            const int stK = (int)(n2 % kStages), stV = (int)((n2 + 1) % kStages);
+            const uint32_t phK = (uint32_t)((n2 / kStages) & 1), phV = (uint32_t)(((n2 + 1) / kStages) & 1);
+            const int key0 = k0 + pg * kPage;
+
+            // ---- scores of the page's 16 keys for this warp's rows
+            if (!mbar_wait(&full[stK], phK)) {
+                flag(p.status, PA_CHECK_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const unsigned char *kpage = stages + stK * C::kPageBytes;
+            float sc[NPASS];
+#pragma unroll
+            for (int ps = 0; ps < NPASS; ++ps) {
+                const int t = ps * TPP + tq;
+                float2 kf[DQ / 2];
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(kpage + t * D * 2 + (j + c * LPT) * 16);
+                    kf[c * 4 + 0] = unpack_pair<T>(raw.x);
+                    kf[c * 4 + 1] = unpack_pair<T>(raw.y);
+                    kf[c * 4 + 2] = unpack_pair<T>(raw.z);
+                    kf[c * 4 + 3] = unpack_pair<T>(raw.w);
                 }
-                const unsigned char *page = stages + stage * S::kPageBytes;
+                float s[RPI];
 #pragma unroll
-                for (int u = 0; u < kPage / kConsumerWarps; ++u) {
-                    const int tk = warp + u * kConsumerWarps;
-                    float kf[DPL];
-                    load_lane<T, DPL>(page + tk * D * 2, lane, kf);
-                    float s[RPI];
+                for (int r = 0; r < RPI; ++r) {
+                    float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < RPI; ++j) {
-                        float a = 0.f;
+                    for (int e = 0; e < DQ / 2; ++e) a = __ffma2_rn(qv[r][e], kf[e], a);
+                    s[r] = a.x + a.y;
+                }
+                reduce_scatter<RPI, LPT>(s, j);
+                sc[ps] = key0 + t <= lim ? s[0] : -INFINITY;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stK]);
+
+            // ---- online softmax update for this lane's row
+            float mp = -INFINITY;
 #pragma unroll
-                        for (int d = 0; d < DPL; ++d) a = fmaf(qr[j][d], kf[d], a);
-                        s[j] = a;
+            for (int ps = 0; ps < NPASS; ++ps) mp = fmaxf(mp, sc[ps]);
+#pragma unroll
+            for (int m = LPT; m < 32; m <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, m));
+            const float m_new = fmaxf(m_run, mp);
+            const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
+            float sum = 0.f;
+#pragma unroll
+            for (int ps = 0; ps < NPASS; ++ps) {
+                const float e = m_new == -INFINITY ? 0.f : fast_exp2(sc[ps] - m_new);
+                sc[ps] = e;
+                sum += e;
+            }
+#pragma unroll
+            for (int m = LPT; m < 32; m <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+            l_run = l_run * alpha + sum;
+            m_run = m_new;
+            if (dup == 0) {
+#pragma unroll
+                for (int ps = 0; ps < NPASS; ++ps) pb[(ps * TPP + tq) * RPI + myrow] = sc[ps];
+                if (tq == 0) pb[kPage * RPI + myrow] = alpha;
+            }
+            __syncwarp();
+
+            // ---- weighted values
+            if (!mbar_wait(&full[stV], phV)) {
+                flag(p.status, PA_CHECK_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const unsigned char *vpage = stages + stV * C::kPageBytes;
+#pragma unroll
+            for (int r = 0; r < RPI; ++r) {
+                const float a = pb[kPage * RPI + r];
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) acc[r][e] = __fmul2_rn(acc[r][e], make_float2(a, a));
+            }
+            const int nvalid = min(kPage, k1 - key0);  // never touch slots past the context
+            for (int t = 0; t < nvalid; ++t) {
+                float2 vf[DPL / 2];
+                if constexpr (DPL == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(vpage + t * D * 2 + lane * 8);
+                    vf[0] = unpack_pair<T>(raw.x);
+                    vf[1] = unpack_pair<T>(raw.y);
+                } else {
+                    vf[0] = unpack_pair<T>(*reinterpret_cast<const uint32_t *>(vpage + t * D * 2 + lane * 4));
+                }
+                float pr[RPI];
+                if constexpr (RPI >= 4) {
+#pragma unroll
+                    for (int r = 0; r < RPI; r += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4 *>(pb + t * RPI + r);
+                        pr[r] = v4.x;
+                        pr[r + 1] = v4.y;
+                        pr[r + 2] = v4.z;
+                        pr[r + 3] = v4.w;
                     }
-                    const int row = reduce_scatter<RPI>(s, lane);
-                    if ((lane & (32 / RPI - 1)) == 0) {
-                        const int kk = pg * kPage + tk;
-                        const int rr = it.chunk * RPI + row;
-                        const bool vis =
-                            rr < nrows && c0 + kk < k1 && c0 + kk <= pos0 + rr / p.G;
-                        uni[row * kChunkKeys + kk] = vis ? s[0] : -INFINITY;
-                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < RPI; ++r) pr[r] = pb[t * RPI + r];
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
+#pragma unroll
+                for (int r = 0; r < RPI; ++r)
+#pragma unroll
+                    for (int e = 0; e < DPL / 2; ++e)
+                        acc[r][e] = __ffma2_rn(make_float2(pr[r], pr[r]), vf[e], acc[r][e]);
             }
-            if (!ok) break;
-            named_bar_sync(1, kConsumers);
-            // ---- online softmax update, one warp per row
-            for (int j = warp; j < RPI; j += kConsumerWarps) {
-                float *srow = uni + j * kChunkKeys;
-                float mx = -INFINITY;
-                for (int k = lane; k < nkeys; k += 32) mx = fmaxf(mx, srow[k]);
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                const float m_old = row_m[j];
-                const float m_new = fmaxf(m_old, mx);
-                float sum = 0.f;
-                for (int k = lane; k < nkeys; k += 32) {
-                    const float e = m_new == -INFINITY ? 0.f : fast_exp2(srow[k] - m_new);
-                    srow[k] = e;
-                    sum += e;
-                }
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                if (lane == 0) {
-                    const float alpha = m_old == -INFINITY ? 0.f : fast_exp2(m_old - m_new);
-                    row_a[j] = alpha;
-                    row_l[j] = row_l[j] * alpha + sum;
-                    row_m[j] = m_new;
-                }
-            }
-            named_bar_sync(1, kConsumers);
-#pragma unroll
-            for (int j = 0; j < RPI; ++j) {
-                const float a = row_a[j];
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) acc[j][d] *= a;
-            }
-            // ---- weighted sum of the chunk's values
-            for (int pg = 0; pg < npages; ++pg) {
-                if (!mbar_wait(&full[stage], phase)) {
-                    flag(p.status, PA_CHECK_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                const unsigned char *page = stages + stage * S::kPageBytes;
-#pragma unroll
-                for (int u = 0; u < kPage / kConsumerWarps; ++u) {
-                    const int tk = warp + u * kConsumerWarps;
-                    const int kk = pg * kPage + tk;
-                    if (c0 + kk < k1) {  // never touch slots past the context
-                        float vf[DPL];
-                        load_lane<T, DPL>(page + tk * D * 2, lane, vf);
-#pragma unroll
-                        for (int j = 0; j < RPI; ++j) {
-                            const float pj = uni[j * kChunkKeys + kk];
-#pragma unroll
-                            for (int d = 0; d < DPL; ++d) acc[j][d] = fmaf(pj, vf[d], acc[j][d]);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-            named_bar_sync(1, kConsumers);  // the chunk's weights are no longer read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stV]);
         }
         if (!ok) break;
+        pair_base += npages;
 
-        // ---- combine the consumer warps' partial sums and write the item out
+        // ---- combine the four warps' states and write the item out
 #pragma unroll
-        for (int j = 0; j < RPI; ++j)
+        for (int r = 0; r < RPI; ++r)
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) uni[(warp * RPI + j) * D + lane * DPL + d] = acc[j][d];
-        named_bar_sync(1, kConsumers);
+            for (int e = 0; e < DPL / 2; ++e)
+                *reinterpret_cast<float2 *>(cw + r * D + lane * DPL + 2 * e) = acc[r][e];
+        if (dup == 0 && tq == 0) {
+            cw[RPI * D + myrow] = m_run;
+            cw[RPI * D + RPI + myrow] = l_run;
+        }
+        if (!consumer_sync(cbar, cpar, lane)) {
+            flag(p.status, PA_CHECK_TIMEOUT);
+            ok = false;
+            break;
+        }
         for (int o = tid; o < RPI * D / 2; o += kConsumers) {
-            const int j = o / (D / 2);
+            const int r = o / (D / 2);
             const int d = (o % (D / 2)) * 2;
-            const int rr = it.chunk * RPI + j;
+            const int rr = it.chunk * RPI + r;
             if (rr >= nrows) continue;
-            float s0 = 0.f, s1 = 0.f;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb[w * C::kComb + RPI * D + r]);
+            float Ls = 0.f, s0 = 0.f, s1 = 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                s0 += uni[(w * RPI + j) * D + d];
-                s1 += uni[(w * RPI + j) * D + d + 1];
+                const float *c = comb + w * C::kComb;
+                const float mw = c[RPI * D + r];
+                const float sw = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                Ls += sw * c[RPI * D + RPI + r];
+                const float2 a = *reinterpret_cast<const float2 *>(c + r * D + d);
+                s0 += sw * a.x;
+                s1 += sw * a.y;
             }
             if (it.pslot < 0) {
-                const float inv = 1.f / row_l[j];
+                const float inv = 1.f / Ls;
                 const int h = it.g * p.G + rr % p.G;
                 T *dst = reinterpret_cast<T *>(p.out) +
                          ((long long)(qstart + rr / p.G) * p.Hq + h) * D + d;
                 *reinterpret_cast<uint32_t *>(dst) = Elt<T>::pack2(s0 * inv, s1 * inv);
             } else {
-                float *po = p.part_o + (it.pslot * RPI + j) * D + d;
+                float *po = p.part_o + (it.pslot * RPI + r) * D + d;
                 *reinterpret_cast<float2 *>(po) = make_float2(s0, s1);
-                if (d == 0) {
-                    *reinterpret_cast<float2 *>(p.part_ml + (it.pslot * RPI + j) * 2) =
-                        make_float2(row_m[j], row_l[j]);
-                }
+                if (d == 0)
+                    *reinterpret_cast<float2 *>(p.part_ml + (it.pslot * RPI + r) * 2) =
+                        make_float2(M, Ls);
             }
         }
-        named_bar_sync(1, kConsumers);  // the union buffer is free again
+        if (!consumer_sync(cbar, cpar, lane)) {  // the combine buffer is free again
+            flag(p.status, PA_CHECK_TIMEOUT);
+            ok = false;
+            break;
+        }
     }
-    // Consumers that stop early (a timed-out wait) release every stage once so
-    // the producer's bounded drain can finish.
+    // A consumer that stops early (a timed-out wait) releases every stage and
+    // the item barrier once, so the others' bounded waits and the producer's
+    // drain can finish.
     if (!ok && lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_arrive(&empty[s]);
+        mbar_arrive(cbar);
     }
 }
 
 // Second pass: for each (token, q head) of a request whose context was split,
 // combine the partitions' (m, l, o): M = max m_s, o = sum 2^(m_s-M) o_s /
-// sum 2^(m_s-M) l_s.  One CTA per token, one warp per head.
+// sum 2^(m_s-M) l_s.  One CTA per token, one warp per head.  Lanes take 32
+// partitions at a time for (m, l); the weighted sum then walks those 32 with
+// lanes over dims, eight independent partial-row loads in flight.
 template <typename T, int D, int RPI>
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Params p) {
     constexpr int DPL = D / 32;
@@ -583,20 +664,42 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Para
         const int rr = tl * p.G + h % p.G;
         const int chunk = rr / RPI, j = rr % RPI;
         const long long first = pbase + ((long long)g * nchunks + chunk) * nsplit;
+        const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
         float M = -INFINITY;
-        for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.part_ml[((first + s) * RPI + j) * 2]);
+        for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, ml[(first + s) * RPI + j].x);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float Lsum = 0.f;
         float o[DPL];
 #pragma unroll
         for (int d = 0; d < DPL; ++d) o[d] = 0.f;
-        float Lsum = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
-            const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + ((first + s) * RPI + j) * 2);
-            const float w = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-            Lsum += w * ml.y;
-            const float *po = p.part_o + ((first + s) * RPI + j) * D + lane * DPL;
-#pragma unroll
-            for (int d = 0; d < DPL; ++d) o[d] = fmaf(w, po[d], o[d]);
+        for (int s0 = 0; s0 < nsplit; s0 += 32) {
+            float w = 0.f;
+            if (s0 + lane < nsplit) {
+                const float2 v = ml[(first + s0 + lane) * RPI + j];
+                w = v.x == -INFINITY ? 0.f : fast_exp2(v.x - M);
+                Lsum += w * v.y;
+            }
+            const int cnt = min(32, nsplit - s0);
+#pragma unroll 8
+            for (int k = 0; k < cnt; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, k);
+                const float *po = p.part_o + ((first + s0 + k) * RPI + j) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(po);
+                    o[0] = fmaf(wk, v.x, o[0]);
+                    o[1] = fmaf(wk, v.y, o[1]);
+                    o[2] = fmaf(wk, v.z, o[2]);
+                    o[3] = fmaf(wk, v.w, o[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(po);
+                    o[0] = fmaf(wk, v.x, o[0]);
+                    o[1] = fmaf(wk, v.y, o[1]);
+                }
+            }
         }
+#pragma unroll
+        for (int s = 16; s >= 1; s >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, s);
         const float inv = 1.f / Lsum;
         T *dst = reinterpret_cast<T *>(p.out) + ((long long)t * p.Hq + h) * D + lane * DPL;
 #pragma unroll
@@ -606,17 +709,25 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Para
 }
 
 template <typename T, int D, int RPI>
-pa_status launch_typed(Params &prm, int grid, bool merge, cudaStream_t stream) {
-    using S = Smem<D, RPI>;
-    static bool configured[64] = {};
+pa_status launch_typed(Params &prm, long long max_items, bool merge, cudaStream_t stream) {
+    using S = Cfg<D, RPI>;
+    static int resident[64] = {};  // CTAs per SM, per device
     int dev = 0;
     PA_TRY_CUDA(cudaGetDevice(&dev));
-    if (dev >= 64 || !configured[dev]) {
+    int per_sm = dev < 64 ? resident[dev] : 0;
+    if (per_sm == 0) {
         PA_TRY_CUDA(cudaFuncSetAttribute(paged_decode_kernel<T, D, RPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes));
-        if (dev < 64) configured[dev] = true;
+        PA_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, paged_decode_kernel<T, D, RPI>, kThreads, S::kBytes));
+        if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+        if (dev < 64) resident[dev] = per_sm;
     }
-    paged_decode_kernel<T, D, RPI><<<grid, kThreads, S::kBytes, stream>>>(prm);
+    // Persistent grid: every resident slot once, no more CTAs than items.
+    long long grid = (long long)per_sm * num_sms();
+    if (max_items < grid) grid = max_items;
+    if (grid < 1) grid = 1;
+    paged_decode_kernel<T, D, RPI><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
     if (merge && prm.T > 0) {
@@ -628,7 +739,7 @@ pa_status launch_typed(Params &prm, int grid, bool merge, cudaStream_t stream) {
 }
 
 template <typename T, int D>
-pa_status dispatch_rpi(int rpi, Params &prm, int grid, bool merge, cudaStream_t stream) {
+pa_status dispatch_rpi(int rpi, Params &prm, long long grid, bool merge, cudaStream_t stream) {
     switch (rpi) {
         case 1: return launch_typed<T, D, 1>(prm, grid, merge, stream);
         case 2: return launch_typed<T, D, 2>(prm, grid, merge, stream);
@@ -720,20 +831,17 @@ pa_status launch_decode(const AttnArgs &a, cudaStream_t stream) {
         }
     }
 
-    // Grid: persistent, kCtasPerSm per SM, no more CTAs than there can be items.
+    // Upper bound on the work items (the grid never exceeds it).
     const long long splits = prm.p_min >= kSingle ? 1 : (a.max_seq + prm.p_min - 1) / prm.p_min;
     const long long chunks = (long long)a.R + ((long long)a.T * prm.G + rpi - 1) / rpi;
-    const long long ub = (long long)a.Hkv * chunks * splits;
-    long long grid = (long long)kCtasPerSm * num_sms();
-    if (ub < grid) grid = ub;
-    if (grid < 1) grid = 1;
+    const long long grid = (long long)a.Hkv * chunks * splits;
 
     const bool bf16 = a.dtype == PA_BF16;
     if (a.D == 128)
-        return bf16 ? dispatch_rpi<__nv_bfloat16, 128>(rpi, prm, (int)grid, merge, stream)
-                    : dispatch_rpi<__half, 128>(rpi, prm, (int)grid, merge, stream);
-    return bf16 ? dispatch_rpi<__nv_bfloat16, 64>(rpi, prm, (int)grid, merge, stream)
-                : dispatch_rpi<__half, 64>(rpi, prm, (int)grid, merge, stream);
+        return bf16 ? dispatch_rpi<__nv_bfloat16, 128>(rpi, prm, grid, merge, stream)
+                    : dispatch_rpi<__half, 128>(rpi, prm, grid, merge, stream);
+    return bf16 ? dispatch_rpi<__nv_bfloat16, 64>(rpi, prm, grid, merge, stream)
+                : dispatch_rpi<__half, 64>(rpi, prm, grid, merge, stream);
 }
 
 }  // namespace pa

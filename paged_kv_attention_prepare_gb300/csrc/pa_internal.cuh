@@ -9,7 +9,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pa.h"
+#include "pa.h"
 
 namespace pa {
 

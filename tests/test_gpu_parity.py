@@ -96,6 +96,20 @@ def test_partition_choice_does_not_change_result(ws):
     _check_attention(res, ref)
 
 
+@pytest.mark.parametrize("group,ws", [(4, None), (8, None), (1, 0)])
+def test_prompt_chunk_longer_than_a_partition(group, ws):
+    # A 600-token chunk at 300 computed spans two 512-key partitions: its first
+    # row chunks see nothing of the second partition (empty work items).
+    rng = np.random.default_rng(group)
+    w = workloads._make("long-chunk", [600, 1, 3], [300, 700, 40], rng, 2 * group, 2, 128,
+                        "bf16")
+    vals = workloads.make_values(w, group)
+    res = run_step(w, vals, workspace_bytes=ws)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    _check_attention(res, ref)
+
+
 @pytest.mark.parametrize("d,dtype,group", [(64, "bf16", 1), (64, "fp16", 8), (128, "fp16", 2),
                                            (128, "bf16", 8), (128, "bf16", 3)])
 def test_head_shapes(d, dtype, group):
