@@ -49,8 +49,6 @@ constexpr int kStages = 16;
 // the rounds apart).
 static_assert((kStages / 2) % kConsumerWarps == 0, "stages must split evenly among warps");
 constexpr int kPage = 16;         // tokens per cache block
-constexpr int kChunkPages = 16;   // pages per softmax chunk
-constexpr int kChunkKeys = kPage * kChunkPages;
 constexpr int kCandidates = 8;    // partition lengths p_min << k
 constexpr int kSingle = INT_MAX / 2;
 
@@ -239,7 +237,7 @@ __device__ __forceinline__ float2 unpack_pair(uint32_t w) {
 __device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &parity, int lane) {
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, parity);
+    const bool ok = mbar_wait_warp(bar, parity);
     parity ^= 1;
     return ok;
 }
@@ -459,7 +457,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             const int key0 = k0 + pg * kPage;
 
             // ---- scores of the page's 16 keys for this warp's rows
-            if (!mbar_wait(&full[stK], phK)) {
+            if (!mbar_wait_warp(&full[stK], phK)) {
                 flag(p.status, PA_CHECK_TIMEOUT);
                 ok = false;
                 break;
@@ -519,7 +517,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             __syncwarp();
 
             // ---- weighted values
-            if (!mbar_wait(&full[stV], phV)) {
+            if (!mbar_wait_warp(&full[stV], phV)) {
                 flag(p.status, PA_CHECK_TIMEOUT);
                 ok = false;
                 break;
@@ -782,7 +780,7 @@ size_t decode_workspace_size(int32_t R, int32_t T, int32_t max_q, int32_t max_se
     return bytes < cap ? bytes : cap;
 }
 
-pa_status launch_decode(const AttnArgs &a, cudaStream_t stream) {
+pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     using namespace decode;
     Params prm;
     memset(&prm, 0, sizeof prm);
@@ -802,11 +800,11 @@ pa_status launch_decode(const AttnArgs &a, cudaStream_t stream) {
     prm.Hq = a.Hq;
     prm.Hkv = a.Hkv;
     prm.G = a.Hq / a.Hkv;
-    prm.tau = INT_MAX;
+    prm.tau = tau;
     prm.qscale = a.scale * 1.4426950408889634f;
     prm.status = status_word();
     if (!prm.status) return PA_ERR_CUDA;
-    const int rpi = rows_per_item(prm.G, a.max_q);
+    const int rpi = rows_per_item(prm.G, a.max_q < tau ? a.max_q : tau);
 
     // Workspace: per-request metadata, then (m, l) and o partials.
     const size_t meta = round_up((size_t)a.R * 16);

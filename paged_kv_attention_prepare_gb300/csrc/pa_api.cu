@@ -181,7 +181,11 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
     a.out = out;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
-    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int tau = prefill_tau(a);
+    const pa_status r = launch_decode(a, tau, st);
+    if (r != PA_OK) return r;
+    return launch_prefill(a, tau, st);
 }
 
 pa_status pa_get_status(pa_stream_t stream, uint32_t *detail) {

@@ -49,7 +49,11 @@ struct AttnArgs {
 
 size_t decode_workspace_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq,
                              int32_t Hq, int32_t Hkv, int32_t D);
-pa_status launch_decode(const AttnArgs &a, cudaStream_t stream);
+// Requests with at most `tau` query tokens run on the split-K kernel, longer
+// ones on the tensor-core kernel (tau == INT_MAX: everything split-K).
+int prefill_tau(const AttnArgs &a);
+pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream);
+pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream);
 
 // Encode a 3-D TMA map over one pool viewed as [NB*bs][Hkv][D] elements with a
 // box of D x 1 kv head x `box_rows` slots.
@@ -118,6 +122,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
     return true;
+}
+
+// The same wait taken by a whole warp: every lane gets one answer, so the
+// warp stays converged for the warp-collective instructions that follow.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
 // 3-D tiled TMA load global -> shared, completion counted on `bar` in bytes.

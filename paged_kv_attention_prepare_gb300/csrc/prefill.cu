@@ -1,0 +1,663 @@
+// Paged attention for long query chunks (prompt prefill) on the 5th-generation
+// tensor cores: tcgen05.mma with operands staged by TMA, accumulators in TMEM.
+//
+// "How vLLM Works Internally", sections "How the Kernel Works" and the
+// prefill/decode split (prefill is compute-bound); "Inside vLLM", the read
+// path (cu_seqlens_q, seqused_k, block_table).  Same maths as the split-K
+// kernel: out = softmax(scale * q K^T, causal) V per request and kv head.
+//
+// Work item = (request, kv head g, 128-row tile).  A row is one (query token,
+// q head of group g) pair, so a K/V tile serves all Hq/Hkv heads of the
+// group; the Q tile is one 3-D TMA box {64 dims, G heads, 128/G tokens} per
+// 64-dim half.  Items run on persistent CTAs (one per SM), heaviest first.
+//
+// Per 128-key KV tile j (8 pages of 16 tokens, each page one TMA box per
+// 64-dim half, 128-byte swizzle, addressed through the block table):
+//   S_j = Q K_j^T         tcgen05.mma, A = Q (smem, K-major), B = K (smem,
+//                         K-major), fp32 accumulator in TMEM (double buffer)
+//   P_j = exp2(S_j*c - m) softmax warps, one row per thread (tcgen05.ld),
+//                         written back over S_j in TMEM as bf16/fp16
+//   O  += P_j V_j         tcgen05.mma, A = P (TMEM), B = V (smem, MN-major)
+// QK_{j+1} is issued before PV_j so the tensor core works while the softmax
+// warps process tile j.  The running max is only moved (and O rescaled in
+// TMEM) when a tile's max exceeds it by more than 2^8; otherwise P uses the
+// old reference, which keeps every P <= 256 and the result exact.
+//
+// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM allocation), 2..5 = softmax
+// and epilogue (TMEM lanes 32*(warp%4)..+31).  Every mbarrier wait is bounded.
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstring>
+#include <type_traits>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace prefill {
+
+constexpr int kBM = 128;          // rows per tile
+constexpr int kBN = 128;          // keys per KV tile
+constexpr int kPage = 16;
+constexpr int kPagesPerTile = kBN / kPage;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.f;  // log2 units
+constexpr int kTauDefault = 16;           // longer query chunks take this kernel
+
+struct Params {
+    CUtensorMap tmQ;
+    CUtensorMap tmK;
+    CUtensorMap tmV;
+    void *out;
+    const int32_t *bt;
+    const int32_t *qsl;
+    const int32_t *seq_lens;
+    int R, T, MB, NB, Hq, Hkv, G;
+    int tau;        // requests with more than tau query tokens are handled here
+    float qscale;   // softmax scale * log2(e)
+    unsigned int *status;
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kQBytes = kBM * D * 2;
+    static constexpr int kTileBytes = kBN * D * 2;
+    static constexpr int kHalfBytes = kBN * 128;     // one 64-dim half of a K/V tile
+    static constexpr int kPageHalfBytes = kPage * 128;
+    static constexpr int kSmem = kQBytes + 4 * kTileBytes + 512 + 1024;
+    static constexpr uint32_t kColO = 256;
+};
+
+// Barrier slots (uint64) in shared memory.
+enum {
+    B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
+    B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ODONE, B_ODONE1, B_OFREE,
+    B_DRAIN, B_COUNT
+};
+
+// ---------------------------------------------------------------------------
+// tcgen05 / TMA wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3fff);
+    d |= (uint64_t)((lbo >> 4) & 0x3fff) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3fff) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for this architecture
+    d |= (uint64_t)2 << 61;  // 128-byte swizzle
+    return d;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t instr_desc(int M, int N, int b_mn_major) {
+    constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    uint32_t d = 1u << 4;  // fp32 accumulator
+    d |= fmt << 7;         // A type
+    d |= fmt << 10;        // B type
+    d |= (uint32_t)b_mn_major << 16;
+    d |= (uint32_t)(N >> 3) << 17;
+    d |= (uint32_t)(M >> 4) << 24;
+    return d;
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit TMEM words: each thread gets its lane's 32.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Work items: per request with more than tau tokens, Hkv x ceil(n*G/128)
+// tiles, ordered last row-tile first (the tile with the most keys), kv heads
+// interleaved.  Every warp walks the request list itself.
+// ---------------------------------------------------------------------------
+
+struct Item {
+    int r, g, mt, n, L, qstart;
+};
+
+struct Walker {
+    const Params *p;
+    int rb;
+    long long base;  // items before the window
+    int n, L, a, items, incl, total;
+
+    __device__ void load(int lane) {
+        const int r = rb + lane;
+        n = 0;
+        L = 0;
+        a = 0;
+        items = 0;
+        if (r < p->R) {
+            a = p->qsl[r];
+            const int b = p->qsl[r + 1];
+            n = b - a;
+            L = p->seq_lens[r];
+            const bool sane = a >= 0 && b <= p->T && n >= 0 && L >= n &&
+                              (L + kPage - 1) / kPage <= p->MB;
+            if (sane && n > p->tau) items = p->Hkv * ((n * p->G + kBM - 1) / kBM);
+        }
+        incl = items;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        total = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __device__ void begin(const Params *params, int lane) {
+        p = params;
+        rb = 0;
+        base = 0;
+        load(lane);
+    }
+    __device__ bool find(long long i, int lane, Item &it) {
+        while (i >= base + total) {
+            base += total;
+            rb += 32;
+            if (rb >= p->R) return false;
+            load(lane);
+        }
+        const int li = (int)(i - base);
+        const int src = __ffs(__ballot_sync(0xffffffffu, incl > li)) - 1;
+        const int excl = __shfl_sync(0xffffffffu, incl - items, src);
+        it.n = __shfl_sync(0xffffffffu, n, src);
+        it.L = __shfl_sync(0xffffffffu, L, src);
+        it.qstart = __shfl_sync(0xffffffffu, a, src);
+        it.r = rb + src;
+        const int local = li - excl;
+        const int nm = (it.n * p->G + kBM - 1) / kBM;
+        it.g = local % p->Hkv;
+        it.mt = nm - 1 - local / p->Hkv;
+        return true;
+    }
+};
+
+// KV tiles an item needs: keys 0 .. (last position any of its rows sees).
+__device__ __forceinline__ int item_tiles(const Params &p, const Item &it) {
+    const int last_row = min((it.mt + 1) * kBM, it.n * p.G) - 1;
+    const int max_pos = it.L - it.n + last_row / p.G;
+    return (max_pos + kBN) / kBN;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid_constant__ Params p) {
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sQ = base;
+    unsigned char *sK = sQ + C::kQBytes;            // 2 stages
+    unsigned char *sV = sK + 2 * C::kTileBytes;     // 2 stages
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sV + 2 * C::kTileBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int i = 0; i < B_COUNT; ++i) {
+            const bool four = i == B_PFULL || i == B_PFULL1 || i == B_OFREE;
+            mbar_init(&bar[i], four ? 4 : 1);
+        }
+        fence_mbar_init();
+        prefetch_tensor_map(&p.tmQ);
+        prefetch_tensor_map(&p.tmK);
+        prefetch_tensor_map(&p.tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    Walker walk;
+    walk.begin(&p, lane);
+    Item it;
+
+    auto fail = [&](void) {
+        flag(p.status, PA_CHECK_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // =================== TMA producer ===================
+        long long t = 0;  // KV tiles issued so far (both rings advance per tile)
+        int items = 0;
+        bool ok = true;
+        long long lastK = -1, lastV = -1;
+        for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x, ++items) {
+            const int nt = item_tiles(p, it);
+            const int32_t *row = p.bt + (long long)it.r * p.MB;
+            const int ctx_pages = (it.L + kPage - 1) / kPage;
+            if (lane == 0) {
+                if (!mbar_wait(&bar[B_QEMPTY], (items & 1) ^ 1)) ok = false;
+                else {
+                    mbar_arrive_expect_tx(&bar[B_QFULL], C::kQBytes);
+                    const int tok0 = it.qstart + it.mt * (kBM / p.G);
+#pragma unroll
+                    for (int h = 0; h < C::kHalves; ++h)
+                        tma_load_3d(sQ + h * (kBM * 128), &p.tmQ, &bar[B_QFULL], h * 64,
+                                    it.g * p.G, tok0);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            for (int j = 0; ok && j < nt; ++j, ++t) {
+                const int pg0 = j * kPagesPerTile;
+                const int npg = min(kPagesPerTile, ctx_pages - pg0);
+                int blk = 0;
+                if (lane < npg) {
+                    blk = row[pg0 + lane];
+                    if (blk < 0 || blk >= p.NB) {
+                        flag(p.status, PA_CHECK_BLOCK_ID);
+                        blk = 0;
+                    }
+                }
+                const int st = (int)(t & 1);
+                const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                const uint32_t bytes = (uint32_t)npg * C::kHalves * C::kPageHalfBytes;
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {
+                    uint64_t *fullb = &bar[(kv ? B_VFULL : B_KFULL) + st];
+                    uint64_t *emptyb = &bar[(kv ? B_VEMPTY : B_KEMPTY) + st];
+                    unsigned char *dst = (kv ? sV : sK) + st * C::kTileBytes;
+                    if (lane == 0) {
+                        if (!mbar_wait(emptyb, ph ^ 1)) ok = false;
+                        else mbar_arrive_expect_tx(fullb, bytes);
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    // lanes 0..npg-1 each issue their page's halves
+                    if (lane < npg) {
+#pragma unroll
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(dst + h * C::kHalfBytes + lane * C::kPageHalfBytes,
+                                        kv ? &p.tmV : &p.tmK, fullb, h * 64, it.g, blk * kPage);
+                    }
+                    if (kv) lastV = t; else lastK = t;
+                }
+            }
+            if (*abort_flag) ok = false;
+        }
+        if (!ok) fail();
+        // Drain: the last copies issued into each ring must have landed.
+        if (lane == 0) {
+            if (lastK >= 0) mbar_wait(&bar[B_KFULL + (int)(lastK & 1)], (uint32_t)((lastK >> 1) & 1));
+            if (lastV >= 0) mbar_wait(&bar[B_VFULL + (int)(lastV & 1)], (uint32_t)((lastV >> 1) & 1));
+        }
+    } else if (warp == 1) {
+        // =================== MMA issuer ===================
+        const uint32_t idQK = instr_desc<T>(kBM, kBN, 0);
+        const uint32_t idPV = instr_desc<T>(kBM, D, 1);
+        long long t0 = 0;
+        int items = 0;
+        bool ok = true;
+        for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x, ++items) {
+            const int nt = item_tiles(p, it);
+            if (lane == 0) {
+                if (!mbar_wait(&bar[B_QFULL], items & 1)) ok = false;
+                for (int j = 0; ok && j <= nt; ++j) {
+                    if (j < nt) {
+                        const long long t = t0 + j;
+                        const int st = (int)(t & 1);
+                        if (!mbar_wait(&bar[B_KFULL + st], (uint32_t)((t >> 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t dS = tmem + (uint32_t)st * 128;
+                        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * C::kTileBytes);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                            const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+                            mma_ss(dS, smem_desc_sw128(q0 + off, 16, 1024),
+                                   smem_desc_sw128(k0 + koff, 16, 1024), idQK, kk > 0);
+                        }
+                        mma_commit(&bar[B_SFULL + st]);
+                        mma_commit(&bar[B_KEMPTY + st]);
+                        if (j == nt - 1) mma_commit(&bar[B_QEMPTY]);
+                    }
+                    if (j >= 1) {
+                        const long long t = t0 + j - 1;
+                        const int st = (int)(t & 1);
+                        const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                        if (!mbar_wait(&bar[B_PFULL + st], ph) || !mbar_wait(&bar[B_VFULL + st], ph) ||
+                            (j == 1 && !mbar_wait(&bar[B_OFREE], (items & 1) ^ 1))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t v0 = smem_u32(sV + st * C::kTileBytes);
+                        const uint32_t aP = tmem + (uint32_t)st * 128;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ts(tmem + C::kColO, aP + 8 * kk,
+                                   smem_desc_sw128(v0 + kk * 2048, C::kHalfBytes, 1024), idPV,
+                                   (j > 1 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bar[B_VEMPTY + st]);
+                        mma_commit(&bar[B_ODONE + st]);
+                    }
+                    if (*abort_flag) ok = false;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            t0 += nt;
+        }
+        if (!ok && lane == 0) fail();
+        if (lane == 0) {
+            // Every MMA issued must be complete before TMEM is released.
+            mma_commit(&bar[B_DRAIN]);
+            mbar_wait(&bar[B_DRAIN], 0);
+        }
+    } else {
+        // =================== softmax + epilogue (warps 2..5) ===================
+        const int sub = warp & 3;                  // TMEM sub-partition of this warp
+        const int row = sub * 32 + lane;           // tile row = TMEM lane
+        const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
+        long long t0 = 0;
+        int items = 0;
+        bool ok = true;
+        for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x, ++items) {
+            const int nt = item_tiles(p, it);
+            const int rr = it.mt * kBM + row;
+            const bool valid = rr < it.n * p.G;
+            const int tl = rr / p.G;
+            const int pos = valid ? it.L - it.n + tl : -1;  // last key this row sees
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < nt; ++j) {
+                const long long t = t0 + j;
+                const int st = (int)(t & 1);
+                const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                if (!mbar_wait_warp(&bar[B_SFULL + st], ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int key0 = j * kBN;
+                float s[kBN];
+#pragma unroll
+                for (int c = 0; c < kBN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_addr + (uint32_t)st * 128 + c, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(r[e]);
+                }
+                float mx = -INFINITY;
+                const bool full_tile = key0 + kBN - 1 <= pos;
+                if (full_tile) {
+#pragma unroll
+                    for (int k = 0; k < kBN; ++k) {
+                        s[k] *= p.qscale;
+                        mx = fmaxf(mx, s[k]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kBN; ++k) {
+                        s[k] = key0 + k <= pos ? s[k] * p.qscale : -INFINITY;
+                        mx = fmaxf(mx, s[k]);
+                    }
+                }
+                const bool need = mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx > -INFINITY);
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    // O holds PV of tiles < j: wait for the last of them, then
+                    // rescale this warp's rows in TMEM.
+                    const long long tp = t - 1;
+                    if (!mbar_wait_warp(&bar[B_ODONE + (int)(tp & 1)], (uint32_t)((tp >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lane_addr + C::kColO + c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(tmem + lane_addr + C::kColO + c, r);
+                    }
+                    tmem_wait_st();
+                    if (need) l *= alpha;
+                }
+                if (need) m_ref = mx;
+                // P = exp2(s - m_ref), packed in pairs, written over S.
+                float sum = 0.f;
+#pragma unroll
+                for (int c = 0; c < kBN; c += 64) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float a = m_ref == -INFINITY ? 0.f : fast_exp2(s[c + 2 * e] - m_ref);
+                        const float b = m_ref == -INFINITY ? 0.f : fast_exp2(s[c + 2 * e + 1] - m_ref);
+                        sum += a + b;
+                        w[e] = Elt<T>::pack2(a, b);
+                    }
+                    tmem_st32(tmem + lane_addr + (uint32_t)st * 128 + c / 2, w);
+                }
+                tmem_wait_st();
+                l += sum;
+                if (j == nt - 1 && it.L < key0 + kBN) {
+                    // Keys past the context in the last tile: their V rows hold
+                    // stale data (or nothing was loaded); make them zero so
+                    // 0 * V stays 0 in the tensor core.  All four warps reach
+                    // the barrier below even if the wait timed out.
+                    const bool landed = mbar_wait_warp(&bar[B_VFULL + st], ph);
+                    if (landed) {
+                        unsigned char *vt = sV + st * C::kTileBytes;
+                        const int first = it.L - key0;
+                        const int rows = kBN - first;
+                        for (int x = row; x < rows * C::kHalves * 8; x += kBM) {
+                            const int h = x / (rows * 8), rem = x % (rows * 8);
+                            *reinterpret_cast<uint4 *>(vt + h * C::kHalfBytes +
+                                                       (first + rem / 8) * 128 + (rem % 8) * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    named_bar_sync(1, 128);
+                    if (!landed) {
+                        ok = false;
+                        break;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_PFULL + st]);
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l for this row
+            const long long tl_last = t0 + nt - 1;
+            if (!mbar_wait_warp(&bar[B_ODONE + (int)(tl_last & 1)], (uint32_t)((tl_last >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            T *dst = reinterpret_cast<T *>(p.out) +
+                     ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + rr % p.G) * D;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_addr + C::kColO + c, r);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v;
+                        v.x = Elt<T>::pack2(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
+                        v.y = Elt<T>::pack2(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+                        v.z = Elt<T>::pack2(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
+                        v.w = Elt<T>::pack2(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + c + e) = v;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_OFREE]);
+            t0 += nt;
+            if (*abort_flag) ok = false;
+        }
+        if (!ok) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+// 3-D TMA map, 128-byte swizzle, 64-element inner box: q as [T][Hq][D] with a
+// {64, G, 128/G} box, or a pool as [NB*bs][Hkv][D] with a {64, 1, 16} box.
+bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint32_t b1, uint32_t b2) {
+    static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    if (!enc) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {64u, b1, b2};
+    const cuuint32_t es[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int D>
+pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) {
+    using C = Cfg<D>;
+    static bool configured[64] = {};
+    int dev = 0;
+    PA_TRY_CUDA(cudaGetDevice(&dev));
+    if (dev >= 64 || !configured[dev]) {
+        PA_TRY_CUDA(cudaFuncSetAttribute(paged_prefill_kernel<T, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem));
+        if (dev < 64) configured[dev] = true;
+    }
+    long long grid = num_sms();
+    if (items < grid) grid = items;
+    if (grid < 1) return PA_OK;
+    paged_prefill_kernel<T, D><<<(int)grid, kThreads, C::kSmem, stream>>>(prm);
+    PA_TRY_CUDA(cudaGetLastError());
+    note_launch();
+    return PA_OK;
+}
+
+}  // namespace prefill
+
+int prefill_tau(const AttnArgs &a) {
+    const int G = a.Hq / a.Hkv;
+    if ((a.D != 64 && a.D != 128) || G < 1 || 128 % G != 0) return INT_MAX;
+    return prefill::kTauDefault;
+}
+
+pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
+    using namespace prefill;
+    if (tau == INT_MAX || a.max_q <= tau) return PA_OK;
+    Params prm;
+    memset(&prm, 0, sizeof prm);
+    const int G = a.Hq / a.Hkv;
+    const uint64_t slots = (uint64_t)a.NB * a.bs;
+    if (!encode_sw128(&prm.tmQ, a.q, a.D, a.Hq, a.T, G, kBM / G) ||
+        !encode_sw128(&prm.tmK, a.kc, a.D, a.Hkv, slots, 1, kPage) ||
+        !encode_sw128(&prm.tmV, a.vc, a.D, a.Hkv, slots, 1, kPage))
+        return PA_ERR_CUDA;
+    prm.out = a.out;
+    prm.bt = a.bt;
+    prm.qsl = a.qsl;
+    prm.seq_lens = a.seq_lens;
+    prm.R = a.R;
+    prm.T = a.T;
+    prm.MB = a.MB;
+    prm.NB = a.NB;
+    prm.Hq = a.Hq;
+    prm.Hkv = a.Hkv;
+    prm.G = G;
+    prm.tau = tau;
+    prm.qscale = a.scale * 1.4426950408889634f;
+    prm.status = status_word();
+    if (!prm.status) return PA_ERR_CUDA;
+    // upper bound on the row tiles
+    const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T * G + kBM - 1) / kBM);
+    const bool bf16 = a.dtype == PA_BF16;
+    if (a.D == 128)
+        return bf16 ? launch_typed<__nv_bfloat16, 128>(prm, items, stream)
+                    : launch_typed<__half, 128>(prm, items, stream);
+    return bf16 ? launch_typed<__nv_bfloat16, 64>(prm, items, stream)
+                : launch_typed<__half, 64>(prm, items, stream);
+}
+
+}  // namespace pa

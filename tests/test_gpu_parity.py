@@ -110,6 +110,57 @@ def test_prompt_chunk_longer_than_a_partition(group, ws):
     _check_attention(res, ref)
 
 
+@pytest.mark.parametrize("d,dtype,group,hkv", [(128, "bf16", 4, 2), (128, "fp16", 8, 1),
+                                               (64, "bf16", 2, 2), (64, "fp16", 1, 3),
+                                               (128, "bf16", 16, 1)])
+def test_tensor_core_prefill_chunks(d, dtype, group, hkv):
+    # Chunks longer than 16 tokens run on the tensor-core kernel: several row
+    # tiles, several key tiles, ragged tails, next to short requests that stay
+    # on the split-K kernel.
+    rng = np.random.default_rng(d + group)
+    nst = [300, 1, 17, 5, 129]
+    nct = [0, 400, 250, 33, 700]
+    w = workloads._make("prefill-mix", nst, nct, rng, hkv * group, hkv, d, dtype)
+    vals = workloads.make_values(w, 11)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_attention(res, ref)
+
+
+def test_head_ratio_without_tensor_path():
+    # 128 is not a multiple of 3 q heads per kv head: every request, long or
+    # short, runs on the split-K kernel.
+    rng = np.random.default_rng(3)
+    w = workloads._make("g3", [90, 1, 20], [10, 300, 0], rng, 6, 2, 128, "bf16")
+    vals = workloads.make_values(w, 3)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    _check_attention(res, ref)
+
+
+@pytest.mark.parametrize("long_chunk", [False, True])
+def test_stale_slots_past_the_context_are_never_used(long_chunk):
+    # Slots of a request's last block past its context hold NaN: neither
+    # kernel may let them reach the output.
+    rng = np.random.default_rng(9)
+    nst = [200, 1, 3] if long_chunk else [1, 1, 3]
+    nct = [37, 50, 61]
+    w = workloads._make("nan-tail", nst, nct, rng, 8, 2, 128, "bf16")
+    vals = workloads.make_values(w, 9)
+    kc, vc = vals["key_cache"], vals["value_cache"]
+    for r in range(w.num_reqs):
+        L = int(w.context_lens[r])
+        last = int(w.block_table[r][(L - 1) // 16])
+        kc[last, L % 16 or 16:] = float("nan")
+        vc[last, L % 16 or 16:] = float("nan")
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    _check_attention(res, ref)
+
+
 @pytest.mark.parametrize("d,dtype,group", [(64, "bf16", 1), (64, "fp16", 8), (128, "fp16", 2),
                                            (128, "bf16", 8), (128, "bf16", 3)])
 def test_head_shapes(d, dtype, group):
