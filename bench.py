@@ -41,6 +41,7 @@ METRIC = "paged-attn step tokens/s"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -73,13 +74,39 @@ def kv_bytes(w) -> tuple[int, int]:
 
 
 def load_peaks():
+    """(hbm GB/s, bf16 TFLOP/s burst, source) from MEASURED_PEAKS.json."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+TENSOR_PATH_MIN_TOKENS = 17   # requests with more query tokens run on the tensor-core kernel
+
+
+def causal_flops(w, mask) -> int:
+    """4*D*Hq per visible (query, key) pair: QK^T and PV, causal-exact."""
+    n = w.num_scheduled_tokens.astype(np.int64)[mask]
+    c = w.num_computed_tokens.astype(np.int64)[mask]
+    pairs = int((n * c + n * (n + 1) // 2).sum())
+    return 4 * w.head_dim * w.num_q_heads * pairs
+
+
+def sub_batch(w, mask, q, bt_dev, qsl_host, sl_host, dev):
+    """The requests selected by `mask` as a batch of their own (inputs for
+    pa_attention), built outside any timed region."""
+    import torch
+    reqs = np.nonzero(mask)[0]
+    toks = np.concatenate([np.arange(qsl_host[r], qsl_host[r + 1]) for r in reqs])
+    n = (qsl_host[reqs + 1] - qsl_host[reqs]).astype(np.int32)
+    qsl = torch.from_numpy(np.concatenate([[0], np.cumsum(n)]).astype(np.int32)).to(dev)
+    sl = torch.from_numpy(sl_host[reqs].astype(np.int32)).to(dev)
+    qs = q.index_select(0, torch.from_numpy(toks).to(dev)).contiguous()
+    bts = bt_dev.index_select(0, torch.from_numpy(reqs).to(dev)).contiguous()
+    return qs, qsl, sl, bts, int(n.max()), int(sl_host[reqs].max())
 
 
 def kernel_source_hash() -> str:
@@ -354,21 +381,64 @@ def run_ours(args):
     if status != pa.PA_OK:
         raise RuntimeError(f"device checks failed: {pa.check_bits(detail)}")
 
-    # ---- roofline of the attention call (decode kernel + merge pass)
+    # ---- rooflines.  The attention call is timed live above; when the batch
+    # mixes both request classes, each class is also timed alone (as a batch
+    # of its own, same kernels) so each kernel gets its own roofline.
+    hbm_peak, tf_peak, peak_kind = load_peaks()
+    long_mask = w.num_scheduled_tokens >= TENSOR_PATH_MIN_TOKENS
+    short_mask = ~long_mask
+    qsl_host = np.concatenate([[0], np.cumsum(w.num_scheduled_tokens)]).astype(np.int64)
+    sl_host = w.context_lens.astype(np.int64)
+
+    def time_sub(mask):
+        qs, qsl_s, sl_s, bt_s, mq, ms = sub_batch(w, mask, q, bt, qsl_host, sl_host, dev)
+        os_ = torch.empty_like(qs)
+        evs = []
+        for k in range(max(args.warmup, 1) + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pa.pa_attention(qs, kc, vc, bt_s, qsl_s, sl_s, mq, ms, w.scale, os_, ws)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs[max(args.warmup, 1):]])) / 1e3
+
     logical, unique = kv_bytes(w)
-    attn_avg_s = float(np.mean(attn_ms)) / 1e3
-    alg = unique if args.workload == "shared_prefix" else logical
-    peak, peak_kind = load_peaks()
-    achieved = alg / attn_avg_s / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
-                "kernel": "pa_attention (paged_decode_kernel + merge_kernel)",
-                "algorithmic_bytes_per_launch": alg, "avg_launch_us": attn_avg_s * 1e6,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "frac_of_8TBps": achieved / 8000.0}
-    if args.workload == "shared_prefix":
-        roofline["effective_logical_GBps"] = logical / attn_avg_s / 1e9
+    if long_mask.any() and short_mask.any():
+        decode_s = time_sub(short_mask)
+        alg = (int(sl_host[short_mask].sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+               + int(short_mask.sum()) * w.num_q_heads * w.head_dim * 4)
+        what = "decode-class requests alone (paged_decode_kernel + merge_kernel)"
+    else:
+        decode_s = float(np.mean(attn_ms)) / 1e3
+        alg = unique if args.workload == "shared_prefix" else logical
+        what = "pa_attention (paged_decode_kernel + merge_kernel)"
+    roofline = None
+    if short_mask.any():
+        achieved = alg / decode_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": recorded_traffic(args.workload),
+                    "kernel": what, "algorithmic_bytes_per_launch": alg,
+                    "avg_launch_us": decode_s * 1e6,
+                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                    "frac_of_8TBps": achieved / 8000.0}
+        if args.workload == "shared_prefix":
+            roofline["effective_logical_GBps"] = logical / decode_s / 1e9
+    roofline_prefill = None
+    if long_mask.any():
+        pre_s = time_sub(long_mask) if short_mask.any() else float(np.mean(attn_ms)) / 1e3
+        flops = causal_flops(w, long_mask)
+        achieved = flops / pre_s / 1e12
+        roofline_prefill = {"bound": "tensor", "achieved": achieved, "peak": tf_peak,
+                            "unit": "TFLOP/s", "frac": achieved / tf_peak, "traffic": None,
+                            "kernel": "paged_prefill_kernel (tcgen05), prefill-class requests "
+                                      "alone", "flops_per_launch": flops,
+                            "avg_launch_us": pre_s * 1e6,
+                            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, "
+                                           "burst; fp16 runs at the same dense rate)"}
+        if roofline is None:
+            roofline = roofline_prefill
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -387,6 +457,7 @@ def run_ours(args):
                        "kv_bytes": w.kv_read_bytes(), "parallelism": f"replicas x{world}",
                        "l2": "flushed between steps (256 MB write outside the timed events)"},
             "roofline": roofline,
+            "roofline_prefill": roofline_prefill,
             "cpu_baseline": cpu,
             "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},

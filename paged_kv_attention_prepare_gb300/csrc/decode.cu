@@ -746,10 +746,14 @@ pa_status dispatch_rpi(int rpi, Params &prm, long long grid, bool merge, cudaStr
     }
 }
 
-// Rows per item: enough for all heads of a group and a few query tokens, at
-// most 8 (register budget).
+// Rows per item: all heads of a kv group (at most 8, the register budget).
+// With 4+ heads per group a single-token decode already fills the item, so
+// short multi-token requests are split into more items rather than making
+// every decode item carry empty rows; with fewer heads per group a few query
+// tokens share an item.
 inline int rows_per_item(int G, int max_q) {
-    const long long rows = (long long)G * (max_q > 0 ? max_q : 1);
+    long long rows = (long long)G * (max_q > 0 ? max_q : 1);
+    if (G >= 4) rows = G;
     int rpi = 1;
     while (rpi < 8 && rpi < rows) rpi <<= 1;
     return rpi;
