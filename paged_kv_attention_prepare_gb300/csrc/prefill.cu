@@ -23,8 +23,10 @@
 // TMEM) when a tile's max exceeds it by more than 2^8; otherwise P uses the
 // old reference, which keeps every P <= 256 and the result exact.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM allocation), 2..5 = softmax
-// and epilogue (TMEM lanes 32*(warp%4)..+31).  Every mbarrier wait is bounded.
+// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM allocation), 2..9 = softmax
+// and epilogue: warp w reads TMEM lanes 32*(w%4)..+31, and the two warps of a
+// lane group split each row's columns in halves, exchanging row max and sum
+// through shared memory.  Every mbarrier wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -40,7 +42,8 @@ constexpr int kBM = 128;          // rows per tile
 constexpr int kBN = 128;          // keys per KV tile
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kBN / kPage;
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;   // two per TMEM sub-partition, one per column half
+constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kTauDefault = 16;           // longer query chunks take this kernel
@@ -66,7 +69,7 @@ struct Cfg {
     static constexpr int kTileBytes = kBN * D * 2;
     static constexpr int kHalfBytes = kBN * 128;     // one 64-dim half of a K/V tile
     static constexpr int kPageHalfBytes = kPage * 128;
-    static constexpr int kSmem = kQBytes + 4 * kTileBytes + 512 + 1024;
+    static constexpr int kSmem = kQBytes + 4 * kTileBytes + 512 + 3 * 2 * kBM * 4 + 1024;
     static constexpr uint32_t kColO = 256;
 };
 
@@ -248,6 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
     uint64_t *bar = reinterpret_cast<uint64_t *>(sV + 2 * C::kTileBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // Row max exchange between the two warps of a lane group, double-buffered
+    // by tile parity ([2][2 halves][128 rows]); row sums at the end of an item.
+    float *xmax = reinterpret_cast<float *>(bar + B_COUNT + 2);
+    float *xsum = xmax + 2 * 2 * kBM;                            // [2 halves][128 rows]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -260,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
     if (tid == 0) {
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i) {
-            const bool four = i == B_PFULL || i == B_PFULL1 || i == B_OFREE;
-            mbar_init(&bar[i], four ? 4 : 1);
+            const bool per_warp = i == B_PFULL || i == B_PFULL1 || i == B_OFREE;
+            mbar_init(&bar[i], per_warp ? kSoftmaxWarps : 1);
         }
         fence_mbar_init();
         prefetch_tensor_map(&p.tmQ);
@@ -413,10 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
             mbar_wait(&bar[B_DRAIN], 0);
         }
     } else {
-        // =================== softmax + epilogue (warps 2..5) ===================
+        // =================== softmax + epilogue (warps 2..9) ===================
         const int sub = warp & 3;                  // TMEM sub-partition of this warp
+        const int half = (warp - 2) >> 2;          // which 64 of the row's 128 keys
         const int row = sub * 32 + lane;           // tile row = TMEM lane
+        const int pair_bar = 1 + sub;              // the two warps sharing these rows
         const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
+        const float c = p.qscale;
         long long t0 = 0;
         int items = 0;
         bool ok = true;
@@ -436,35 +446,42 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                     break;
                 }
                 tc_fence_after();
-                const int key0 = j * kBN;
-                float s[kBN];
+                const int key0 = j * kBN + half * 64;
+                float2 x[32];
 #pragma unroll
-                for (int c = 0; c < kBN; c += 32) {
+                for (int cc = 0; cc < 64; cc += 32) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lane_addr + (uint32_t)st * 128 + c, r);
+                    tmem_ld32(tmem + lane_addr + (uint32_t)st * 128 + half * 64 + cc, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c + e] = __uint_as_float(r[e]);
+                    for (int e = 0; e < 16; ++e)
+                        x[cc / 2 + e] = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
                 }
                 float mx = -INFINITY;
-                const bool full_tile = key0 + kBN - 1 <= pos;
-                if (full_tile) {
+                const float2 c2 = make_float2(c, c);
+                if (key0 + 63 <= pos) {
 #pragma unroll
-                    for (int k = 0; k < kBN; ++k) {
-                        s[k] *= p.qscale;
-                        mx = fmaxf(mx, s[k]);
+                    for (int e = 0; e < 32; ++e) {
+                        x[e] = __fmul2_rn(x[e], c2);
+                        mx = fmaxf(mx, fmaxf(x[e].x, x[e].y));
                     }
                 } else {
 #pragma unroll
-                    for (int k = 0; k < kBN; ++k) {
-                        s[k] = key0 + k <= pos ? s[k] * p.qscale : -INFINITY;
-                        mx = fmaxf(mx, s[k]);
+                    for (int e = 0; e < 32; ++e) {
+                        x[e] = __fmul2_rn(x[e], c2);
+                        if (key0 + 2 * e > pos) x[e].x = -INFINITY;
+                        if (key0 + 2 * e + 1 > pos) x[e].y = -INFINITY;
+                        mx = fmaxf(mx, fmaxf(x[e].x, x[e].y));
                     }
                 }
-                const bool need = mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx > -INFINITY);
+                float *xm = xmax + (int)(t & 1) * 2 * kBM;
+                xm[half * kBM + row] = mx;
+                named_bar_sync(pair_bar, 64);
+                mx = fmaxf(mx, xm[(half ^ 1) * kBM + row]);
+                const bool need = mx > m_ref + kRescaleThreshold;
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
                     // O holds PV of tiles < j: wait for the last of them, then
-                    // rescale this warp's rows in TMEM.
+                    // rescale this warp's half of its rows in TMEM.
                     const long long tp = t - 1;
                     if (!mbar_wait_warp(&bar[B_ODONE + (int)(tp & 1)], (uint32_t)((tp >> 1) & 1))) {
                         ok = false;
@@ -473,53 +490,54 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                     tc_fence_after();
                     const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
 #pragma unroll
-                    for (int c = 0; c < D; c += 32) {
+                    for (int cc = 0; cc < D / 2; cc += 32) {
                         uint32_t r[32];
-                        tmem_ld32(tmem + lane_addr + C::kColO + c, r);
+                        const uint32_t a = tmem + lane_addr + C::kColO + half * (D / 2) + cc;
+                        tmem_ld32(a, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(tmem + lane_addr + C::kColO + c, r);
+                        tmem_st32(a, r);
                     }
                     tmem_wait_st();
                     if (need) l *= alpha;
                 }
                 if (need) m_ref = mx;
-                // P = exp2(s - m_ref), packed in pairs, written over S.
-                float sum = 0.f;
+                // P = exp2(x - m_ref), packed in pairs, written over this half of S.
+                const float2 mneg = make_float2(-m_ref, -m_ref);
+                float2 acc = make_float2(0.f, 0.f);
+                uint32_t w[32];
 #pragma unroll
-                for (int c = 0; c < kBN; c += 64) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float a = m_ref == -INFINITY ? 0.f : fast_exp2(s[c + 2 * e] - m_ref);
-                        const float b = m_ref == -INFINITY ? 0.f : fast_exp2(s[c + 2 * e + 1] - m_ref);
-                        sum += a + b;
-                        w[e] = Elt<T>::pack2(a, b);
-                    }
-                    tmem_st32(tmem + lane_addr + (uint32_t)st * 128 + c / 2, w);
+                for (int e = 0; e < 32; ++e) {
+                    float2 y = __fadd2_rn(x[e], mneg);
+                    y.x = fast_exp2(y.x);
+                    y.y = fast_exp2(y.y);
+                    if (m_ref == -INFINITY) y = make_float2(0.f, 0.f);
+                    acc = __fadd2_rn(acc, y);
+                    w[e] = Elt<T>::pack2(y.x, y.y);
                 }
+                tmem_st32(tmem + lane_addr + (uint32_t)st * 128 + half * 32, w);
                 tmem_wait_st();
-                l += sum;
-                if (j == nt - 1 && it.L < key0 + kBN) {
+                l += acc.x + acc.y;
+                if (j == nt - 1 && it.L < j * kBN + kBN) {
                     // Keys past the context in the last tile: their V rows hold
                     // stale data (or nothing was loaded); make them zero so
-                    // 0 * V stays 0 in the tensor core.  All four warps reach
-                    // the barrier below even if the wait timed out.
+                    // 0 * V stays 0 in the tensor core.  All softmax warps
+                    // reach the barrier below even if the wait timed out.
                     const bool landed = mbar_wait_warp(&bar[B_VFULL + st], ph);
                     if (landed) {
                         unsigned char *vt = sV + st * C::kTileBytes;
-                        const int first = it.L - key0;
+                        const int first = it.L - j * kBN;
                         const int rows = kBN - first;
-                        for (int x = row; x < rows * C::kHalves * 8; x += kBM) {
-                            const int h = x / (rows * 8), rem = x % (rows * 8);
+                        for (int xx = half * kBM + row; xx < rows * C::kHalves * 8; xx += 2 * kBM) {
+                            const int h = xx / (rows * 8), rem = xx % (rows * 8);
                             *reinterpret_cast<uint4 *>(vt + h * C::kHalfBytes +
                                                        (first + rem / 8) * 128 + (rem % 8) * 16) =
                                 make_uint4(0, 0, 0, 0);
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
-                    named_bar_sync(1, 128);
+                    named_bar_sync(5, kSoftmaxWarps * 32);
                     if (!landed) {
                         ok = false;
                         break;
@@ -530,7 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                 if (lane == 0) mbar_arrive(&bar[B_PFULL + st]);
             }
             if (!ok) break;
-            // ---- epilogue: O / l for this row
+            // ---- epilogue: O / l for this row's half of the columns
+            xsum[half * kBM + row] = l;
+            named_bar_sync(pair_bar, 64);
+            l += xsum[(half ^ 1) * kBM + row];
             const long long tl_last = t0 + nt - 1;
             if (!mbar_wait_warp(&bar[B_ODONE + (int)(tl_last & 1)], (uint32_t)((tl_last >> 1) & 1))) {
                 ok = false;
@@ -539,11 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             T *dst = reinterpret_cast<T *>(p.out) +
-                     ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + rr % p.G) * D;
+                     ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + rr % p.G) * D + half * (D / 2);
 #pragma unroll
-            for (int c = 0; c < D; c += 32) {
+            for (int cc = 0; cc < D / 2; cc += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_addr + C::kColO + c, r);
+                tmem_ld32(tmem + lane_addr + C::kColO + half * (D / 2) + cc, r);
                 tmem_wait_ld();
                 if (valid) {
 #pragma unroll
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                         v.y = Elt<T>::pack2(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
                         v.z = Elt<T>::pack2(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
                         v.w = Elt<T>::pack2(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + c + e) = v;
+                        *reinterpret_cast<uint4 *>(dst + cc + e) = v;
                     }
                 }
             }
