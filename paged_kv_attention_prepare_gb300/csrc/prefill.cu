@@ -6,27 +6,29 @@
 // path (cu_seqlens_q, seqused_k, block_table).  Same maths as the split-K
 // kernel: out = softmax(scale * q K^T, causal) V per request and kv head.
 //
-// Work item = (request, kv head g, 128-row tile).  A row is one (query token,
-// q head of group g) pair, so a K/V tile serves all Hq/Hkv heads of the
-// group; the Q tile is one 3-D TMA box {64 dims, G heads, 128/G tokens} per
-// 64-dim half.  Items run on persistent CTAs (one per SM), heaviest first.
+// Work item = (request, kv head g, 256-row pair of tiles).  A row is one
+// (query token, q head of group g) pair, so a K/V tile serves all Hq/Hkv
+// heads of the group and both 128-row tiles ("slots" A and B) of the pair;
+// each Q tile is one 3-D TMA box {64 dims, G heads, 128/G tokens} per 64-dim
+// half.  Items run on persistent CTAs (one per SM), heaviest first.
 //
 // Per 128-key KV tile j (8 pages of 16 tokens, each page one TMA box per
-// 64-dim half, 128-byte swizzle, addressed through the block table):
-//   S_j = Q K_j^T         tcgen05.mma, A = Q (smem, K-major), B = K (smem,
-//                         K-major), fp32 accumulator in TMEM (double buffer)
-//   P_j = exp2(S_j*c - m) softmax warps, one row per thread (tcgen05.ld),
-//                         written back over S_j in TMEM as bf16/fp16
-//   O  += P_j V_j         tcgen05.mma, A = P (TMEM), B = V (smem, MN-major)
-// QK_{j+1} is issued before PV_j so the tensor core works while the softmax
-// warps process tile j.  The running max is only moved (and O rescaled in
-// TMEM) when a tile's max exceeds it by more than 2^8; otherwise P uses the
-// old reference, which keeps every P <= 256 and the result exact.
+// 64-dim half, 128-byte swizzle, addressed through the block table), for
+// each slot X in {A, B}:
+//   S_X = Q_X K_j^T       tcgen05.mma, A = Q (smem, K-major), B = K (smem,
+//                         K-major), fp32 accumulator in TMEM
+//   P_X = exp2(S_X*c - m) the slot's softmax warps, one row per thread
+//                         (tcgen05.ld), written back over S_X in TMEM
+//   O_X += P_X V_j        tcgen05.mma, A = P (TMEM), B = V (smem, MN-major)
+// The MMA warp issues PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1): while one
+// slot's softmax runs, the tensor core works for the other slot.  The
+// running max only moves (and O is rescaled in TMEM) when a tile's max
+// exceeds it by more than 2^8; otherwise P keeps the old reference, which
+// bounds every P by 256 and leaves the result exact.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM allocation), 2..9 = softmax
-// and epilogue: warp w reads TMEM lanes 32*(w%4)..+31, and the two warps of a
-// lane group split each row's columns in halves, exchanging row max and sum
-// through shared memory.  Every mbarrier wait is bounded.
+// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM allocation), 2..5 = slot A
+// softmax and epilogue, 6..9 = slot B; warp w reads TMEM lanes 32*(w%4)..+31.
+// Every mbarrier wait is bounded.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -42,7 +44,7 @@ constexpr int kBM = 128;          // rows per tile
 constexpr int kBN = 128;          // keys per KV tile
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kBN / kPage;
-constexpr int kSoftmaxWarps = 8;   // two per TMEM sub-partition, one per column half
+constexpr int kSoftmaxWarps = 8;   // four per slot
 constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
@@ -65,19 +67,26 @@ struct Params {
 template <int D>
 struct Cfg {
     static constexpr int kHalves = D / 64;
-    static constexpr int kQBytes = kBM * D * 2;
+    static constexpr int kQBytes = kBM * D * 2;          // one 128-row Q tile
     static constexpr int kTileBytes = kBN * D * 2;
-    static constexpr int kHalfBytes = kBN * 128;     // one 64-dim half of a K/V tile
+    static constexpr int kHalfBytes = kBN * 128;         // one 64-dim half of a K/V tile
     static constexpr int kPageHalfBytes = kPage * 128;
-    static constexpr int kSmem = kQBytes + 4 * kTileBytes + 512 + 3 * 2 * kBM * 4 + 1024;
-    static constexpr uint32_t kColO = 256;
+    static constexpr int kSmem = 2 * kQBytes + 4 * kTileBytes + 512 + 1024;
+    // TMEM columns: S_A 0, O_A 128, S_B 256, O_B 384
+    __device__ static constexpr uint32_t col_s(int slot) { return (uint32_t)slot * 256; }
+    __device__ static constexpr uint32_t col_o(int slot) { return (uint32_t)slot * 256 + 128; }
 };
 
 // Barrier slots (uint64) in shared memory.
 enum {
     B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
-    B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ODONE, B_ODONE1, B_OFREE,
-    B_DRAIN, B_COUNT
+    B_VEMPTY, B_VEMPTY1,
+    B_SFULL,      // [2] per slot: S_X ready
+    B_PFULL = B_SFULL + 2,   // [2] per slot: P_X written (one arrive per softmax warp)
+    B_ODONE = B_PFULL + 2,   // [2] per slot: PV_X done
+    B_OFREE = B_ODONE + 2,   // [2] per slot: O_X read out by the epilogue
+    B_DRAIN = B_OFREE + 2,
+    B_COUNT
 };
 
 // ---------------------------------------------------------------------------
@@ -162,12 +171,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
-// Work items: per request with more than tau tokens, Hkv x ceil(n*G/128)
-// tiles, ordered last row-tile first (the tile with the most keys), kv heads
+// Work items: per request with more than tau tokens, Hkv x ceil(n*G/256)
+// tile pairs, ordered last pair first (the tile with the most keys), kv heads
 // interleaved.  Every warp walks the request list itself.
 // ---------------------------------------------------------------------------
 
@@ -194,7 +213,7 @@ struct Walker {
             L = p->seq_lens[r];
             const bool sane = a >= 0 && b <= p->T && n >= 0 && L >= n &&
                               (L + kPage - 1) / kPage <= p->MB;
-            if (sane && n > p->tau) items = p->Hkv * ((n * p->G + kBM - 1) / kBM);
+            if (sane && n > p->tau) items = p->Hkv * ((n * p->G + 2 * kBM - 1) / (2 * kBM));
         }
         incl = items;
 #pragma unroll
@@ -225,16 +244,28 @@ struct Walker {
         it.qstart = __shfl_sync(0xffffffffu, a, src);
         it.r = rb + src;
         const int local = li - excl;
-        const int nm = (it.n * p->G + kBM - 1) / kBM;
+        const int nm = (it.n * p->G + 2 * kBM - 1) / (2 * kBM);
         it.g = local % p->Hkv;
-        it.mt = nm - 1 - local / p->Hkv;
+        it.mt = nm - 1 - local / p->Hkv;  // index of the 256-row pair
         return true;
     }
 };
 
-// KV tiles an item needs: keys 0 .. (last position any of its rows sees).
-__device__ __forceinline__ int item_tiles(const Params &p, const Item &it) {
-    const int last_row = min((it.mt + 1) * kBM, it.n * p.G) - 1;
+// The k-th item of CTA b: rounds of gridDim items, dealt left to right in
+// even rounds and right to left in odd ones, so the heavy items at the front
+// of the list spread evenly over the CTAs.
+__device__ __forceinline__ long long snake_item(int k) {
+    const long long round = (long long)k * gridDim.x;
+    return (k & 1) ? round + (gridDim.x - 1 - blockIdx.x) : round + blockIdx.x;
+}
+
+// KV tiles slot `slot` of an item needs: keys 0 .. (last position any of its
+// rows sees); 0 when the slot has no rows.
+__device__ __forceinline__ int slot_tiles(const Params &p, const Item &it, int slot) {
+    const int first_row = it.mt * 2 * kBM + slot * kBM;
+    const int nrows = it.n * p.G;
+    if (first_row >= nrows) return 0;
+    const int last_row = min(first_row + kBM, nrows) - 1;
     const int max_pos = it.L - it.n + last_row / p.G;
     return (max_pos + kBN) / kBN;
 }
@@ -245,16 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *sQ = base;
-    unsigned char *sK = sQ + C::kQBytes;            // 2 stages
+    unsigned char *sQ = base;                       // 2 tiles: slot A, slot B
+    unsigned char *sK = sQ + 2 * C::kQBytes;        // 2 stages
     unsigned char *sV = sK + 2 * C::kTileBytes;     // 2 stages
     uint64_t *bar = reinterpret_cast<uint64_t *>(sV + 2 * C::kTileBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    // Row max exchange between the two warps of a lane group, double-buffered
-    // by tile parity ([2][2 halves][128 rows]); row sums at the end of an item.
-    float *xmax = reinterpret_cast<float *>(bar + B_COUNT + 2);
-    float *xsum = xmax + 2 * 2 * kBM;                            // [2 halves][128 rows]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -267,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
     if (tid == 0) {
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i) {
-            const bool per_warp = i == B_PFULL || i == B_PFULL1 || i == B_OFREE;
-            mbar_init(&bar[i], per_warp ? kSoftmaxWarps : 1);
+            const bool per_warp = (i >= B_PFULL && i < B_PFULL + 2) || (i >= B_OFREE && i < B_OFREE + 2);
+            mbar_init(&bar[i], per_warp ? kSoftmaxWarps / 2 : 1);
         }
         fence_mbar_init();
         prefetch_tensor_map(&p.tmQ);
@@ -295,19 +322,23 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
         int items = 0;
         bool ok = true;
         long long lastK = -1, lastV = -1;
-        for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x, ++items) {
-            const int nt = item_tiles(p, it);
+        for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k, ++items) {
+            const int ntB = slot_tiles(p, it, 1);
+            const int nt = max(slot_tiles(p, it, 0), ntB);
             const int32_t *row = p.bt + (long long)it.r * p.MB;
             const int ctx_pages = (it.L + kPage - 1) / kPage;
             if (lane == 0) {
                 if (!mbar_wait(&bar[B_QEMPTY], (items & 1) ^ 1)) ok = false;
                 else {
-                    mbar_arrive_expect_tx(&bar[B_QFULL], C::kQBytes);
-                    const int tok0 = it.qstart + it.mt * (kBM / p.G);
+                    const int nslots = ntB > 0 ? 2 : 1;
+                    mbar_arrive_expect_tx(&bar[B_QFULL], nslots * C::kQBytes);
+                    for (int sl = 0; sl < nslots; ++sl) {
+                        const int tok0 = it.qstart + (it.mt * 2 + sl) * (kBM / p.G);
 #pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h)
-                        tma_load_3d(sQ + h * (kBM * 128), &p.tmQ, &bar[B_QFULL], h * 64,
-                                    it.g * p.G, tok0);
+                        for (int h = 0; h < C::kHalves; ++h)
+                            tma_load_3d(sQ + sl * C::kQBytes + h * (kBM * 128), &p.tmQ,
+                                        &bar[B_QFULL], h * 64, it.g * p.G, tok0);
+                    }
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -336,7 +367,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
-                    // lanes 0..npg-1 each issue their page's halves
                     if (lane < npg) {
 #pragma unroll
                         for (int h = 0; h < C::kHalves; ++h)
@@ -358,59 +388,87 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
         // =================== MMA issuer ===================
         const uint32_t idQK = instr_desc<T>(kBM, kBN, 0);
         const uint32_t idPV = instr_desc<T>(kBM, D, 1);
-        long long t0 = 0;
+        long long t0 = 0;           // KV tiles of earlier items
+        long long cnt[2] = {0, 0};  // tiles processed per slot (barrier phases)
+        int its[2] = {0, 0};        // items processed per slot
         int items = 0;
         bool ok = true;
-        for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x, ++items) {
-            const int nt = item_tiles(p, it);
+        for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k, ++items) {
+            int ns[2] = {slot_tiles(p, it, 0), slot_tiles(p, it, 1)};
+            const int nt = max(ns[0], ns[1]);
             if (lane == 0) {
-                if (!mbar_wait(&bar[B_QFULL], items & 1)) ok = false;
-                for (int j = 0; ok && j <= nt; ++j) {
-                    if (j < nt) {
-                        const long long t = t0 + j;
-                        const int st = (int)(t & 1);
-                        if (!mbar_wait(&bar[B_KFULL + st], (uint32_t)((t >> 1) & 1))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t dS = tmem + (uint32_t)st * 128;
-                        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK + st * C::kTileBytes);
+                const uint32_t q0 = smem_u32(sQ);
+                auto wait_or_fail = [&](uint64_t *b, uint32_t par) {
+                    if (ok && !mbar_wait(b, par)) ok = false;
+                    return ok;
+                };
+                auto issue_qk = [&](int slot, int kst) {
+                    const uint32_t qa = q0 + slot * C::kQBytes;
+                    const uint32_t ka = smem_u32(sK + kst * C::kTileBytes);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                            const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-                            mma_ss(dS, smem_desc_sw128(q0 + off, 16, 1024),
-                                   smem_desc_sw128(k0 + koff, 16, 1024), idQK, kk > 0);
-                        }
-                        mma_commit(&bar[B_SFULL + st]);
-                        mma_commit(&bar[B_KEMPTY + st]);
-                        if (j == nt - 1) mma_commit(&bar[B_QEMPTY]);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+                        const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+                        mma_ss(tmem + C::col_s(slot), smem_desc_sw128(qa + off, 16, 1024),
+                               smem_desc_sw128(ka + koff, 16, 1024), idQK, kk > 0);
                     }
-                    if (j >= 1) {
-                        const long long t = t0 + j - 1;
-                        const int st = (int)(t & 1);
-                        const uint32_t ph = (uint32_t)((t >> 1) & 1);
-                        if (!mbar_wait(&bar[B_PFULL + st], ph) || !mbar_wait(&bar[B_VFULL + st], ph) ||
-                            (j == 1 && !mbar_wait(&bar[B_OFREE], (items & 1) ^ 1))) {
-                            ok = false;
+                    mma_commit(&bar[B_SFULL + slot]);
+                };
+                wait_or_fail(&bar[B_QFULL], items & 1);
+                // tile 0: both slots' scores
+                if (ok && wait_or_fail(&bar[B_KFULL + (int)(t0 & 1)], (uint32_t)((t0 >> 1) & 1))) {
+                    tc_fence_after();
+                    for (int sl = 0; sl < 2; ++sl)
+                        if (ns[sl] > 0) issue_qk(sl, (int)(t0 & 1));
+                    mma_commit(&bar[B_KEMPTY + (int)(t0 & 1)]);
+                    if (nt == 1) mma_commit(&bar[B_QEMPTY]);
+                }
+                for (int j = 0; ok && j < nt; ++j) {
+                    const long long t = t0 + j;
+                    const int st = (int)(t & 1);
+                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                    bool v_ready = false, k_next_ready = false;
+                    const long long t1 = t + 1;
+                    for (int sl = 0; ok && sl < 2; ++sl) {
+                        if (j >= ns[sl]) continue;
+                        if (!wait_or_fail(&bar[B_PFULL + sl], (uint32_t)(cnt[sl] & 1))) break;
+                        if (!v_ready && !wait_or_fail(&bar[B_VFULL + st], ph)) break;
+                        v_ready = true;
+                        if (j == 0 && !wait_or_fail(&bar[B_OFREE + sl], (uint32_t)((its[sl] & 1) ^ 1)))
                             break;
-                        }
                         tc_fence_after();
                         const uint32_t v0 = smem_u32(sV + st * C::kTileBytes);
-                        const uint32_t aP = tmem + (uint32_t)st * 128;
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk)
-                            mma_ts(tmem + C::kColO, aP + 8 * kk,
+                            mma_ts(tmem + C::col_o(sl), tmem + C::col_s(sl) + 8 * kk,
                                    smem_desc_sw128(v0 + kk * 2048, C::kHalfBytes, 1024), idPV,
-                                   (j > 1 || kk > 0) ? 1u : 0u);
-                        mma_commit(&bar[B_VEMPTY + st]);
-                        mma_commit(&bar[B_ODONE + st]);
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bar[B_ODONE + sl]);
+                        ++cnt[sl];
+                        if (j + 1 < ns[sl]) {
+                            if (!k_next_ready &&
+                                !wait_or_fail(&bar[B_KFULL + (int)(t1 & 1)], (uint32_t)((t1 >> 1) & 1)))
+                                break;
+                            k_next_ready = true;
+                            tc_fence_after();
+                            issue_qk(sl, (int)(t1 & 1));
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&bar[B_VEMPTY + st]);
+                    if (k_next_ready) {
+                        mma_commit(&bar[B_KEMPTY + (int)(t1 & 1)]);
+                        if (j + 1 == nt - 1) mma_commit(&bar[B_QEMPTY]);
                     }
                     if (*abort_flag) ok = false;
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            // keep the per-slot counters in step on every lane
+            for (int sl = 0; sl < 2; ++sl) {
+                cnt[sl] = __shfl_sync(0xffffffffu, cnt[sl], 0);
+                if (ns[sl] > 0) ++its[sl];
+            }
             t0 += nt;
         }
         if (!ok && lane == 0) fail();
@@ -421,115 +479,122 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
         }
     } else {
         // =================== softmax + epilogue (warps 2..9) ===================
+        const int slot = (warp - 2) >> 2;          // 0 = A, 1 = B
         const int sub = warp & 3;                  // TMEM sub-partition of this warp
-        const int half = (warp - 2) >> 2;          // which 64 of the row's 128 keys
         const int row = sub * 32 + lane;           // tile row = TMEM lane
-        const int pair_bar = 1 + sub;              // the two warps sharing these rows
         const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
-        const float c = p.qscale;
-        long long t0 = 0;
-        int items = 0;
+        const uint32_t colS = tmem + lane_addr + C::col_s(slot);
+        const uint32_t colO = tmem + lane_addr + C::col_o(slot);
+        const float2 c2 = make_float2(p.qscale, p.qscale);
+        long long cnt = 0;   // tiles this slot processed (barrier phases)
+        long long t0 = 0;    // KV tiles of earlier items (V ring phases)
         bool ok = true;
-        for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x, ++items) {
-            const int nt = item_tiles(p, it);
-            const int rr = it.mt * kBM + row;
+        for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k) {
+            const int ntS = slot_tiles(p, it, slot);
+            const int nt = max(slot_tiles(p, it, 0), slot_tiles(p, it, 1));
+            if (ntS == 0) {
+                t0 += nt;
+                continue;
+            }
+            const int rr = (it.mt * 2 + slot) * kBM + row;
             const bool valid = rr < it.n * p.G;
             const int tl = rr / p.G;
             const int pos = valid ? it.L - it.n + tl : -1;  // last key this row sees
             float m_ref = -INFINITY, l = 0.f;
-            for (int j = 0; j < nt; ++j) {
-                const long long t = t0 + j;
-                const int st = (int)(t & 1);
-                const uint32_t ph = (uint32_t)((t >> 1) & 1);
-                if (!mbar_wait_warp(&bar[B_SFULL + st], ph)) {
+            for (int j = 0; j < ntS; ++j, ++cnt) {
+                if (!mbar_wait_warp(&bar[B_SFULL + slot], (uint32_t)(cnt & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int key0 = j * kBN + half * 64;
-                float2 x[32];
+                const int key0 = j * kBN;
+                const bool full_tile = key0 + kBN - 1 <= pos;
+                // Pass 1: row max of the raw scores (scale > 0 keeps the
+                // argmax), 64 columns per TMEM round trip, four chains.
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_addr + (uint32_t)st * 128 + half * 64 + cc, r);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld32(colS + hh * 64, *reinterpret_cast<uint32_t (*)[32]>(r));
+                    tmem_ld32(colS + hh * 64 + 32, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
                     tmem_wait_ld();
+                    if (!full_tile) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        x[cc / 2 + e] = make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                }
-                float mx = -INFINITY;
-                const float2 c2 = make_float2(c, c);
-                if (key0 + 63 <= pos) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        x[e] = __fmul2_rn(x[e], c2);
-                        mx = fmaxf(mx, fmaxf(x[e].x, x[e].y));
+                        for (int k = 0; k < 64; ++k)
+                            if (key0 + hh * 64 + k > pos) r[k] = 0xff800000u;
                     }
-                } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        x[e] = __fmul2_rn(x[e], c2);
-                        if (key0 + 2 * e > pos) x[e].x = -INFINITY;
-                        if (key0 + 2 * e + 1 > pos) x[e].y = -INFINITY;
-                        mx = fmaxf(mx, fmaxf(x[e].x, x[e].y));
-                    }
+                    for (int k = 0; k < 64; k += 2)
+                        m4[(k >> 1) & 3] = fmaxf(m4[(k >> 1) & 3],
+                                                 fmaxf(__uint_as_float(r[k]), __uint_as_float(r[k + 1])));
                 }
-                float *xm = xmax + (int)(t & 1) * 2 * kBM;
-                xm[half * kBM + row] = mx;
-                named_bar_sync(pair_bar, 64);
-                mx = fmaxf(mx, xm[(half ^ 1) * kBM + row]);
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2.x;
                 const bool need = mx > m_ref + kRescaleThreshold;
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    // O holds PV of tiles < j: wait for the last of them, then
-                    // rescale this warp's half of its rows in TMEM.
-                    const long long tp = t - 1;
-                    if (!mbar_wait_warp(&bar[B_ODONE + (int)(tp & 1)], (uint32_t)((tp >> 1) & 1))) {
+                    // O holds PV of tiles < j (all complete once S_j is): rescale.
+                    if (!mbar_wait_warp(&bar[B_ODONE + slot], (uint32_t)((cnt - 1) & 1))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
 #pragma unroll
-                    for (int cc = 0; cc < D / 2; cc += 32) {
-                        uint32_t r[32];
-                        const uint32_t a = tmem + lane_addr + C::kColO + half * (D / 2) + cc;
-                        tmem_ld32(a, r);
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(colO + cc, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(a, r);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(colO + cc, o);
                     }
                     tmem_wait_st();
                     if (need) l *= alpha;
                 }
                 if (need) m_ref = mx;
-                // P = exp2(x - m_ref), packed in pairs, written over this half of S.
+                // Pass 2: P = exp2(s*c - m_ref) in packed pairs, written over
+                // the scores already read (64 keys -> columns 32hh..32hh+31).
+                // A row with no visible key is never written out, so any NaN
+                // stays in its own row.
                 const float2 mneg = make_float2(-m_ref, -m_ref);
-                float2 acc = make_float2(0.f, 0.f);
-                uint32_t w[32];
+                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float2 y = __fadd2_rn(x[e], mneg);
-                    y.x = fast_exp2(y.x);
-                    y.y = fast_exp2(y.y);
-                    if (m_ref == -INFINITY) y = make_float2(0.f, 0.f);
-                    acc = __fadd2_rn(acc, y);
-                    w[e] = Elt<T>::pack2(y.x, y.y);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld32(colS + hh * 64, *reinterpret_cast<uint32_t (*)[32]>(r));
+                    tmem_ld32(colS + hh * 64 + 32, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
+                    tmem_wait_ld();
+                    if (!full_tile) {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k)
+                            if (key0 + hh * 64 + k > pos) r[k] = 0xff800000u;
+                    }
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]),
+                                                          __uint_as_float(r[2 * e + 1])), c2, mneg);
+                        y.x = fast_exp2(y.x);
+                        y.y = fast_exp2(y.y);
+                        acc[e & 1] = __fadd2_rn(acc[e & 1], y);
+                        w[e] = Elt<T>::pack2(y.x, y.y);
+                    }
+                    tmem_st32(colS + hh * 32, w);
                 }
-                tmem_st32(tmem + lane_addr + (uint32_t)st * 128 + half * 32, w);
                 tmem_wait_st();
-                l += acc.x + acc.y;
-                if (j == nt - 1 && it.L < j * kBN + kBN) {
-                    // Keys past the context in the last tile: their V rows hold
-                    // stale data (or nothing was loaded); make them zero so
-                    // 0 * V stays 0 in the tensor core.  All softmax warps
-                    // reach the barrier below even if the wait timed out.
-                    const bool landed = mbar_wait_warp(&bar[B_VFULL + st], ph);
+                l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                if (j == ntS - 1 && ntS == nt && it.L < key0 + kBN) {
+                    // Keys past the context in the item's last tile: their V
+                    // rows hold stale data (or nothing was loaded); make them
+                    // zero so 0 * V stays 0 in the tensor core.  The slot's
+                    // four warps reach the barrier even if the wait timed out.
+                    const long long tv = t0 + j;
+                    const bool landed = mbar_wait_warp(&bar[B_VFULL + (int)(tv & 1)],
+                                                       (uint32_t)((tv >> 1) & 1));
                     if (landed) {
-                        unsigned char *vt = sV + st * C::kTileBytes;
-                        const int first = it.L - j * kBN;
+                        unsigned char *vt = sV + (int)(tv & 1) * C::kTileBytes;
+                        const int first = it.L - key0;
                         const int rows = kBN - first;
-                        for (int xx = half * kBM + row; xx < rows * C::kHalves * 8; xx += 2 * kBM) {
+                        for (int xx = row; xx < rows * C::kHalves * 8; xx += kBM) {
                             const int h = xx / (rows * 8), rem = xx % (rows * 8);
                             *reinterpret_cast<uint4 *>(vt + h * C::kHalfBytes +
                                                        (first + rem / 8) * 128 + (rem % 8) * 16) =
@@ -537,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     }
-                    named_bar_sync(5, kSoftmaxWarps * 32);
+                    named_bar_sync(1 + slot, kBM);
                     if (!landed) {
                         ok = false;
                         break;
@@ -545,26 +610,22 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[B_PFULL + st]);
+                if (lane == 0) mbar_arrive(&bar[B_PFULL + slot]);
             }
             if (!ok) break;
-            // ---- epilogue: O / l for this row's half of the columns
-            xsum[half * kBM + row] = l;
-            named_bar_sync(pair_bar, 64);
-            l += xsum[(half ^ 1) * kBM + row];
-            const long long tl_last = t0 + nt - 1;
-            if (!mbar_wait_warp(&bar[B_ODONE + (int)(tl_last & 1)], (uint32_t)((tl_last >> 1) & 1))) {
+            // ---- epilogue: O / l for this row
+            if (!mbar_wait_warp(&bar[B_ODONE + slot], (uint32_t)((cnt - 1) & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             T *dst = reinterpret_cast<T *>(p.out) +
-                     ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + rr % p.G) * D + half * (D / 2);
+                     ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + rr % p.G) * D;
 #pragma unroll
-            for (int cc = 0; cc < D / 2; cc += 32) {
+            for (int cc = 0; cc < D; cc += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_addr + C::kColO + half * (D / 2) + cc, r);
+                tmem_ld32(colO + cc, r);
                 tmem_wait_ld();
                 if (valid) {
 #pragma unroll
@@ -580,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_OFREE]);
+            if (lane == 0) mbar_arrive(&bar[B_OFREE + slot]);
             t0 += nt;
             if (*abort_flag) ok = false;
         }
@@ -641,7 +702,8 @@ pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) 
 
 int prefill_tau(const AttnArgs &a) {
     const int G = a.Hq / a.Hkv;
-    if ((a.D != 64 && a.D != 128) || G < 1 || 128 % G != 0) return INT_MAX;
+    // The tensor-core kernel takes the row max of unscaled scores: scale > 0.
+    if ((a.D != 64 && a.D != 128) || G < 1 || 128 % G != 0 || !(a.scale > 0.f)) return INT_MAX;
     return prefill::kTauDefault;
 }
 
@@ -672,7 +734,7 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     prm.status = status_word();
     if (!prm.status) return PA_ERR_CUDA;
     // upper bound on the row tiles
-    const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T * G + kBM - 1) / kBM);
+    const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T * G + 2 * kBM - 1) / (2 * kBM));
     const bool bf16 = a.dtype == PA_BF16;
     if (a.D == 128)
         return bf16 ? launch_typed<__nv_bfloat16, 128>(prm, items, stream)
