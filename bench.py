@@ -62,6 +62,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def replica_workload(name: str, rank: int):
+    """Every rank runs an independent replica of the workload: the same shape
+    with its own seed (rank 0 keeps the workload's default seed)."""
+    return workloads.named(name, None if rank == 0 else 1000 + rank)
+
+
+def reduce_over_ranks(x: float, op: str, dist, device) -> float:
+    """max or sum of a host scalar over all ranks (no-op on one rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def kv_bytes(w) -> tuple[int, int]:
     """Algorithmic bytes of one attention call: K/V context read (logical and
     unique-physical), plus q read, out write and the block-table entries."""
@@ -274,7 +290,7 @@ def run_ours(args):
     import paged_kv_attention_prepare_gb300 as pa
 
     dev = torch.device("cuda", local)
-    w = workloads.named(args.workload, None if rank == 0 else 1000 + rank)
+    w = replica_workload(args.workload, rank)
     vals = workloads.make_values(w, 1 + rank, device=dev)
     i32 = torch.int32
     R, T = w.num_reqs, w.num_tokens
@@ -331,13 +347,10 @@ def run_ours(args):
         dist.barrier()
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     attn_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    total_ms = float(np.sum(step_ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_over_ranks(float(np.sum(step_ms)), "max", dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * T / (ms_per_step / 1e3)
+    all_tokens = reduce_over_ranks(T, "sum", dist, dev)
+    value = all_tokens / (ms_per_step / 1e3)
 
     # ---- end to end: inputs from pinned host memory, output back to host
     host_in = {"nst": w.num_scheduled_tokens, "nct": w.num_computed_tokens, "bt": w.block_table}
@@ -371,11 +384,9 @@ def run_ours(args):
         e2e_step()
         e2e_ev[k][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = float(np.sum([a.elapsed_time(b) for a, b in e2e_ev]))
+    e2e_ms = reduce_over_ranks(float(np.sum([a.elapsed_time(b) for a, b in e2e_ev])), "max",
+                               dist, dev)
     if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
         dist.barrier()
     status, detail = pa.pa_get_status()
     if status != pa.PA_OK:
@@ -459,7 +470,7 @@ def run_ours(args):
             "roofline": roofline,
             "roofline_prefill": roofline_prefill,
             "cpu_baseline": cpu,
-            "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": UNIT,
+            "e2e": {"value": all_tokens / (e2e_ms / args.steps / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": int(launches),
             "clocks": clocks.summary(),

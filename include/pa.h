@@ -248,6 +248,16 @@ pa_status pa_attention_noalloc(const void *q, const void *key_cache, const void 
  */
 pa_status pa_get_status(pa_stream_t stream, uint32_t *detail);
 
+/*
+ * pa_selftest_wait_timeout -- diagnostic.  Launches one small kernel that
+ * takes the library's bounded mbarrier wait on a barrier nothing ever
+ * completes.  The wait gives up after its time limit (about one second),
+ * the kernel records PA_CHECK_TIMEOUT and returns; the next pa_get_status()
+ * then reports PA_ERR_TIMEOUT and the context stays usable.  No counterpart
+ * on the pages: it checks this library's own failure handling.
+ */
+pa_status pa_selftest_wait_timeout(pa_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *pa_status_string(pa_status s);
 

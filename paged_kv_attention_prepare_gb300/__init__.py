@@ -74,6 +74,8 @@ def lib():
             L.pa_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                                i32, i32, i32, i32, i32, ctypes.c_float,
                                                ctypes.c_int, vp, vp]
+            L.pa_selftest_wait_timeout.restype = ctypes.c_int
+            L.pa_selftest_wait_timeout.argtypes = [vp]
             L.pa_get_status.restype = ctypes.c_int
             L.pa_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             L.pa_status_string.restype = ctypes.c_char_p
@@ -211,6 +213,11 @@ def pa_get_status(stream=None):
     detail = ctypes.c_uint32(0)
     rc = lib().pa_get_status(_stream(stream), ctypes.byref(detail))
     return int(rc), int(detail.value)
+
+
+def pa_selftest_wait_timeout(stream=None):
+    """Diagnostic: run a kernel whose bounded wait cannot succeed (see pa.h)."""
+    _check(lib().pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
 
 
 def pa_launch_count() -> int:

@@ -630,14 +630,19 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
 // Second pass: for each (token, q head) of a request whose context was split,
 // combine the partitions' (m, l, o): M = max m_s, o = sum 2^(m_s-M) o_s /
-// sum 2^(m_s-M) l_s.  One CTA per token, one warp per head.  Lanes take 32
-// partitions at a time for (m, l); the weighted sum then walks those 32 with
-// lanes over dims, eight independent partial-row loads in flight.
+// sum 2^(m_s-M) l_s.  One CTA per (token, group of 8 heads), one warp per
+// head, so a long request's partitions are combined on many SMs at once.
+// Lanes take 32 partitions at a time for (m, l); the weighted sum then walks
+// those 32 with lanes over dims, eight independent partial-row loads in flight.
+constexpr int kMergeHeadsPerCta = 8;
+
 template <typename T, int D, int RPI>
-__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(32 * kMergeHeadsPerCta) merge_kernel(const __grid_constant__ Params p) {
     constexpr int DPL = D / 32;
-    const int t = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int groups = (p.Hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta;
+    const int t = blockIdx.x / groups;
+    const int h = (blockIdx.x % groups) * kMergeHeadsPerCta + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     __shared__ int s_r;
     if (threadIdx.x == 0) {
         // the last request whose start is <= t
@@ -650,6 +655,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Para
         s_r = lo;
     }
     __syncthreads();
+    if (h >= p.Hq) return;
     const int r = s_r;
     const int4 meta = reinterpret_cast<const int4 *>(p.req_meta)[r];
     const int nsplit = meta.z, nchunks = meta.w;
@@ -657,53 +663,51 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Para
     const int tl = t - p.qsl[r];
     if (tl < 0 || tl >= p.qsl[r + 1] - p.qsl[r]) return;
     const long long pbase = (long long)(unsigned)meta.x | ((long long)meta.y << 32);
-    for (int h = warp; h < p.Hq; h += 8) {
-        const int g = h / p.G;
-        const int rr = tl * p.G + h % p.G;
-        const int chunk = rr / RPI, j = rr % RPI;
-        const long long first = pbase + ((long long)g * nchunks + chunk) * nsplit;
-        const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
-        float M = -INFINITY;
-        for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, ml[(first + s) * RPI + j].x);
+    const int g = h / p.G;
+    const int rr = tl * p.G + h % p.G;
+    const int chunk = rr / RPI, j = rr % RPI;
+    const long long first = pbase + ((long long)g * nchunks + chunk) * nsplit;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
+    float M = -INFINITY;
+    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, ml[(first + s) * RPI + j].x);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float Lsum = 0.f;
-        float o[DPL];
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Lsum = 0.f;
+    float o[DPL];
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) o[d] = 0.f;
-        for (int s0 = 0; s0 < nsplit; s0 += 32) {
-            float w = 0.f;
-            if (s0 + lane < nsplit) {
-                const float2 v = ml[(first + s0 + lane) * RPI + j];
-                w = v.x == -INFINITY ? 0.f : fast_exp2(v.x - M);
-                Lsum += w * v.y;
-            }
-            const int cnt = min(32, nsplit - s0);
+    for (int d = 0; d < DPL; ++d) o[d] = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+        float w = 0.f;
+        if (s0 + lane < nsplit) {
+            const float2 v = ml[(first + s0 + lane) * RPI + j];
+            w = v.x == -INFINITY ? 0.f : fast_exp2(v.x - M);
+            Lsum += w * v.y;
+        }
+        const int cnt = min(32, nsplit - s0);
 #pragma unroll 8
-            for (int k = 0; k < cnt; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, w, k);
-                const float *po = p.part_o + ((first + s0 + k) * RPI + j) * D + lane * DPL;
-                if constexpr (DPL == 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(po);
-                    o[0] = fmaf(wk, v.x, o[0]);
-                    o[1] = fmaf(wk, v.y, o[1]);
-                    o[2] = fmaf(wk, v.z, o[2]);
-                    o[3] = fmaf(wk, v.w, o[3]);
-                } else {
-                    const float2 v = *reinterpret_cast<const float2 *>(po);
-                    o[0] = fmaf(wk, v.x, o[0]);
-                    o[1] = fmaf(wk, v.y, o[1]);
-                }
+        for (int k = 0; k < cnt; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            const float *po = p.part_o + ((first + s0 + k) * RPI + j) * D + lane * DPL;
+            if constexpr (DPL == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(po);
+                o[0] = fmaf(wk, v.x, o[0]);
+                o[1] = fmaf(wk, v.y, o[1]);
+                o[2] = fmaf(wk, v.z, o[2]);
+                o[3] = fmaf(wk, v.w, o[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(po);
+                o[0] = fmaf(wk, v.x, o[0]);
+                o[1] = fmaf(wk, v.y, o[1]);
             }
         }
-#pragma unroll
-        for (int s = 16; s >= 1; s >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, s);
-        const float inv = 1.f / Lsum;
-        T *dst = reinterpret_cast<T *>(p.out) + ((long long)t * p.Hq + h) * D + lane * DPL;
-#pragma unroll
-        for (int d = 0; d < DPL; d += 2)
-            *reinterpret_cast<uint32_t *>(dst + d) = Elt<T>::pack2(o[d] * inv, o[d + 1] * inv);
     }
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, s);
+    const float inv = 1.f / Lsum;
+    T *dst = reinterpret_cast<T *>(p.out) + ((long long)t * p.Hq + h) * D + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; d += 2)
+        *reinterpret_cast<uint32_t *>(dst + d) = Elt<T>::pack2(o[d] * inv, o[d + 1] * inv);
 }
 
 template <typename T, int D, int RPI>
@@ -729,7 +733,8 @@ pa_status launch_typed(Params &prm, long long max_items, bool merge, cudaStream_
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
     if (merge && prm.T > 0) {
-        merge_kernel<T, D, RPI><<<prm.T, 256, 0, stream>>>(prm);
+        const long long groups = (prm.Hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta;
+        merge_kernel<T, D, RPI><<<(unsigned)(prm.T * groups), 32 * kMergeHeadsPerCta, 0, stream>>>(prm);
         PA_TRY_CUDA(cudaGetLastError());
         note_launch();
     }

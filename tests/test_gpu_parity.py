@@ -334,3 +334,17 @@ def test_launch_count():
     pa.pa_launch_count()
     run_step(w, vals)
     assert pa.pa_launch_count() >= 3
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    # A wait on a barrier nothing completes ends with a timeout status, not a
+    # hang, and the next step on the same context is still correct.
+    pa.pa_selftest_wait_timeout()
+    st, detail = pa.pa_get_status()
+    assert st == pa.PA_ERR_TIMEOUT and pa.check_bits(detail) == {"timeout"}
+    w = workloads.tiny()
+    vals = workloads.make_values(w, 0)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    _check_attention(res, ref)
