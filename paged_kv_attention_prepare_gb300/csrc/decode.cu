@@ -84,7 +84,9 @@ struct Cfg {
     static constexpr int DPL = D / 32;
     static constexpr int kPageBytes = kPage * D * 2;
     static constexpr int kStageBytes = kStages * kPageBytes;
-    static constexpr int kPbuf = kPage * RPI + RPI;   // per warp: p[key][row], alpha[row]
+    // per warp: p[key][row], alpha[row]; padded to 16 bytes so every warp's
+    // buffer (and the float4 reads of it) stays aligned for any RPI
+    static constexpr int kPbuf = (kPage * RPI + RPI + 3) / 4 * 4;
     static constexpr int kComb = RPI * (D + 2);       // per warp: acc[row][D], m[row], l[row]
     static constexpr int kBytes = kStageBytes + kConsumerWarps * (kPbuf + kComb) * 4 +
                                   (2 * kStages + 2) * 8 + kCandidates * 8 + 256;
