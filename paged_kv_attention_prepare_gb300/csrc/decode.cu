@@ -48,6 +48,7 @@ constexpr int kStages = 16;
 // a whole ring round ahead on a stage (where mbarrier parity could not tell
 // the rounds apart).
 static_assert((kStages / 2) % kConsumerWarps == 0, "stages must split evenly among warps");
+static_assert((kStages & (kStages - 1)) == 0, "ring index arithmetic uses a power-of-two ring");
 constexpr int kPage = 16;         // tokens per cache block
 constexpr int kCandidates = 8;    // partition lengths p_min << k
 constexpr int kSingle = INT_MAX / 2;
@@ -202,28 +203,23 @@ __device__ __forceinline__ void item_keys(const Params &p, const typename Walker
 }
 
 // Reduce v[RPI] across the LPT lanes of a key group so that each row's full
-// sum ends in v[0] of the lanes whose low log2(LPT/RPI) bits are zero; returns
-// the row the lane holds.  Each halving step trades half of the rows with the
-// partner lane, so RPI rows cost RPI - 1 + log2(LPT/RPI) shuffles.
+// sum ends in v[0] of the lanes whose low log2(LPT/RPI) bits are zero.  Each
+// halving step trades half of the rows with the partner lane; the lane's q
+// rows are stored XOR-permuted by the row it ends up holding (slot i holds
+// row i ^ myrow), which makes "keep the low half, send the high half" right
+// for every lane and needs no selects.  RPI rows cost RPI - 1 + log2(LPT/RPI)
+// shuffles.
 template <int RPI, int LPT>
-__device__ __forceinline__ int reduce_scatter(float (&v)[RPI], int j) {
-    int row = 0;
+__device__ __forceinline__ void reduce_scatter(float (&v)[RPI]) {
 #pragma unroll
     for (int step = 0; (1 << step) < RPI; ++step) {
         const int half = RPI >> (step + 1);
         const int mask = (LPT / 2) >> step;
-        const bool upper = j & mask;
 #pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? v[i] : v[i + half];
-            const float keep = upper ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-        }
-        if (upper) row += half;
+        for (int i = 0; i < half; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + half], mask);
     }
 #pragma unroll
     for (int m = LPT / RPI / 2; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
-    return row;
 }
 
 // Unpack a word of two 16-bit elements into a float pair (element order kept).
@@ -406,7 +402,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         if (j & ((LPT / 2) >> step)) myrow += RPI >> (step + 1);
     float *pb = pbuf + warp * C::kPbuf;
     float *cw = comb + warp * C::kComb;
-    long long pair_base = 0;         // page pairs of earlier items
+    int pair_base = 0;               // page pairs of earlier items
     uint32_t cpar = 0;
     bool ok = true;
     for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x) {
@@ -421,12 +417,17 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             const int rr = it.chunk * RPI + myrow;
             lim = rr < nrows ? min(pos0 + rr / p.G, k1 - 1) : -1;
         }
+        // Pages whose last key every row of the item sees need no mask (rows
+        // past the request's end may then pick up scores, but they are never
+        // written out and stay in their own accumulators).
+        const int lim_all = min(pos0 + (it.chunk * RPI) / p.G, k1 - 1);
 
-        // q rows of this item, this lane's QK dims, pre-scaled by scale*log2(e).
+        // q rows of this item, this lane's QK dims, pre-scaled by scale*log2(e);
+        // slot r holds row r ^ myrow (see reduce_scatter).
         float2 qv[RPI][DQ / 2];
 #pragma unroll
         for (int r = 0; r < RPI; ++r) {
-            const int rr = it.chunk * RPI + r;
+            const int rr = it.chunk * RPI + (r ^ myrow);
             if (rr < nrows) {
                 const T *qrow = q + ((long long)(qstart + rr / p.G) * p.Hq + it.g * p.G + rr % p.G) * D;
 #pragma unroll
@@ -451,12 +452,13 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             for (int e = 0; e < DPL / 2; ++e) acc[r][e] = make_float2(0.f, 0.f);
         float m_run = -INFINITY, l_run = 0.f;
 
-        for (int pg = (int)((warp - pair_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
+        for (int pg = (warp - pair_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
              pg < npages; pg += kConsumerWarps) {
-            const long long n2 = 2 * (pair_base + pg);
-            const int stK = (int)(n2 % kStages), stV = (int)((n2 + 1) % kStages);
-            const uint32_t phK = (uint32_t)((n2 / kStages) & 1), phV = (uint32_t)(((n2 + 1) / kStages) & 1);
+            const int n2 = 2 * (pair_base + pg);
+            const int stK = n2 & (kStages - 1), stV = (n2 + 1) & (kStages - 1);
+            const uint32_t phK = (uint32_t)(n2 / kStages) & 1u, phV = (uint32_t)((n2 + 1) / kStages) & 1u;
             const int key0 = k0 + pg * kPage;
+            const bool page_visible = key0 + kPage - 1 <= lim_all;
 
             // ---- scores of the page's 16 keys for this warp's rows
             if (!mbar_wait_warp(&full[stK], phK)) {
@@ -486,8 +488,8 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                     for (int e = 0; e < DQ / 2; ++e) a = __ffma2_rn(qv[r][e], kf[e], a);
                     s[r] = a.x + a.y;
                 }
-                reduce_scatter<RPI, LPT>(s, j);
-                sc[ps] = key0 + t <= lim ? s[0] : -INFINITY;
+                reduce_scatter<RPI, LPT>(s);
+                sc[ps] = (page_visible || key0 + t <= lim) ? s[0] : -INFINITY;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stK]);
@@ -532,7 +534,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 for (int e = 0; e < DPL / 2; ++e) acc[r][e] = __fmul2_rn(acc[r][e], make_float2(a, a));
             }
             const int nvalid = min(kPage, k1 - key0);  // never touch slots past the context
-            for (int t = 0; t < nvalid; ++t) {
+            auto pv_key = [&](int t) {
                 float2 vf[DPL / 2];
                 if constexpr (DPL == 4) {
                     const uint2 raw = *reinterpret_cast<const uint2 *>(vpage + t * D * 2 + lane * 8);
@@ -560,6 +562,12 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 #pragma unroll
                     for (int e = 0; e < DPL / 2; ++e)
                         acc[r][e] = __ffma2_rn(make_float2(pr[r], pr[r]), vf[e], acc[r][e]);
+            };
+            if (nvalid == kPage) {
+#pragma unroll
+                for (int t = 0; t < kPage; ++t) pv_key(t);
+            } else {
+                for (int t = 0; t < nvalid; ++t) pv_key(t);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stV]);
