@@ -30,6 +30,7 @@
 //     kernel combines them.
 #include <climits>
 #include <cstring>
+#include <type_traits>
 
 #include "pa_internal.cuh"
 
@@ -468,51 +469,67 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             }
             const unsigned char *kpage = stages + stK * C::kPageBytes;
             float sc[NPASS];
+            float alpha;
+            // Scores and the online-softmax update for this lane's row.  With
+            // every key of the page visible to every row (the common case) no
+            // mask is applied and the running max is always finite.
+            auto qk_softmax = [&](auto all_visible) {
+                constexpr bool kVis = decltype(all_visible)::value;
 #pragma unroll
-            for (int ps = 0; ps < NPASS; ++ps) {
-                const int t = ps * TPP + tq;
-                float2 kf[DQ / 2];
+                for (int ps = 0; ps < NPASS; ++ps) {
+                    const int t = ps * TPP + tq;
+                    float2 kf[DQ / 2];
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(kpage + t * D * 2 + (j + c * LPT) * 16);
-                    kf[c * 4 + 0] = unpack_pair<T>(raw.x);
-                    kf[c * 4 + 1] = unpack_pair<T>(raw.y);
-                    kf[c * 4 + 2] = unpack_pair<T>(raw.z);
-                    kf[c * 4 + 3] = unpack_pair<T>(raw.w);
+                    for (int c = 0; c < CPL; ++c) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(kpage + t * D * 2 + (j + c * LPT) * 16);
+                        kf[c * 4 + 0] = unpack_pair<T>(raw.x);
+                        kf[c * 4 + 1] = unpack_pair<T>(raw.y);
+                        kf[c * 4 + 2] = unpack_pair<T>(raw.z);
+                        kf[c * 4 + 3] = unpack_pair<T>(raw.w);
+                    }
+                    float sr[RPI];
+#pragma unroll
+                    for (int r = 0; r < RPI; ++r) {
+                        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < DQ / 2; ++e) a = __ffma2_rn(qv[r][e], kf[e], a);
+                        sr[r] = a.x + a.y;
+                    }
+                    reduce_scatter<RPI, LPT>(sr);
+                    sc[ps] = (kVis || key0 + t <= lim) ? sr[0] : -INFINITY;
                 }
-                float s[RPI];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stK]);
+                float mp = sc[0];
 #pragma unroll
-                for (int r = 0; r < RPI; ++r) {
-                    float2 a = make_float2(0.f, 0.f);
+                for (int ps = 1; ps < NPASS; ++ps) mp = fmaxf(mp, sc[ps]);
 #pragma unroll
-                    for (int e = 0; e < DQ / 2; ++e) a = __ffma2_rn(qv[r][e], kf[e], a);
-                    s[r] = a.x + a.y;
+                for (int m = LPT; m < 32; m <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, m));
+                const float m_new = fmaxf(m_run, mp);
+                float sum = 0.f;
+                if (kVis) {
+                    alpha = fast_exp2(m_run - m_new);
+#pragma unroll
+                    for (int ps = 0; ps < NPASS; ++ps) {
+                        sc[ps] = fast_exp2(sc[ps] - m_new);
+                        sum += sc[ps];
+                    }
+                } else {
+                    alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
+#pragma unroll
+                    for (int ps = 0; ps < NPASS; ++ps) {
+                        const float e = m_new == -INFINITY ? 0.f : fast_exp2(sc[ps] - m_new);
+                        sc[ps] = e;
+                        sum += e;
+                    }
                 }
-                reduce_scatter<RPI, LPT>(s);
-                sc[ps] = (page_visible || key0 + t <= lim) ? s[0] : -INFINITY;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stK]);
-
-            // ---- online softmax update for this lane's row
-            float mp = -INFINITY;
 #pragma unroll
-            for (int ps = 0; ps < NPASS; ++ps) mp = fmaxf(mp, sc[ps]);
-#pragma unroll
-            for (int m = LPT; m < 32; m <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, m));
-            const float m_new = fmaxf(m_run, mp);
-            const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
-            float sum = 0.f;
-#pragma unroll
-            for (int ps = 0; ps < NPASS; ++ps) {
-                const float e = m_new == -INFINITY ? 0.f : fast_exp2(sc[ps] - m_new);
-                sc[ps] = e;
-                sum += e;
-            }
-#pragma unroll
-            for (int m = LPT; m < 32; m <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
-            l_run = l_run * alpha + sum;
-            m_run = m_new;
+                for (int m = LPT; m < 32; m <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+                l_run = l_run * alpha + sum;
+                m_run = m_new;
+            };
+            if (page_visible) qk_softmax(std::true_type{});
+            else qk_softmax(std::false_type{});
             if (dup == 0) {
 #pragma unroll
                 for (int ps = 0; ps < NPASS; ++ps) pb[(ps * TPP + tq) * RPI + myrow] = sc[ps];
