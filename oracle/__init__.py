@@ -9,6 +9,16 @@ Parity status of each function (how it is pinned, in ``tests/test_oracle.py``):
 * ``prepare_inputs`` -- pinned by the pages' printed worked examples
   (``tests/golden/``), hand-derived exercise answers, invariants and a brute
   force against a separately written pure-Python restatement.
+* ``gather_input_ids`` -- pinned by the printed token_indices comment
+  ([0, 1, M, M+1, ..., 2M+2] for query positions [0, 1, 0, 1, 2, 3, 4, 0, 1, 2])
+  and the Go program's input_ids (token ids 100.., 200.., 300..), plus
+  invariants (each id comes from its own request's row at its position).
+* ``discard_request_mask`` -- pinned by the printed [False, True, True] of the
+  [2, 5, 3] example and the Go program's per-request verdicts.
+* ``spec_logits_indices`` -- pinned by the printed no-draft rows [1, 6, 9]
+  (drafts all zero reduce to query_start_loc[1:] - 1) and by invariants of the
+  draft case (length R + sum(d); each request's rows are consecutive, inside
+  its own slice and end on its last row).
 * ``cache_write`` -- pinned by bit equality against a direct per-slot copy,
   untouched-slot preservation and write-then-gather round trips.
 * ``attention`` -- pinned by closed forms (one visible key, K = 0, constant V,
@@ -69,6 +79,16 @@ def _load():
                 i32p, i32p, i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                 ctypes.c_int32, ctypes.c_int32, i32p, i32p, i32p, i32p, ctypes.c_int32,
                 i32p, i32p]
+            lib.oracle_gather_input_ids.restype = ctypes.c_int
+            lib.oracle_gather_input_ids.argtypes = [
+                i32p, i32p, ctypes.c_int32, i32p, ctypes.c_int32, ctypes.c_int32,
+                ctypes.POINTER(ctypes.c_int64), i32p]
+            lib.oracle_discard_request_mask.restype = ctypes.c_int
+            lib.oracle_discard_request_mask.argtypes = [
+                i32p, i32p, i32p, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint8)]
+            lib.oracle_spec_logits_indices.restype = ctypes.c_int
+            lib.oracle_spec_logits_indices.argtypes = [
+                i32p, i32p, ctypes.c_int32, ctypes.c_int32, i32p, i32p]
             lib.oracle_cache_write.restype = ctypes.c_int
             lib.oracle_cache_write.argtypes = [
                 u16p, u16p, ctypes.c_int64, u16p, u16p, i32p, ctypes.c_int32,
@@ -134,6 +154,58 @@ def prepare_inputs(num_scheduled_tokens, num_computed_tokens, block_table, block
     if check and rc != 0:
         raise OracleError(f"oracle_prepare_inputs rejected the inputs ({rc})")
     return out
+
+
+def gather_input_ids(req_indices, positions, token_ids, check=True):
+    """token_indices (int64) and input_ids (int32) of every flat token, gathered
+    from the ``[max_num_reqs, max_model_len]`` token buffer ``token_ids``.
+    Returns (token_indices, input_ids, status)."""
+    lib = _load()
+    req, pos = _i32(req_indices), _i32(positions)
+    ids = _i32(token_ids)
+    if ids.ndim != 2:
+        raise OracleError("token_ids must be [max_num_reqs, max_model_len]")
+    t = req.shape[0]
+    tok_idx = np.full(t, -7, np.int64)
+    input_ids = np.full(t, -7, np.int32)
+    rc = lib.oracle_gather_input_ids(
+        _p32(req), _p32(pos), t, _p32(ids), ids.shape[0], ids.shape[1],
+        tok_idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _p32(input_ids))
+    if check and rc != 0:
+        raise OracleError(f"oracle_gather_input_ids rejected the inputs ({rc})")
+    return tok_idx, input_ids, int(rc)
+
+
+def discard_request_mask(num_computed_tokens, num_scheduled_tokens, request_num_tokens):
+    """Boolean per request: True when computed + scheduled is still short of
+    the request's total token count (its sampled token is thrown away)."""
+    lib = _load()
+    nct, nst, ntok = (_i32(num_computed_tokens), _i32(num_scheduled_tokens),
+                      _i32(request_num_tokens))
+    r = nst.shape[0]
+    mask = np.full(r, 7, np.uint8)
+    rc = lib.oracle_discard_request_mask(_p32(nct), _p32(nst), _p32(ntok), r,
+                                         mask.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    if rc != 0:
+        raise OracleError(f"oracle_discard_request_mask rejected the inputs ({rc})")
+    return mask.astype(bool)
+
+
+def spec_logits_indices(query_start_loc, num_draft_tokens=None, num_logits=None, check=True):
+    """Sampled rows.  Returns (logits_indices [num_logits], cu_num_logits [R+1],
+    status).  ``num_draft_tokens`` None means no drafts (one row per request)."""
+    lib = _load()
+    qsl = _i32(query_start_loc)
+    r = qsl.shape[0] - 1
+    d = None if num_draft_tokens is None else _i32(num_draft_tokens)
+    n = (r + (int(d.sum()) if d is not None else 0)) if num_logits is None else int(num_logits)
+    rows = np.full(max(n, 0), -7, np.int32)
+    cu = np.full(r + 1, -7, np.int32)
+    rc = lib.oracle_spec_logits_indices(_p32(qsl), None if d is None else _p32(d), r, n,
+                                        _p32(rows), _p32(cu))
+    if check and rc != 0:
+        raise OracleError(f"oracle_spec_logits_indices rejected the inputs ({rc})")
+    return rows, cu, int(rc)
 
 
 def cache_write(key, value, key_cache, value_cache, slot_mapping, num_kv_heads, head_dim,

@@ -6,7 +6,7 @@
  * this library; the CUDA library never links, includes or calls it, and it
  * shares no code with the CUDA library.  Floating point is fp64 throughout.
  *
- * Three functions, each citing the passage it follows:
+ * Six functions, each citing the passage it follows:
  *
  *   oracle_prepare_inputs  -- the per-step index tensors
  *       ("Building the Batch", sections "How they are computed" and
@@ -16,6 +16,20 @@
  *        logits_indices = query_start_loc[1:] - 1; and the same page's Go
  *        program, which builds the tensors with one loop over requests and
  *        one over each request's scheduled tokens).
+ *   oracle_gather_input_ids -- "Building the Batch", section "How they are
+ *        computed" (token_indices = positions + req_indices * M, M the width
+ *        of the per-request token buffer, then one index_select of the
+ *        flattened buffer) and "vLLM's Model Runner", section "Flattening
+ *        the batch into one token axis".
+ *   oracle_discard_request_mask -- "vLLM's Model Runner", sections "The two
+ *        things this method returns" and "The batch contains rows that must
+ *        not be sampled": optimistic seq len = computed + scheduled; a
+ *        request's sample is discarded when that is below its total token
+ *        count.
+ *   oracle_spec_logits_indices -- "Building the Batch", section "Only one row
+ *        per request reaches the vocabulary": without drafts one row per
+ *        request, query_start_loc[1:] - 1; with d draft tokens a request
+ *        needs d + 1 rows, read as the last d + 1 rows of its slice.
  *   oracle_cache_write     -- "Inside vLLM: Following One Request", section
  *        on reshape_and_cache_flash: token i's K and V are copied to slot
  *        slot_mapping[i].  A bit copy.
@@ -140,6 +154,93 @@ int oracle_prepare_inputs(const int32_t *num_scheduled_tokens,
     /* Pad the tail with the total so the array never decreases. */
     for (int32_t i = num_reqs + 1; i < qsl_capacity; ++i)
         query_start_loc[i] = num_tokens;
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Token ids, discard mask, sampled rows                                     */
+/* ------------------------------------------------------------------------ */
+
+/* The token buffer holds one row of max_model_len ids per request slot, so
+ * the id at position p of row r sits at flat offset r * max_model_len + p.
+ * Every token of the step is gathered from there in one pass. */
+int oracle_gather_input_ids(const int32_t *req_indices, const int32_t *positions,
+                            int32_t num_tokens, const int32_t *token_ids,
+                            int32_t max_num_reqs, int32_t max_model_len,
+                            int64_t *token_indices, int32_t *input_ids)
+{
+    int err = 0;
+    if (num_tokens < 0 || max_num_reqs < 0 || max_model_len <= 0)
+        return -1;
+    /* Step 1: flat offsets into the [max_num_reqs][max_model_len] buffer. */
+    for (int32_t t = 0; t < num_tokens; ++t)
+        token_indices[t] = (int64_t)positions[t] + (int64_t)req_indices[t] * max_model_len;
+    /* Step 2: index_select of the flattened buffer at those offsets. */
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        if (req_indices[t] < 0 || req_indices[t] >= max_num_reqs || positions[t] < 0 ||
+            positions[t] >= max_model_len) {
+            err = -6;            /* the offset would leave its own row */
+            token_indices[t] = -1;
+            input_ids[t] = -1;
+            continue;
+        }
+        input_ids[t] = token_ids[token_indices[t]];
+    }
+    return err;
+}
+
+int oracle_discard_request_mask(const int32_t *num_computed_tokens,
+                                const int32_t *num_scheduled_tokens,
+                                const int32_t *request_num_tokens, int32_t num_reqs,
+                                uint8_t *discard_request_mask)
+{
+    if (num_reqs < 0)
+        return -1;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        /* how long the sequence is once this step has run */
+        int64_t optimistic_seq_len =
+            (int64_t)num_computed_tokens[r] + (int64_t)num_scheduled_tokens[r];
+        discard_request_mask[r] = optimistic_seq_len < (int64_t)request_num_tokens[r];
+    }
+    return 0;
+}
+
+/* Rows of the step's output that get a next-token distribution.  Request r
+ * with d[r] draft tokens owns d[r] + 1 consecutive entries, starting at
+ * cu_num_logits[r]; they are the last d[r] + 1 rows of its slice
+ * [query_start_loc[r], query_start_loc[r+1]).  num_draft_tokens == NULL
+ * means no drafts.  cu_num_logits (optional) gets the R + 1 starts. */
+int oracle_spec_logits_indices(const int32_t *query_start_loc,
+                               const int32_t *num_draft_tokens, int32_t num_reqs,
+                               int32_t num_logits, int32_t *logits_indices,
+                               int32_t *cu_num_logits)
+{
+    int err = 0;
+    if (num_reqs < 0 || num_logits < 0)
+        return -1;
+    int32_t row = 0;
+    for (int32_t r = 0; r < num_reqs; ++r) {
+        int32_t d = num_draft_tokens ? num_draft_tokens[r] : 0;
+        int32_t q_len = query_start_loc[r + 1] - query_start_loc[r];
+        if (d < 0 || d + 1 > q_len) {
+            err = -7;           /* the drafts must be among the scheduled tokens */
+            d = d < 0 ? 0 : (q_len > 0 ? q_len - 1 : 0);
+        }
+        if (cu_num_logits)
+            cu_num_logits[r] = row;
+        int32_t last = query_start_loc[r + 1] - 1;
+        for (int32_t k = 0; k <= d; ++k) {
+            if (row >= num_logits) {
+                err = -3;
+                break;
+            }
+            logits_indices[row++] = last - d + k;
+        }
+    }
+    if (cu_num_logits)
+        cu_num_logits[num_reqs] = row;
+    if (row != num_logits)
+        err = err ? err : -3;
     return err;
 }
 

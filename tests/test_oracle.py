@@ -167,6 +167,158 @@ def test_prep_rejects_bad_inputs(bad):
 
 
 # ---------------------------------------------------------------------------
+# Input ids, discard mask, sampled rows
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m", [8, 16, 1000, 131072])
+def test_token_indices_printed_comment(m):
+    g = golden("prep_token_indices_comment.json")
+    i = g["inputs"]
+    # Every entry of the buffer holds its own flat offset, so the gathered
+    # id equals the offset the page prints.
+    ids = np.arange(3 * m, dtype=np.int64).astype(np.int32).reshape(3, m)
+    tok, inp, st = oracle.gather_input_ids(i["req_indices"], i["positions"], ids)
+    want = [a * m + b for a, b in g["printed"]["token_indices_as_multiple_of_M_plus_offset"]]
+    assert st == 0
+    assert tok.tolist() == want
+    assert inp.tolist() == want
+
+
+def test_token_indices_from_oracle_prep_positions():
+    # The same comment, with req_indices / positions produced by the index build.
+    g = golden("prep_token_indices_comment.json")
+    i = g["inputs"]
+    out = oracle.prepare_inputs(i["num_scheduled_tokens"], i["num_computed_tokens"],
+                                [[0], [1], [2]], 16, 10, 3)
+    assert out["positions"].tolist() == i["positions"]
+    assert out["req_indices"].tolist() == i["req_indices"]
+
+
+def _go_token_buffer(width):
+    g = golden("prep_go_program_bs4.json")
+    rows = np.full((4, width), -5, np.int32)      # a spare fourth row, unused
+    for r, name in enumerate("ABC"):
+        base, n = g["inputs"]["token_ids_rows"][name]
+        rows[r, :n] = np.arange(base, base + n)
+    return g, rows
+
+
+@pytest.mark.parametrize("width", [20, 64])
+def test_input_ids_go_program(width):
+    g, rows = _go_token_buffer(width)
+    i = g["inputs"]
+    out = oracle.prepare_inputs(i["num_scheduled_tokens"], i["num_computed_tokens"],
+                                i["block_table"], i["block_size"], 9, i["num_blocks"])
+    tok, inp, st = oracle.gather_input_ids(out["req_indices"], out["positions"], rows)
+    assert st == 0
+    assert inp.tolist() == g["derived_by_hand"]["input_ids"]
+    assert np.array_equal(tok // width, out["req_indices"])
+    assert np.array_equal(tok % width, out["positions"])
+
+
+def test_input_ids_brute_force_two_dimensional_lookup():
+    rng = np.random.default_rng(21)
+    for _ in range(200):
+        rows_n = int(rng.integers(1, 7))
+        width = int(rng.integers(1, 50))
+        ids = rng.integers(0, 2**31 - 1, size=(rows_n, width)).astype(np.int32)
+        t = int(rng.integers(0, 40))
+        req = rng.integers(0, rows_n, size=t)
+        pos = rng.integers(0, width, size=t)
+        tok, inp, st = oracle.gather_input_ids(req, pos, ids)
+        assert st == 0
+        assert inp.tolist() == [int(ids[a][b]) for a, b in zip(req, pos)]
+        assert tok.tolist() == [int(a) * width + int(b) for a, b in zip(req, pos)]
+
+
+@pytest.mark.parametrize("bad", ["position_past_row", "row_past_buffer", "negative"])
+def test_input_ids_rejects_offsets_outside_own_row(bad):
+    ids = np.arange(12, dtype=np.int32).reshape(3, 4)
+    req, pos = [0, 1, 2], [1, 2, 3]
+    if bad == "position_past_row":
+        pos = [1, 4, 3]          # would read row 2's first id
+    elif bad == "row_past_buffer":
+        req = [0, 3, 2]
+    else:
+        pos = [1, -1, 3]
+    tok, inp, st = oracle.gather_input_ids(req, pos, ids, check=False)
+    assert st != 0
+    assert tok[1] == -1 and inp[1] == -1
+    assert inp[0] == 1 and inp[2] == 11
+
+
+def test_discard_mask_printed_2_5_3():
+    g = golden("prep_worked_example_2_5_3.json")
+    i = g["inputs"]
+    m = oracle.discard_request_mask(i["num_computed_tokens"], i["num_scheduled_tokens"],
+                                    i["request_num_tokens"])
+    assert m.tolist() == g["printed"]["discard_request_mask"]
+
+
+def test_discard_mask_go_program():
+    g = golden("prep_go_program_bs4.json")
+    i, h = g["inputs"], g["derived_by_hand"]
+    m = oracle.discard_request_mask(i["num_computed_tokens"], i["num_scheduled_tokens"],
+                                    h["request_num_tokens"])
+    assert m.tolist() == h["discard_request_mask"]
+
+
+def test_discard_mask_boundaries():
+    # caught up exactly -> sampled; one short -> discarded; decode (1 token,
+    # total already known) -> sampled
+    m = oracle.discard_request_mask([9, 9, 41, 0], [1, 1, 1, 16], [10, 11, 42, 17])
+    assert m.tolist() == [False, True, False, True]
+
+
+def test_spec_logits_no_drafts_is_printed_rows():
+    g = golden("prep_worked_example_2_5_3.json")
+    qsl = g["printed"]["query_start_loc"]
+    for drafts in (None, [0, 0, 0]):
+        rows, cu, st = oracle.spec_logits_indices(qsl, drafts)
+        assert st == 0
+        assert rows.tolist() == g["printed"]["logits_indices"]
+        assert cu.tolist() == [0, 1, 2, 3]
+
+
+def test_spec_logits_draft_invariants():
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        r = int(rng.integers(1, 10))
+        nst = rng.integers(1, 9, size=r)
+        d = np.array([int(rng.integers(0, n)) for n in nst])
+        qsl = np.concatenate([[0], np.cumsum(nst)])
+        rows, cu, st = oracle.spec_logits_indices(qsl, d)
+        assert st == 0
+        assert len(rows) == r + d.sum()                    # one per draft plus one
+        assert cu[0] == 0 and np.array_equal(np.diff(cu), d + 1)
+        for q in range(r):
+            mine = rows[cu[q]:cu[q + 1]]
+            assert np.array_equal(np.diff(mine), np.ones(d[q], np.int32))  # consecutive
+            assert mine[-1] == qsl[q + 1] - 1                # ends on the slice's last row
+            assert mine[0] >= qsl[q]                         # stays in its own slice
+
+
+def test_spec_logits_decode_with_drafts_example():
+    # Two decoding requests verifying 2 and 0 drafts, one prefill chunk:
+    # scheduled [3, 1, 4] -> slices [0,3) [3,4) [4,8); rows: 0,1,2 | 3 | 7.
+    rows, cu, st = oracle.spec_logits_indices([0, 3, 4, 8], [2, 0, 0])
+    assert st == 0 and rows.tolist() == [0, 1, 2, 3, 7] and cu.tolist() == [0, 3, 4, 5]
+
+
+@pytest.mark.parametrize("bad", ["too_many_drafts", "negative", "count_mismatch"])
+def test_spec_logits_rejects(bad):
+    qsl, d, n = [0, 3, 4], [2, 0], None
+    if bad == "too_many_drafts":
+        d = [3, 0]              # 4 rows from a 3-token slice
+    elif bad == "negative":
+        d = [-1, 0]
+    else:
+        n = 3
+    rows, cu, st = oracle.spec_logits_indices(qsl, d, n, check=False)
+    assert st != 0
+
+
+# ---------------------------------------------------------------------------
 # Cache write
 # ---------------------------------------------------------------------------
 

@@ -34,6 +34,17 @@ MUTANTS = {
     "qsl_tail_zero": ("query_start_loc[i] = num_tokens;", "query_start_loc[i] = 0;"),
     "pv_reads_keys": ("acc += w[j] * vc[", "acc += w[j] * kc["),
     "seq_len_without_new_tokens": ("seq_lens[r] = c + n;", "seq_lens[r] = c;"),
+    "token_index_row_stride": ("(int64_t)req_indices[t] * max_model_len;",
+                               "(int64_t)req_indices[t] * max_num_reqs;"),
+    "discard_when_caught_up": ("optimistic_seq_len < (int64_t)request_num_tokens[r];",
+                               "optimistic_seq_len <= (int64_t)request_num_tokens[r];"),
+    "discard_ignores_scheduled": (
+        "(int64_t)num_computed_tokens[r] + (int64_t)num_scheduled_tokens[r];",
+        "(int64_t)num_computed_tokens[r];"),
+    "spec_rows_from_slice_start": ("logits_indices[row++] = last - d + k;",
+                                   "logits_indices[row++] = query_start_loc[r] + k;"),
+    "spec_drafts_ignored": ("int32_t d = num_draft_tokens ? num_draft_tokens[r] : 0;",
+                            "int32_t d = 0;"),
     "gather_wrong_offset": ("int64_t slot = (int64_t)phys * jb->block_size + j % jb->block_size;",
                             "int64_t slot = (int64_t)phys * jb->block_size + j / jb->block_size;"),
 }
