@@ -7,6 +7,9 @@
  *   pa_prepare_inputs  the per-step index tensors (request of each token,
  *                      positions, query_start_loc, seq_lens, slot_mapping,
  *                      logits_indices);
+ *   pa_prepare_inputs_ex  the same plus input_ids (gathered through
+ *                      token_indices), the discard mask and the sampled rows
+ *                      of speculative decoding;
  *   pa_cache_write     each new token's K and V copied to its cache slot;
  *   pa_attention       causal grouped-query attention of every token over
  *                      its own request's context, read through the block
@@ -75,7 +78,12 @@ enum {
     PA_CHECK_SLOT = 1u << 4,           /* slot_mapping entry >= num_blocks * block_size */
     PA_CHECK_SEQ_LEN = 1u << 5,        /* seq_lens[r] < query length, qsl decreasing, or
                                           a context wider than the table */
-    PA_CHECK_TIMEOUT = 1u << 6         /* a bounded wait inside a kernel ran out */
+    PA_CHECK_TIMEOUT = 1u << 6,        /* a bounded wait inside a kernel ran out */
+    PA_CHECK_TOKEN_INDEX = 1u << 7,    /* a token's position >= max_model_len (its id
+                                          would come from another request's row) */
+    PA_CHECK_DRAFT_COUNT = 1u << 8     /* num_draft_tokens[r] < 0 or >=
+                                          num_scheduled_tokens[r], or num_reqs +
+                                          sum(num_draft_tokens) != num_logits */
 };
 
 /*
@@ -121,6 +129,73 @@ pa_status pa_prepare_inputs(const int32_t *num_scheduled_tokens,
                             int32_t *slot_mapping, int32_t *query_start_loc,
                             int32_t qsl_capacity, int32_t *seq_lens,
                             int32_t *logits_indices, pa_stream_t stream);
+
+/*
+ * pa_prepare_inputs_ex -- pa_prepare_inputs plus the rest of the step's
+ * input preparation, in the same single launch.
+ *
+ * Defined by "Building the Batch", sections "How they are computed" (token
+ * ids gathered through token_indices = positions + req_indices * M) and
+ * "Only one row per request reaches the vocabulary" (with speculative
+ * decoding a request needs one row per draft token plus one), and by "vLLM's
+ * Model Runner", sections "Flattening the batch into one token axis", "The
+ * two things this method returns" and "The batch contains rows that must not
+ * be sampled" (the discard mask).  Everything pa_prepare_inputs computes is
+ * computed identically; in addition, each optional group below runs when its
+ * pointers are given:
+ *
+ *   token-id gather (max_model_len > 0):
+ *     token_ids is the per-request token buffer [max_num_reqs][max_model_len]
+ *     (int32, row-major; row r holds batch row r's ids).  It may be device
+ *     memory or host memory the device can read (page-locked host memory
+ *     from cudaHostAlloc / cudaMallocHost, or pageable memory on systems
+ *     whose devices report pageable-memory access).
+ *       token_indices[t] = positions[t] + req_indices[t] * max_model_len  (int64)
+ *       input_ids[t]     = token_ids[token_indices[t]]
+ *     A token whose position is >= max_model_len gets -1 in both and sets
+ *     PA_CHECK_TOKEN_INDEX.
+ *   discard mask (request_num_tokens != NULL):
+ *     discard_request_mask[r] = (num_computed_tokens[r] + num_scheduled_tokens[r]
+ *                                < request_num_tokens[r])   (one byte, 0 or 1)
+ *     request_num_tokens[r] is the request's total known token count
+ *     (prompt plus output so far).
+ *   sampled rows:
+ *     num_draft_tokens == NULL: num_logits must equal num_reqs, and
+ *       logits_indices[r] = query_start_loc[r+1] - 1 (as pa_prepare_inputs);
+ *     otherwise, with d = num_draft_tokens[r], request r owns the d + 1
+ *       entries cu_num_logits[r] .. cu_num_logits[r+1] - 1 of logits_indices,
+ *       cu_num_logits being the exclusive scan of (num_draft_tokens + 1), and
+ *       logits_indices[cu_num_logits[r] + k] = query_start_loc[r+1] - 1 - d + k,
+ *       k = 0..d: the last d + 1 rows of its slice.  num_logits must be
+ *       num_reqs + sum(num_draft_tokens) (known to the host); a mismatch or a
+ *       draft count outside [0, num_scheduled_tokens[r]) sets
+ *       PA_CHECK_DRAFT_COUNT and no row past num_logits is written.
+ *     cu_num_logits [num_reqs + 1] is optional (NULL skips it).
+ *
+ * Errors: as pa_prepare_inputs, plus PA_ERR_INVALID when a group is half
+ * given (max_model_len > 0 without token_ids, or without token_indices /
+ * input_ids while num_tokens > 0; max_model_len == 0 with any of the three;
+ * request_num_tokens
+ * without discard_request_mask or the reverse), max_num_reqs < num_reqs,
+ * max_model_len < 0, num_logits != num_reqs without drafts, num_logits < 0,
+ * or a token buffer the current device cannot read.
+ */
+pa_status pa_prepare_inputs_ex(const int32_t *num_scheduled_tokens,
+                               const int32_t *num_computed_tokens,
+                               const int32_t *block_table, int32_t num_reqs,
+                               int32_t max_blocks_per_req, int32_t block_size,
+                               int32_t num_tokens, int32_t num_blocks,
+                               const int32_t *token_ids, int32_t max_num_reqs,
+                               int32_t max_model_len,
+                               const int32_t *request_num_tokens,
+                               const int32_t *num_draft_tokens, int32_t num_logits,
+                               int32_t *req_indices, int32_t *positions,
+                               int32_t *slot_mapping, int32_t *query_start_loc,
+                               int32_t qsl_capacity, int32_t *seq_lens,
+                               int64_t *token_indices, int32_t *input_ids,
+                               uint8_t *discard_request_mask,
+                               int32_t *logits_indices, int32_t *cu_num_logits,
+                               pa_stream_t stream);
 
 /*
  * pa_cache_write -- scatter the step's new K and V into the cache.

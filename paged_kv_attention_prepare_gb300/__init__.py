@@ -6,9 +6,9 @@ stream to the C ABI in ``include/pa.h``.  Every step runs in the library's
 CUDA kernels; there is no CPU or PyTorch fallback, and using the package
 without the built library raises immediately.
 
-Functions carry the C names: ``pa_prepare_inputs``, ``pa_cache_write``,
-``pa_attention_workspace_size``, ``pa_attention``, ``pa_attention_noalloc``,
-``pa_get_status``, ``pa_launch_count``.
+Functions carry the C names: ``pa_prepare_inputs``, ``pa_prepare_inputs_ex``,
+``pa_cache_write``, ``pa_attention_workspace_size``, ``pa_attention``,
+``pa_attention_noalloc``, ``pa_get_status``, ``pa_launch_count``.
 """
 
 from __future__ import annotations
@@ -29,6 +29,7 @@ PA_BF16, PA_FP16 = 0, 1
 CHECK_BITS = {
     "empty_request": 1 << 0, "token_count": 1 << 1, "block_id": 1 << 2,
     "logical_block": 1 << 3, "slot": 1 << 4, "seq_len": 1 << 5, "timeout": 1 << 6,
+    "token_index": 1 << 7, "draft_count": 1 << 8,
 }
 
 _DTYPES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
@@ -62,6 +63,10 @@ def lib():
             L.pa_prepare_inputs.restype = ctypes.c_int
             L.pa_prepare_inputs.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                             i32, vp, vp, vp]
+            L.pa_prepare_inputs_ex.restype = ctypes.c_int
+            L.pa_prepare_inputs_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
+                                               vp, vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp,
+                                               vp, vp, vp]
             L.pa_cache_write.restype = ctypes.c_int
             L.pa_cache_write.argtypes = [vp, vp, i64, vp, vp, vp, i32, i32, i32, i32, i32,
                                          ctypes.c_int, vp]
@@ -130,6 +135,55 @@ def pa_prepare_inputs(num_scheduled_tokens, num_computed_tokens, block_table, bl
         query_start_loc.shape[0], _dev(seq_lens, "seq_lens", i32),
         _dev(logits_indices, "logits_indices", i32), _stream(stream))
     _check(rc, "pa_prepare_inputs")
+
+
+def _opt(t, name, dtype):
+    return None if t is None else _dev(t, name, dtype)
+
+
+def pa_prepare_inputs_ex(num_scheduled_tokens, num_computed_tokens, block_table, block_size,
+                         num_tokens, num_blocks, req_indices, positions, slot_mapping,
+                         query_start_loc, seq_lens, logits_indices, token_ids=None,
+                         token_indices=None, input_ids=None, request_num_tokens=None,
+                         discard_request_mask=None, num_draft_tokens=None, cu_num_logits=None,
+                         stream=None):
+    """``pa_prepare_inputs`` plus the token-id gather (``token_ids`` is the
+    [max_num_reqs, max_model_len] int32 buffer, a CUDA tensor or a pinned CPU
+    tensor; ``token_indices`` int64 and ``input_ids`` int32 [T] receive the
+    result), the discard mask (``request_num_tokens`` int32 [R] in,
+    ``discard_request_mask`` bool/uint8 [R] out) and the sampled rows of
+    speculative decoding (``num_draft_tokens`` int32 [R]; ``logits_indices``
+    then holds R + sum(drafts) rows, ``cu_num_logits`` [R+1] their starts)."""
+    i32 = torch.int32
+    R = num_scheduled_tokens.shape[0]
+    if token_ids is not None:
+        if token_ids.dtype != i32 or token_ids.dim() != 2 or not token_ids.is_contiguous():
+            raise TypeError("token_ids must be a contiguous int32 [max_num_reqs, max_model_len]")
+        if not (token_ids.is_cuda or token_ids.is_pinned()):
+            raise TypeError("token_ids must be a CUDA tensor or a pinned CPU tensor")
+        tok_ptr = ctypes.c_void_p(token_ids.data_ptr())
+        rows, width = token_ids.shape
+    else:
+        tok_ptr, rows, width = None, 0, 0
+    mask_ptr = None
+    if discard_request_mask is not None:
+        if discard_request_mask.dtype not in (torch.bool, torch.uint8):
+            raise TypeError("discard_request_mask must be bool or uint8")
+        mask_ptr = _dev(discard_request_mask, "discard_request_mask")
+    rc = lib().pa_prepare_inputs_ex(
+        _dev(num_scheduled_tokens, "num_scheduled_tokens", i32),
+        _dev(num_computed_tokens, "num_computed_tokens", i32),
+        _dev(block_table, "block_table", i32), R, block_table.shape[1] if R else 0,
+        int(block_size), int(num_tokens), int(num_blocks), tok_ptr, rows, width,
+        _opt(request_num_tokens, "request_num_tokens", i32),
+        _opt(num_draft_tokens, "num_draft_tokens", i32), logits_indices.shape[0],
+        _dev(req_indices, "req_indices", i32), _dev(positions, "positions", i32),
+        _dev(slot_mapping, "slot_mapping", i32), _dev(query_start_loc, "query_start_loc", i32),
+        query_start_loc.shape[0], _dev(seq_lens, "seq_lens", i32),
+        _opt(token_indices, "token_indices", torch.int64), _opt(input_ids, "input_ids", i32),
+        mask_ptr, _dev(logits_indices, "logits_indices", i32),
+        _opt(cu_num_logits, "cu_num_logits", i32), _stream(stream))
+    _check(rc, "pa_prepare_inputs_ex")
 
 
 def pa_cache_write(key, value, key_cache, value_cache, slot_mapping, num_blocks=None,

@@ -87,6 +87,48 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_slots, int 
 
 using namespace pa;
 
+namespace {
+
+// Checks and argument packing shared by both index-build entry points.
+pa_status check_prepare_core(const PrepArgs &a) {
+    if (a.R < 0 || a.T < 0 || a.bs <= 0 || a.NB < 0 || a.MB < 0 || a.qsl_cap < a.R + 1)
+        return PA_ERR_INVALID;
+    if (!a.qsl) return PA_ERR_INVALID;
+    if (a.R > 0 && (!a.nst || !a.nct || !a.seq_lens || (a.MB > 0 && !a.bt)))
+        return PA_ERR_INVALID;
+    if (a.num_logits > 0 && !a.logits) return PA_ERR_INVALID;
+    if (a.T > 0 && (!a.req || !a.pos || !a.slot)) return PA_ERR_INVALID;
+    if ((int64_t)a.NB * a.bs >= (int64_t)INT32_MAX) return PA_ERR_INVALID;
+    return PA_OK;
+}
+
+// True when a kernel on the current device can dereference `p` as given.
+bool device_readable(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+        return true;
+    case cudaMemoryTypeHost:
+        // Page-locked host memory: readable at the same address under
+        // unified addressing.
+        return at.devicePointer == p;
+    default: {
+        int dev = current_device(), pageable = 0;
+        if (dev < 0 || cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) !=
+                           cudaSuccess)
+            return false;
+        return pageable != 0;
+    }
+    }
+}
+
+}  // namespace
+
 extern "C" {
 
 pa_status pa_prepare_inputs(const int32_t *num_scheduled_tokens, const int32_t *num_computed_tokens,
@@ -95,19 +137,83 @@ pa_status pa_prepare_inputs(const int32_t *num_scheduled_tokens, const int32_t *
                             int32_t num_blocks, int32_t *req_indices, int32_t *positions,
                             int32_t *slot_mapping, int32_t *query_start_loc, int32_t qsl_capacity,
                             int32_t *seq_lens, int32_t *logits_indices, pa_stream_t stream) {
-    if (num_reqs < 0 || num_tokens < 0 || block_size <= 0 || num_blocks < 0 ||
-        max_blocks_per_req < 0 || qsl_capacity < num_reqs + 1)
+    PrepArgs a{};
+    a.nst = num_scheduled_tokens;
+    a.nct = num_computed_tokens;
+    a.bt = block_table;
+    a.R = num_reqs;
+    a.MB = max_blocks_per_req;
+    a.bs = block_size;
+    a.T = num_tokens;
+    a.NB = num_blocks;
+    a.num_logits = num_reqs;
+    a.req = req_indices;
+    a.pos = positions;
+    a.slot = slot_mapping;
+    a.qsl = query_start_loc;
+    a.qsl_cap = qsl_capacity;
+    a.seq_lens = seq_lens;
+    a.logits = logits_indices;
+    const pa_status st = check_prepare_core(a);
+    if (st != PA_OK) return st;
+    return launch_prepare(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_prepare_inputs_ex(const int32_t *num_scheduled_tokens,
+                               const int32_t *num_computed_tokens, const int32_t *block_table,
+                               int32_t num_reqs, int32_t max_blocks_per_req, int32_t block_size,
+                               int32_t num_tokens, int32_t num_blocks, const int32_t *token_ids,
+                               int32_t max_num_reqs, int32_t max_model_len,
+                               const int32_t *request_num_tokens,
+                               const int32_t *num_draft_tokens, int32_t num_logits,
+                               int32_t *req_indices, int32_t *positions, int32_t *slot_mapping,
+                               int32_t *query_start_loc, int32_t qsl_capacity, int32_t *seq_lens,
+                               int64_t *token_indices, int32_t *input_ids,
+                               uint8_t *discard_request_mask, int32_t *logits_indices,
+                               int32_t *cu_num_logits, pa_stream_t stream) {
+    PrepArgs a{};
+    a.nst = num_scheduled_tokens;
+    a.nct = num_computed_tokens;
+    a.bt = block_table;
+    a.R = num_reqs;
+    a.MB = max_blocks_per_req;
+    a.bs = block_size;
+    a.T = num_tokens;
+    a.NB = num_blocks;
+    a.token_ids = token_ids;
+    a.max_num_reqs = max_num_reqs;
+    a.M = max_model_len;
+    a.req_num_tokens = request_num_tokens;
+    a.num_draft = num_draft_tokens;
+    a.num_logits = num_logits;
+    a.req = req_indices;
+    a.pos = positions;
+    a.slot = slot_mapping;
+    a.qsl = query_start_loc;
+    a.qsl_cap = qsl_capacity;
+    a.seq_lens = seq_lens;
+    a.token_indices = token_indices;
+    a.input_ids = input_ids;
+    a.discard = discard_request_mask;
+    a.logits = logits_indices;
+    a.cu_logits = cu_num_logits;
+    const pa_status st = check_prepare_core(a);
+    if (st != PA_OK) return st;
+    if (num_logits < 0 || (!num_draft_tokens && num_logits != num_reqs)) return PA_ERR_INVALID;
+    // token-id gather group
+    if (max_model_len < 0) return PA_ERR_INVALID;
+    if (max_model_len > 0) {
+        if (!token_ids || max_num_reqs < num_reqs ||
+            (num_tokens > 0 && (!token_indices || !input_ids)))
+            return PA_ERR_INVALID;
+        if (!device_readable(token_ids)) return PA_ERR_INVALID;
+    } else if (token_ids || token_indices || input_ids) {
         return PA_ERR_INVALID;
-    if (!query_start_loc) return PA_ERR_INVALID;
-    if (num_reqs > 0 && (!num_scheduled_tokens || !num_computed_tokens || !seq_lens ||
-                         !logits_indices || (max_blocks_per_req > 0 && !block_table)))
+    }
+    // discard group
+    if ((request_num_tokens == nullptr) != (discard_request_mask == nullptr))
         return PA_ERR_INVALID;
-    if (num_tokens > 0 && (!req_indices || !positions || !slot_mapping)) return PA_ERR_INVALID;
-    if ((int64_t)num_blocks * block_size >= (int64_t)INT32_MAX) return PA_ERR_INVALID;
-    return launch_prepare(num_scheduled_tokens, num_computed_tokens, block_table, num_reqs,
-                          max_blocks_per_req, block_size, num_tokens, num_blocks, req_indices,
-                          positions, slot_mapping, query_start_loc, qsl_capacity, seq_lens,
-                          logits_indices, reinterpret_cast<cudaStream_t>(stream));
+    return launch_prepare(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_stride,

@@ -23,11 +23,27 @@ unsigned int *status_word();
 void note_launch(int n = 1);
 int num_sms();
 
-pa_status launch_prepare(const int32_t *nst, const int32_t *nct, const int32_t *bt,
-                         int32_t R, int32_t MB, int32_t bs, int32_t T, int32_t NB,
-                         int32_t *req, int32_t *pos, int32_t *slot, int32_t *qsl,
-                         int32_t qsl_cap, int32_t *seq_lens, int32_t *logits,
-                         cudaStream_t stream);
+// Inputs and outputs of the index build.  The three optional groups are off
+// when their pointers are NULL: the token-id gather (M > 0), the discard mask
+// and the draft tokens (then num_logits == R, one row per request).
+struct PrepArgs {
+    const int32_t *nst, *nct, *bt;
+    int32_t R, MB, bs, T, NB;
+    const int32_t *token_ids;       // [max_num_reqs][M], device-readable
+    int32_t max_num_reqs, M;
+    const int32_t *req_num_tokens;  // [R]
+    const int32_t *num_draft;       // [R]
+    int32_t num_logits;
+    int32_t *req, *pos, *slot, *qsl;
+    int32_t qsl_cap;
+    int32_t *seq_lens;
+    int64_t *token_indices;
+    int32_t *input_ids;
+    uint8_t *discard;
+    int32_t *logits, *cu_logits;
+};
+
+pa_status launch_prepare(const PrepArgs &a, cudaStream_t stream);
 
 pa_status launch_cache_write(const void *key, const void *value, int64_t stride_elems,
                              void *kc, void *vc, const int32_t *slots, int32_t T,

@@ -76,6 +76,39 @@ def test_prepare_rejects_small_qsl_capacity_and_huge_pool():
                                4, FAKE, FAKE, None) == pa.PA_ERR_INVALID
 
 
+@pytest.mark.parametrize("case", ["gather_without_ids", "ids_without_width", "negative_width",
+                                  "rows_below_reqs", "mask_without_counts",
+                                  "counts_without_mask", "logits_count_without_drafts",
+                                  "negative_logits", "qsl_capacity"])
+def test_prepare_ex_rejects_half_given_groups(case):
+    L = pa.lib()
+    a = dict(tok=None, rows=0, width=0, ntok=None, drafts=None, nlog=3, ti=None, ids=None,
+             mask=None, cap=4)
+    if case == "gather_without_ids":
+        a.update(tok=FAKE, rows=3, width=8, ti=FAKE)             # input_ids missing
+    elif case == "ids_without_width":
+        a.update(tok=FAKE, rows=3, ti=FAKE, ids=FAKE)            # max_model_len == 0
+    elif case == "negative_width":
+        a.update(width=-1)
+    elif case == "rows_below_reqs":
+        a.update(tok=FAKE, rows=2, width=8, ti=FAKE, ids=FAKE)
+    elif case == "mask_without_counts":
+        a.update(mask=FAKE)
+    elif case == "counts_without_mask":
+        a.update(ntok=FAKE)
+    elif case == "logits_count_without_drafts":
+        a.update(nlog=5)
+    elif case == "negative_logits":
+        a.update(drafts=FAKE, nlog=-1)
+    else:
+        a.update(cap=3)
+    rc = L.pa_prepare_inputs_ex(FAKE, FAKE, FAKE, 3, 2, 16, 5, 8, a["tok"], a["rows"],
+                                a["width"], a["ntok"], a["drafts"], a["nlog"], FAKE, FAKE, FAKE,
+                                FAKE, a["cap"], FAKE, a["ti"], a["ids"], a["mask"], FAKE, None,
+                                None)
+    assert rc == pa.PA_ERR_INVALID
+
+
 def test_cache_write_rejects_short_stride_and_bad_dtype():
     L = pa.lib()
     assert L.pa_cache_write(FAKE, FAKE, 100, FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, pa.PA_BF16,

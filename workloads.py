@@ -20,6 +20,10 @@ Recipe (the same for every named workload):
 * Values: every element of q, the new tokens' key/value and the whole cache
   pool is N(0, 1) drawn by a seeded ``torch.Generator`` on the requested
   device, rounded to bf16 / fp16 (round to nearest even).
+* Request state for the rest of input preparation: a token buffer of random
+  ids (vocabulary 128,256), each request's total known token count (caught
+  up or mid-prompt, half each) and draft counts for speculative decoding
+  (uniform up to 7, never more than scheduled - 1).
 """
 
 from __future__ import annotations
@@ -237,6 +241,50 @@ def random_case(seed: int, *, max_reqs: int = 6, max_new: int = 40,
     d = int(head_dim or rng.choice([64, 128]))
     dt = dtype or str(rng.choice(["bf16", "fp16"]))
     return _make(f"random-{seed}", nst, nct, rng, hkv * g, hkv, d, dt)
+
+
+# ---------------------------------------------------------------------------
+# Request state around the step: token lists, known totals, draft counts
+# ---------------------------------------------------------------------------
+
+VOCAB = 128_256
+
+
+def make_token_buffer(w: Workload, seed: int = 0, max_num_reqs: int | None = None,
+                      max_model_len: int | None = None) -> np.ndarray:
+    """The per-request token buffer: int32 ``[max_num_reqs, max_model_len]``
+    of random ids in [0, VOCAB).  Row r stands for batch row r's prompt plus
+    output so far; every row is filled to the full width (a real buffer
+    leaves its tail stale, and the step never reads past a request's
+    positions).  Defaults: ``max_num_reqs = R + 3`` (spare rows) and
+    ``max_model_len`` = the longest context rounded up to 16."""
+    rng = np.random.default_rng(seed + 7_001)
+    rows = w.num_reqs + 3 if max_num_reqs is None else int(max_num_reqs)
+    width = max_model_len
+    if width is None:
+        width = max(16, -(-int(w.context_lens.max(initial=1)) // 16) * 16)
+    return rng.integers(0, VOCAB, size=(rows, int(width)), dtype=np.int32)
+
+
+def make_request_totals(w: Workload, seed: int = 0, p_caught_up: float = 0.5) -> np.ndarray:
+    """Each request's total known token count (prompt plus output so far).
+    With probability ``p_caught_up`` it equals computed + scheduled (the
+    step reaches it: a decode, or a prompt's last chunk); otherwise the
+    prompt continues for 1..2000 more tokens (a prefill chunk mid-prompt)."""
+    rng = np.random.default_rng(seed + 7_002)
+    reach = w.num_computed_tokens.astype(np.int64) + w.num_scheduled_tokens
+    more = rng.integers(1, 2001, size=w.num_reqs)
+    caught = rng.random(w.num_reqs) < p_caught_up
+    return np.where(caught, reach, reach + more).astype(np.int32)
+
+
+def make_draft_counts(w: Workload, seed: int = 0, max_drafts: int = 7) -> np.ndarray:
+    """Draft tokens each request verifies this step: uniform in
+    [0, min(max_drafts, scheduled - 1)] (the drafts are among the request's
+    scheduled tokens, so a one-token request has none)."""
+    rng = np.random.default_rng(seed + 7_003)
+    hi = np.minimum(max_drafts, w.num_scheduled_tokens - 1)
+    return (rng.random(w.num_reqs) * (hi + 1)).astype(np.int32).clip(0, hi)
 
 
 # ---------------------------------------------------------------------------
