@@ -5,10 +5,12 @@ paged attention) on synthetic workloads shaped like the pages' examples.
                     [--impl ours|reference]
 
 Prints one JSON line.  A step is the whole path over one batch: the three
-C-ABI calls on inputs already resident in HBM.  The L2 is flushed (a 256 MB
-write) between timed steps, outside the timed events.  ``e2e`` repeats the
-step through the same public calls with the step's inputs copied from pinned
-host memory and the output copied back inside the timed region.
+C-ABI calls on inputs already resident in HBM, captured once into a CUDA
+graph and replayed once per step (``eager`` reports the same calls launched
+one by one).  The L2 is flushed (a 256 MB write) between timed steps,
+outside the timed events.  ``e2e`` repeats the step through the same public
+calls with the step's inputs copied from pinned host memory and the output
+copied back inside the timed region.
 
 Under torchrun every rank runs an independent replica (its own pool and
 requests, seeded by rank): the path has no exchange step.  Timing is the max
@@ -26,6 +28,7 @@ import json
 import os
 import re
 import subprocess
+import threading
 import sys
 import time
 
@@ -47,7 +50,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode", choices=sorted(workloads.NAMED))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -149,17 +152,69 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled during the timed
+    region.  Reads NVML directly (every 20 ms, from a thread; read-only
+    queries), else falls back to ``nvidia-smi -lms 200``."""
 
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, index: int, uuid: str | None = None):
+        self.index, self.uuid = index, uuid
         self.proc = None
+        self.samples = []          # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            u = self.uuid if self.uuid.startswith("GPU-") else "GPU-" + self.uuid
+            ok = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index),
+                                                   ctypes.byref(h)) == 0
+        if not ok:
+            lib.nvmlShutdown()
+            return False
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # 1 = SM clock
+            self.max_mhz = float(mx.value)
+        self._nvml, self._handle = lib, h
+        return True
+
+    def _poll(self):
+        import ctypes
+        lib, h = self._nvml, self._handle
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if get_reasons(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            self._stop.wait(0.02)
 
     def __enter__(self):
+        if self._open_nvml():
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -170,7 +225,11 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+            self._nvml.nvmlShutdown()
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -178,27 +237,28 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            names = [0x8, 0x40, 0x20, 0x4]
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm, self.max_mhz = float(parts[1]), float(parts[2])
+                except ValueError:
+                    continue
+                bits = sum(b for b, v in zip(names, parts[5:9]) if v.lower() == "active")
+                self.samples.append((sm, bits))
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in getattr(self, "lines", []):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not self.samples:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for _, bits in self.samples:
+            reasons |= {n for b, n in self.REASONS.items() if bits & b}
+        return {"sm_mhz": float(np.median([c for c, _ in self.samples])),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi"}
 
 
 # ---------------------------------------------------------------------------
@@ -308,13 +368,15 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(nst=nst, nct=nct, bt=bt, q=q, key=key, value=value):
+    def step(nst=nst, nct=nct, bt=bt, q=q, key=key, value=value, timed=True):
         pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot, qsl,
                              sl, li)
         pa.pa_cache_write(key, value, kc, vc, slot)
-        a0.record(stream)
+        if timed:
+            a0.record(stream)
         pa.pa_attention(q, kc, vc, bt, qsl, sl, w.max_query_len, w.max_seq_len, w.scale, out, ws)
-        a1.record(stream)
+        if timed:
+            a1.record(stream)
 
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(max(args.warmup, 0)):
@@ -325,15 +387,35 @@ def run_ours(args):
     if status != pa.PA_OK:
         raise RuntimeError(f"device checks failed during warm-up: {pa.check_bits(detail)}")
 
-    # ---- timed region: device-resident inputs
+    # ---- the step captured once into a CUDA graph (the three calls, same
+    # buffers); the launches of one replay are counted at capture
+    graph, graph_error = None, None
+    pa.pa_launch_count()
+    try:
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gstream):
+            step(timed=False)
+        torch.cuda.synchronize()
+    except RuntimeError as exc:  # capture refused: report it, time the calls eagerly
+        graph, graph_error = None, str(exc).splitlines()[0]
+    launches_per_replay = pa.pa_launch_count()
+
+    # ---- timed regions: device-resident inputs.  (1) the calls launched one
+    # by one (per-step events also bracket the attention call); (2) graph
+    # replays, the headline when the capture succeeded.
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    pa.pa_launch_count()
-    with ClockSampler(local) as clocks:
+    g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "") or None
+    with ClockSampler(local, uuid) as clocks:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        pa.pa_launch_count()
         for k in range(args.steps):
             flush.zero_()
             s0, s1, b0, b1 = ev[k]
@@ -342,15 +424,76 @@ def run_ours(args):
             step()
             s1.record(stream)
         torch.cuda.synchronize()
-    launches = pa.pa_launch_count()
-    if dist is not None:
-        dist.barrier()
+        eager_launches = pa.pa_launch_count()
+        if dist is not None:
+            dist.barrier()
+        if graph is not None:
+            for _ in range(max(args.warmup, 1)):
+                flush.zero_()
+                graph.replay()
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize()
+            for k in range(args.steps):
+                flush.zero_()
+                g_ev[k][0].record(stream)
+                graph.replay()
+                g_ev[k][1].record(stream)
+            torch.cuda.synchronize()
+            if dist is not None:
+                dist.barrier()
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     attn_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    total_ms = reduce_over_ranks(float(np.sum(step_ms)), "max", dist, dev)
-    ms_per_step = total_ms / args.steps
+    eager_ms = reduce_over_ranks(float(np.sum(step_ms)), "max", dist, dev) / args.steps
     all_tokens = reduce_over_ranks(T, "sum", dist, dev)
+    if graph is not None:
+        graph_ms = reduce_over_ranks(float(np.sum([x.elapsed_time(y) for x, y in g_ev])), "max",
+                                     dist, dev) / args.steps
+        ms_per_step, launches = graph_ms, launches_per_replay * args.steps
+        del graph
+    else:
+        graph_ms, ms_per_step, launches = None, eager_ms, eager_launches
     value = all_tokens / (ms_per_step / 1e3)
+    status, detail = pa.pa_get_status()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device checks failed in the timed region: {pa.check_bits(detail)}")
+
+    # ---- the index build alone: the plain call vs. the extended one (token-id
+    # gather from a device or page-locked host token buffer, discard mask)
+    def time_calls(fn, reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        for k in range(max(args.warmup, 1) + reps):
+            flush.zero_()
+            if k >= max(args.warmup, 1):
+                evs[k - max(args.warmup, 1)][0].record(stream)
+            fn()
+            if k >= max(args.warmup, 1):
+                evs[k - max(args.warmup, 1)][1].record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs])) * 1e3
+
+    tok_buf = workloads.make_token_buffer(w, 1 + rank)
+    tok_dev = torch.from_numpy(tok_buf).to(dev)
+    tok_host = torch.from_numpy(tok_buf).pin_memory()
+    totals = up(workloads.make_request_totals(w, 1 + rank))
+    tok_idx = torch.empty(T, dtype=torch.int64, device=dev)
+    in_ids = torch.empty(T, dtype=i32, device=dev)
+    discard = torch.empty(R, dtype=torch.uint8, device=dev)
+
+    def prep_ex(ids):
+        pa.pa_prepare_inputs_ex(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot, qsl,
+                                sl, li, token_ids=ids, token_indices=tok_idx, input_ids=in_ids,
+                                request_num_tokens=totals, discard_request_mask=discard)
+
+    prep_us = {
+        "pa_prepare_inputs": time_calls(
+            lambda: pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos,
+                                         slot, qsl, sl, li), args.steps),
+        "pa_prepare_inputs_ex_device_tokens": time_calls(lambda: prep_ex(tok_dev), args.steps),
+        "pa_prepare_inputs_ex_host_tokens": time_calls(lambda: prep_ex(tok_host), args.steps),
+    }
+    del tok_dev, tok_host
 
     # ---- end to end: inputs from pinned host memory, output back to host
     host_in = {"nst": w.num_scheduled_tokens, "nct": w.num_computed_tokens, "bt": w.block_table}
@@ -475,6 +618,12 @@ def run_ours(args):
             "gpu_launches": int(launches),
             "clocks": clocks.summary(),
             "attn_us_per_step": float(np.mean(attn_ms)) * 1e3,
+            "prep_us": prep_us,
+            "launch": ("cuda_graph: the three calls captured once, one replay per step"
+                       if graph_ms is not None else f"eager (graph capture failed: {graph_error})"),
+            "eager": {"ms_per_step": eager_ms, "value": all_tokens / (eager_ms / 1e3),
+                      "unit": UNIT, "gpu_launches": int(eager_launches),
+                      "what": "the three C-ABI calls launched one by one per step"},
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
