@@ -19,6 +19,11 @@ Parity status of each function (how it is pinned, in ``tests/test_oracle.py``):
   (drafts all zero reduce to query_start_loc[1:] - 1) and by invariants of the
   draft case (length R + sum(d); each request's rows are consecutive, inside
   its own slice and end on its last row).
+* ``copy_blocks`` / ``zero_blocks`` -- pinned by NumPy block slicing (a
+  library copy), untouched-block preservation, and the beam-search scenario
+  (after a copy and a table remap, the diverging beam attends over exactly
+  what it attended over before, and its new token no longer reaches the
+  other beam).
 * ``cache_write`` -- pinned by bit equality against a direct per-slot copy,
   untouched-slot preservation and write-then-gather round trips.
 * ``attention`` -- pinned by closed forms (one visible key, K = 0, constant V,
@@ -89,6 +94,12 @@ def _load():
             lib.oracle_spec_logits_indices.restype = ctypes.c_int
             lib.oracle_spec_logits_indices.argtypes = [
                 i32p, i32p, ctypes.c_int32, ctypes.c_int32, i32p, i32p]
+            for fn in (lib.oracle_copy_blocks, lib.oracle_zero_blocks):
+                fn.restype = ctypes.c_int
+            lib.oracle_copy_blocks.argtypes = [u16p, u16p, ctypes.c_int64, ctypes.c_int32, i32p,
+                                               i32p, ctypes.c_int32]
+            lib.oracle_zero_blocks.argtypes = [u16p, u16p, ctypes.c_int64, ctypes.c_int32, i32p,
+                                               ctypes.c_int32]
             lib.oracle_cache_write.restype = ctypes.c_int
             lib.oracle_cache_write.argtypes = [
                 u16p, u16p, ctypes.c_int64, u16p, u16p, i32p, ctypes.c_int32,
@@ -206,6 +217,49 @@ def spec_logits_indices(query_start_loc, num_draft_tokens=None, num_logits=None,
     if check and rc != 0:
         raise OracleError(f"oracle_spec_logits_indices rejected the inputs ({rc})")
     return rows, cu, int(rc)
+
+
+def _pool_bytes(pool) -> np.ndarray:
+    """A private byte copy of a pool ([NB, ...], any element type; a torch
+    tensor or a NumPy array), shaped [NB, block_bytes]."""
+    if isinstance(pool, np.ndarray):
+        a = np.ascontiguousarray(pool)
+    else:
+        import torch  # local: torch only as a carrier of the pool's bytes
+        t = pool.detach().to("cpu").contiguous()
+        a = t.view(torch.uint8).numpy() if t.element_size() == 1 else \
+            t.view(torch.int16).numpy()
+    nb = a.shape[0]
+    return a.view(np.uint8).reshape(nb, -1).copy()
+
+
+def copy_blocks(key_cache, value_cache, src_blocks, dst_blocks, check=True):
+    """Copy-on-write block copy.  Returns (key bytes, value bytes, status): the
+    pools as uint8 [NB, block_bytes] after block dst[i] became a copy of
+    block src[i] in both pools."""
+    lib = _load()
+    kb, vb = _pool_bytes(key_cache), _pool_bytes(value_cache)
+    src, dst = _i32(src_blocks), _i32(dst_blocks)
+    if src.shape != dst.shape or kb.shape != vb.shape:
+        raise OracleError("src/dst lengths or pool shapes differ")
+    rc = lib.oracle_copy_blocks(kb.ctypes.data, vb.ctypes.data, kb.shape[1], kb.shape[0],
+                                _p32(src), _p32(dst), src.shape[0])
+    if check and rc != 0:
+        raise OracleError(f"oracle_copy_blocks rejected the inputs ({rc})")
+    return kb, vb, int(rc)
+
+
+def zero_blocks(key_cache, value_cache, block_ids, check=True):
+    """Zero whole blocks of both pools.  Returns (key bytes, value bytes,
+    status) as uint8 [NB, block_bytes]."""
+    lib = _load()
+    kb, vb = _pool_bytes(key_cache), _pool_bytes(value_cache)
+    ids = _i32(block_ids)
+    rc = lib.oracle_zero_blocks(kb.ctypes.data, vb.ctypes.data, kb.shape[1], kb.shape[0],
+                                _p32(ids), ids.shape[0])
+    if check and rc != 0:
+        raise OracleError(f"oracle_zero_blocks rejected the inputs ({rc})")
+    return kb, vb, int(rc)
 
 
 def cache_write(key, value, key_cache, value_cache, slot_mapping, num_kv_heads, head_dim,

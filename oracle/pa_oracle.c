@@ -6,7 +6,7 @@
  * this library; the CUDA library never links, includes or calls it, and it
  * shares no code with the CUDA library.  Floating point is fp64 throughout.
  *
- * Six functions, each citing the passage it follows:
+ * Eight functions, each citing the passage it follows:
  *
  *   oracle_prepare_inputs  -- the per-step index tensors
  *       ("Building the Batch", sections "How they are computed" and
@@ -30,6 +30,14 @@
  *        per request reaches the vocabulary": without drafts one row per
  *        request, query_start_loc[1:] - 1; with d draft tokens a request
  *        needs d + 1 rows, read as the last d + 1 rows of its slice.
+ *   oracle_copy_blocks     -- "How vLLM Works Internally", section
+ *        "Copy-on-Write for Beam Search", step 3: the old block's contents
+ *        are copied to the newly allocated one (every slot, every head, both
+ *        the K and the V pool).  A byte copy.
+ *   oracle_zero_blocks     -- "Inside vLLM: Following One Request", the
+ *        scheduler output's new_block_ids_to_zero: freshly allocated blocks
+ *        are cleared before the forward pass.  Every byte of the block, in
+ *        both pools, becomes 0.
  *   oracle_cache_write     -- "Inside vLLM: Following One Request", section
  *        on reshape_and_cache_flash: token i's K and V are copied to slot
  *        slot_mapping[i].  A bit copy.
@@ -241,6 +249,55 @@ int oracle_spec_logits_indices(const int32_t *query_start_loc,
         cu_num_logits[num_reqs] = row;
     if (row != num_logits)
         err = err ? err : -3;
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Whole-block operations: copy-on-write copy, zeroing                       */
+/* ------------------------------------------------------------------------ */
+
+/* A block of a pool is block_bytes consecutive bytes starting at
+ * block * block_bytes (block_bytes = block_size * num_kv_heads * head_dim *
+ * element size).  Pairs are copied in order; the destinations are new
+ * blocks, so no destination is also a source. */
+int oracle_copy_blocks(uint8_t *key_cache, uint8_t *value_cache, int64_t block_bytes,
+                       int32_t num_blocks, const int32_t *src_blocks,
+                       const int32_t *dst_blocks, int32_t num_pairs)
+{
+    int err = 0;
+    if (block_bytes <= 0 || num_blocks < 0 || num_pairs < 0)
+        return -1;
+    for (int32_t i = 0; i < num_pairs; ++i) {
+        int32_t s = src_blocks[i], d = dst_blocks[i];
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+            err = -5;             /* a block outside the pool: that pair is skipped */
+            continue;
+        }
+        for (int64_t b = 0; b < block_bytes; ++b) {
+            key_cache[(int64_t)d * block_bytes + b] = key_cache[(int64_t)s * block_bytes + b];
+            value_cache[(int64_t)d * block_bytes + b] = value_cache[(int64_t)s * block_bytes + b];
+        }
+    }
+    return err;
+}
+
+int oracle_zero_blocks(uint8_t *key_cache, uint8_t *value_cache, int64_t block_bytes,
+                       int32_t num_blocks, const int32_t *block_ids, int32_t num_ids)
+{
+    int err = 0;
+    if (block_bytes <= 0 || num_blocks < 0 || num_ids < 0)
+        return -1;
+    for (int32_t i = 0; i < num_ids; ++i) {
+        int32_t blk = block_ids[i];
+        if (blk < 0 || blk >= num_blocks) {
+            err = -5;
+            continue;
+        }
+        for (int64_t b = 0; b < block_bytes; ++b) {
+            key_cache[(int64_t)blk * block_bytes + b] = 0;
+            value_cache[(int64_t)blk * block_bytes + b] = 0;
+        }
+    }
     return err;
 }
 

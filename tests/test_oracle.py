@@ -319,6 +319,122 @@ def test_spec_logits_rejects(bad):
 
 
 # ---------------------------------------------------------------------------
+# Whole-block operations: copy-on-write copy and zeroing
+# ---------------------------------------------------------------------------
+
+def _pools(seed, nb=12, bs=4, hkv=2, d=8, dtype=np.uint16):
+    rng = np.random.default_rng(seed)
+    k = rng.integers(0, 2**16, size=(nb, bs, hkv, d)).astype(dtype)
+    v = rng.integers(0, 2**16, size=(nb, bs, hkv, d)).astype(dtype)
+    return k, v
+
+
+@pytest.mark.parametrize("dtype", [np.uint16, np.uint8])
+def test_copy_blocks_equals_numpy_block_slicing(dtype):
+    for seed in range(20):
+        k, v = _pools(seed, dtype=dtype)
+        rng = np.random.default_rng(100 + seed)
+        n = int(rng.integers(0, 6))
+        blocks = rng.permutation(k.shape[0])
+        src, dst = blocks[:n], blocks[n:2 * n]          # fresh destinations
+        kb, vb, st = oracle.copy_blocks(k, v, src, dst)
+        assert st == 0
+        ke, ve = k.copy(), v.copy()
+        ke[dst] = k[src]
+        ve[dst] = v[src]
+        np.testing.assert_array_equal(kb.view(dtype).reshape(k.shape), ke)
+        np.testing.assert_array_equal(vb.view(dtype).reshape(v.shape), ve)
+
+
+def test_copy_blocks_one_source_many_beams():
+    # four beams fork from one shared block: each gets its own copy
+    k, v = _pools(3)
+    kb, vb, st = oracle.copy_blocks(k, v, [5, 5, 5, 5], [0, 1, 2, 3])
+    assert st == 0
+    kb = kb.view(np.uint16).reshape(k.shape)
+    vb = vb.view(np.uint16).reshape(v.shape)
+    for b in range(4):
+        np.testing.assert_array_equal(kb[b], k[5])
+        np.testing.assert_array_equal(vb[b], v[5])
+    np.testing.assert_array_equal(kb[4:], k[4:])
+
+
+def test_copy_blocks_skips_pairs_outside_the_pool():
+    k, v = _pools(4)
+    kb, vb, st = oracle.copy_blocks(k, v, [1, 12, -1, 2], [3, 4, 5, 6], check=False)
+    assert st != 0
+    kb = kb.view(np.uint16).reshape(k.shape)
+    np.testing.assert_array_equal(kb[3], k[1])
+    np.testing.assert_array_equal(kb[6], k[2])
+    np.testing.assert_array_equal(kb[4], k[4])          # skipped pairs leave dst alone
+    np.testing.assert_array_equal(kb[5], k[5])
+
+
+def test_zero_blocks_clears_exactly_those_blocks():
+    for dtype in (np.uint16, np.uint8):
+        k, v = _pools(5, dtype=dtype)
+        ids = [7, 0, 11]
+        kb, vb, st = oracle.zero_blocks(k, v, ids)
+        assert st == 0
+        kb, vb = kb.view(dtype).reshape(k.shape), vb.view(dtype).reshape(v.shape)
+        keep = [b for b in range(k.shape[0]) if b not in ids]
+        assert not kb[ids].any() and not vb[ids].any()
+        np.testing.assert_array_equal(kb[keep], k[keep])
+        np.testing.assert_array_equal(vb[keep], v[keep])
+    # zero bytes decode as +0.0 in bf16 and fp16
+    z = np.zeros(4, np.uint16)
+    assert (from_bits(z, torch.bfloat16) == 0).all() and (z.view(np.float16) == 0).all()
+    k, v = _pools(6)
+    _, _, st = oracle.zero_blocks(k, v, [3, 12], check=False)
+    assert st != 0
+
+
+def test_beam_fork_copy_on_write_scenario():
+    # Two beams share blocks [a, b]; b holds 2 of its 4 slots.  Beam 1 writes
+    # its next token: b is shared, so b is copied to a new block c, beam 1's
+    # table is remapped to [a, c], and the token goes to c ("How vLLM Works
+    # Internally", Copy-on-Write for Beam Search, steps 1-5).
+    rng = np.random.default_rng(8)
+    bs, hkv, hq, d, nb = 4, 1, 2, 8, 6
+    k = from_bits(rng.integers(0, 2**16, size=(nb, bs, hkv, d)).astype(np.uint16) & 0x3FFF,
+                  torch.bfloat16)
+    v = from_bits(rng.integers(0, 2**16, size=(nb, bs, hkv, d)).astype(np.uint16) & 0x3FFF,
+                  torch.bfloat16)
+    a, b, c = 2, 4, 1
+    shared = np.array([[a, b], [a, b]], np.int32)
+    q = torch.randn(1, hq, d).to(torch.bfloat16).repeat(2, 1, 1)   # both beams ask the same
+    # before the fork both beams see the same 6 tokens
+    before = oracle.attention(q, k, v, shared, [0, 1, 2], [6, 6], hq, hkv, d, bs, nb, 0.3,
+                              "bf16")
+    np.testing.assert_array_equal(before[0], before[1])
+    kb, vb, st = oracle.copy_blocks(k, v, [b], [c])
+    assert st == 0
+    kc = from_bits(kb.view(np.uint16).reshape(k.shape), torch.bfloat16)
+    vc = from_bits(vb.view(np.uint16).reshape(v.shape), torch.bfloat16)
+    forked = np.array([[a, b], [a, c]], np.int32)
+    # the copy changes nothing either beam sees
+    after = oracle.attention(q, kc, vc, forked, [0, 1, 2], [6, 6], hq, hkv, d, bs, nb, 0.3,
+                             "bf16")
+    np.testing.assert_array_equal(after, before)
+    # beam 1's new token lands in c (slot c*bs + 2) and beam 0 does not see it
+    newk = torch.randn(1, hkv, d).to(torch.bfloat16) * 4
+    newv = torch.randn(1, hkv, d).to(torch.bfloat16) * 4
+    k2, v2, _ = oracle.cache_write(newk, newv, kc, vc, [c * bs + 2], hkv, d, bs, nb)
+    k2, v2 = from_bits(k2, torch.bfloat16), from_bits(v2, torch.bfloat16)
+    grown = oracle.attention(q, k2, v2, forked, [0, 1, 2], [6, 7], hq, hkv, d, bs, nb, 0.3,
+                             "bf16")
+    np.testing.assert_array_equal(grown[0], before[0])
+    assert not np.array_equal(grown[1], before[1])
+    # and beam 1 over [a, c] equals dense attention over its 7 tokens
+    keys = torch.cat([k2[a], k2[c][:3]]).double().numpy()
+    vals = torch.cat([v2[a], v2[c][:3]]).double().numpy()
+    for h in range(hq):
+        sc = 0.3 * keys[:, 0, :] @ q[1, h].double().numpy()
+        w = np.exp(sc - sc.max())
+        np.testing.assert_allclose(grown[1, h], (w / w.sum()) @ vals[:, 0, :], atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # Cache write
 # ---------------------------------------------------------------------------
 

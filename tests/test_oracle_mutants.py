@@ -45,6 +45,12 @@ MUTANTS = {
                                    "logits_indices[row++] = query_start_loc[r] + k;"),
     "spec_drafts_ignored": ("int32_t d = num_draft_tokens ? num_draft_tokens[r] : 0;",
                             "int32_t d = 0;"),
+    "copy_k_into_v": (
+        "value_cache[(int64_t)d * block_bytes + b] = value_cache[(int64_t)s * block_bytes + b];",
+        "value_cache[(int64_t)d * block_bytes + b] = key_cache[(int64_t)s * block_bytes + b];"),
+    "copy_half_block": ("        for (int64_t b = 0; b < block_bytes; ++b) {\n            key_cache[(int64_t)d",
+                        "        for (int64_t b = 0; b < block_bytes / 2; ++b) {\n            key_cache[(int64_t)d"),
+    "zero_k_only": ("            value_cache[(int64_t)blk * block_bytes + b] = 0;\n", ""),
     "gather_wrong_offset": ("int64_t slot = (int64_t)phys * jb->block_size + j % jb->block_size;",
                             "int64_t slot = (int64_t)phys * jb->block_size + j / jb->block_size;"),
 }
