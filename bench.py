@@ -594,6 +594,32 @@ def run_ours(args):
         if roofline is None:
             roofline = roofline_prefill
 
+    # ---- whole-block operations on this workload's pools (run last: they
+    # overwrite blocks): copy-on-write copies and new-block zeroing of up to
+    # 4096 blocks, timed alone; algorithmic bytes = read + written.
+    block_ops = None
+    n_ops = min(4096, w.num_blocks // 2)
+    if n_ops > 0:
+        perm = np.random.default_rng(77 + rank).permutation(w.num_blocks).astype(np.int32)
+        src_b, dst_b = up(perm[:n_ops]), up(perm[n_ops:2 * n_ops])
+        block_bytes = w.block_size * w.num_kv_heads * w.head_dim * kc.element_size()
+        copy_us = time_calls(lambda: pa.pa_copy_blocks(kc, vc, src_b, dst_b), args.steps)
+        zero_us = time_calls(lambda: pa.pa_zero_blocks(kc, vc, dst_b), args.steps)
+        copy_bytes = 2 * 2 * n_ops * block_bytes
+        zero_bytes = 2 * n_ops * block_bytes
+        block_ops = {
+            "blocks": n_ops, "block_bytes": block_bytes,
+            "copy_blocks": {"us": copy_us, "bytes": copy_bytes,
+                            "GBps": copy_bytes / copy_us / 1e3,
+                            "frac": copy_bytes / copy_us / 1e3 / hbm_peak},
+            "zero_blocks": {"us": zero_us, "bytes": zero_bytes,
+                            "GBps": zero_bytes / zero_us / 1e3,
+                            "frac": zero_bytes / zero_us / 1e3 / hbm_peak},
+            "peak": hbm_peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"}
+        status, detail = pa.pa_get_status()
+        if status != pa.PA_OK:
+            raise RuntimeError(f"device checks failed in block ops: {pa.check_bits(detail)}")
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, threads, desc = oracle_sample(w, host_values(vals), args.cpu_seconds)
@@ -619,6 +645,7 @@ def run_ours(args):
             "clocks": clocks.summary(),
             "attn_us_per_step": float(np.mean(attn_ms)) * 1e3,
             "prep_us": prep_us,
+            "block_ops": block_ops,
             "launch": ("cuda_graph: the three calls captured once, one replay per step"
                        if graph_ms is not None else f"eager (graph capture failed: {graph_error})"),
             "eager": {"ms_per_step": eager_ms, "value": all_tokens / (eager_ms / 1e3),

@@ -11,6 +11,8 @@
  *                      token_indices), the discard mask and the sampled rows
  *                      of speculative decoding;
  *   pa_cache_write     each new token's K and V copied to its cache slot;
+ *   pa_copy_blocks / pa_zero_blocks  whole-block copy-on-write copies and
+ *                      the zeroing of newly allocated blocks;
  *   pa_attention       causal grouped-query attention of every token over
  *                      its own request's context, read through the block
  *                      table.
@@ -222,6 +224,45 @@ pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_st
                          const int32_t *slot_mapping, int32_t num_tokens,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                          int32_t num_blocks, pa_dtype dtype, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write: make whole cache blocks copies of others.
+ *
+ * Defined by "How vLLM Works Internally", section "Copy-on-Write for Beam
+ * Search", step 3 (the old block's contents are copied to the newly
+ * allocated block).  Steps 1, 2, 4 and 5 (reference counts, allocation, the
+ * block-table update) are the block manager's, on the host.
+ *   for i in [0, num_pairs): block dst_blocks[i] of the K pool and of the V
+ *   pool becomes a byte copy of block src_blocks[i] of the same pool
+ *   (block_size * num_kv_heads * head_dim elements each).
+ * The destinations must be distinct and none may be a source (they are new
+ * blocks); otherwise the contents of the overlapping blocks are unspecified
+ * (every access still stays inside the pools).
+ *
+ * Arguments: key_cache, value_cache device pools as in pa_cache_write
+ * (16-byte aligned); src_blocks, dst_blocks device int32 [num_pairs].
+ * Errors: PA_ERR_INVALID for negative sizes, NULL buffers with num_pairs > 0,
+ * unaligned pools or a bad dtype; PA_ERR_UNSUPPORTED when a block is not a
+ * multiple of 16 bytes.  Data check: PA_CHECK_BLOCK_ID (that pair skipped).
+ */
+pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_blocks,
+                         const int32_t *dst_blocks, int32_t num_pairs, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                         pa_dtype dtype, pa_stream_t stream);
+
+/*
+ * pa_zero_blocks -- clear newly allocated cache blocks.
+ *
+ * Defined by "Inside vLLM: Following One Request", the scheduler output's
+ * new_block_ids_to_zero: blocks that must be cleared before the forward pass
+ * so that stale data or NaNs of an earlier owner cannot reach attention.
+ *   every byte of block block_ids[i] of both pools becomes 0 (+0.0).
+ * Arguments and errors as pa_copy_blocks; block_ids device int32 [num_ids].
+ */
+pa_status pa_zero_blocks(void *key_cache, void *value_cache, const int32_t *block_ids,
+                         int32_t num_ids, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t num_blocks, pa_dtype dtype,
+                         pa_stream_t stream);
 
 /*
  * pa_attention_workspace_size -- bytes of workspace that let pa_attention

@@ -7,8 +7,9 @@ CUDA kernels; there is no CPU or PyTorch fallback, and using the package
 without the built library raises immediately.
 
 Functions carry the C names: ``pa_prepare_inputs``, ``pa_prepare_inputs_ex``,
-``pa_cache_write``, ``pa_attention_workspace_size``, ``pa_attention``,
-``pa_attention_noalloc``, ``pa_get_status``, ``pa_launch_count``.
+``pa_cache_write``, ``pa_copy_blocks``, ``pa_zero_blocks``,
+``pa_attention_workspace_size``, ``pa_attention``, ``pa_attention_noalloc``,
+``pa_get_status``, ``pa_launch_count``.
 """
 
 from __future__ import annotations
@@ -67,6 +68,10 @@ def lib():
             L.pa_prepare_inputs_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
                                                vp, vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp,
                                                vp, vp, vp]
+            for fn in (L.pa_copy_blocks, L.pa_zero_blocks):
+                fn.restype = ctypes.c_int
+            L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp]
+            L.pa_zero_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp]
             L.pa_cache_write.restype = ctypes.c_int
             L.pa_cache_write.argtypes = [vp, vp, i64, vp, vp, vp, i32, i32, i32, i32, i32,
                                          ctypes.c_int, vp]
@@ -203,6 +208,38 @@ def pa_cache_write(key, value, key_cache, value_cache, slot_mapping, num_blocks=
         _dev(value_cache, "value_cache"), _dev(slot_mapping, "slot_mapping", torch.int32), T,
         hkv, d, bs, nb if num_blocks is None else int(num_blocks), dt, _stream(stream))
     _check(rc, "pa_cache_write")
+
+
+def _pools(key_cache, value_cache):
+    if key_cache.shape != value_cache.shape or key_cache.dim() != 4:
+        raise ValueError("key/value caches must both be [NB, bs, Hkv, D]")
+    dt = _DTYPES.get(key_cache.dtype)
+    if dt is None or value_cache.dtype != key_cache.dtype:
+        raise TypeError("caches must share a bf16/fp16 dtype")
+    nb, bs, hkv, d = key_cache.shape
+    return nb, bs, hkv, d, dt
+
+
+def pa_copy_blocks(key_cache, value_cache, src_blocks, dst_blocks, stream=None):
+    """Copy-on-write: block dst_blocks[i] of both pools becomes a copy of
+    block src_blocks[i] (int32 CUDA tensors of equal length)."""
+    nb, bs, hkv, d, dt = _pools(key_cache, value_cache)
+    if src_blocks.shape != dst_blocks.shape or src_blocks.dim() != 1:
+        raise ValueError("src_blocks and dst_blocks must be 1-D of equal length")
+    rc = lib().pa_copy_blocks(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+                              _dev(src_blocks, "src_blocks", torch.int32),
+                              _dev(dst_blocks, "dst_blocks", torch.int32), src_blocks.shape[0],
+                              bs, hkv, d, nb, dt, _stream(stream))
+    _check(rc, "pa_copy_blocks")
+
+
+def pa_zero_blocks(key_cache, value_cache, block_ids, stream=None):
+    """Zero every byte of the listed blocks in both pools."""
+    nb, bs, hkv, d, dt = _pools(key_cache, value_cache)
+    rc = lib().pa_zero_blocks(_dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+                              _dev(block_ids, "block_ids", torch.int32), block_ids.shape[0], bs,
+                              hkv, d, nb, dt, _stream(stream))
+    _check(rc, "pa_zero_blocks")
 
 
 def pa_attention_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len, num_q_heads,

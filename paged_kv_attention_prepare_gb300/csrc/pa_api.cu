@@ -216,6 +216,43 @@ pa_status pa_prepare_inputs_ex(const int32_t *num_scheduled_tokens,
     return launch_prepare(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+static pa_status check_block_op(void *kc, void *vc, const void *a, const void *b, int32_t n,
+                                int32_t bs, int32_t hkv, int32_t d, int32_t nb, pa_dtype dtype,
+                                int64_t *block_bytes) {
+    if (n < 0 || bs <= 0 || hkv <= 0 || d <= 0 || nb < 0 || (dtype != PA_BF16 && dtype != PA_FP16))
+        return PA_ERR_INVALID;
+    if (n > 0 && (!kc || !vc || !a || !b)) return PA_ERR_INVALID;
+    if (n > 0 && (!aligned(kc, 16) || !aligned(vc, 16))) return PA_ERR_INVALID;
+    const int64_t bb = (int64_t)bs * hkv * d * 2;
+    if (bb % 16 != 0) return PA_ERR_UNSUPPORTED;
+    *block_bytes = bb;
+    return PA_OK;
+}
+
+pa_status pa_copy_blocks(void *key_cache, void *value_cache, const int32_t *src_blocks,
+                         const int32_t *dst_blocks, int32_t num_pairs, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                         pa_dtype dtype, pa_stream_t stream) {
+    int64_t bb = 0;
+    const pa_status st = check_block_op(key_cache, value_cache, src_blocks, dst_blocks, num_pairs,
+                                        block_size, num_kv_heads, head_dim, num_blocks, dtype, &bb);
+    if (st != PA_OK) return st;
+    return launch_copy_blocks(key_cache, value_cache, bb, num_blocks, src_blocks, dst_blocks,
+                              num_pairs, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_zero_blocks(void *key_cache, void *value_cache, const int32_t *block_ids,
+                         int32_t num_ids, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t num_blocks, pa_dtype dtype,
+                         pa_stream_t stream) {
+    int64_t bb = 0;
+    const pa_status st = check_block_op(key_cache, value_cache, block_ids, block_ids, num_ids,
+                                        block_size, num_kv_heads, head_dim, num_blocks, dtype, &bb);
+    if (st != PA_OK) return st;
+    return launch_zero_blocks(key_cache, value_cache, bb, num_blocks, block_ids, num_ids,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
 pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_stride,
                          void *key_cache, void *value_cache, const int32_t *slot_mapping,
                          int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,

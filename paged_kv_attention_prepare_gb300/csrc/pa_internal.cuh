@@ -45,6 +45,12 @@ struct PrepArgs {
 
 pa_status launch_prepare(const PrepArgs &a, cudaStream_t stream);
 
+pa_status launch_copy_blocks(void *kc, void *vc, int64_t block_bytes, int32_t num_blocks,
+                             const int32_t *src, const int32_t *dst, int32_t n,
+                             cudaStream_t stream);
+pa_status launch_zero_blocks(void *kc, void *vc, int64_t block_bytes, int32_t num_blocks,
+                             const int32_t *ids, int32_t n, cudaStream_t stream);
+
 pa_status launch_cache_write(const void *key, const void *value, int64_t stride_elems,
                              void *kc, void *vc, const int32_t *slots, int32_t T,
                              int32_t row_elems, int64_t num_slots, cudaStream_t stream);

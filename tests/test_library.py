@@ -109,6 +109,24 @@ def test_prepare_ex_rejects_half_given_groups(case):
     assert rc == pa.PA_ERR_INVALID
 
 
+@pytest.mark.parametrize("fn", ["copy", "zero"])
+def test_block_ops_reject_bad_arguments(fn):
+    L = pa.lib()
+    unaligned = ctypes.c_void_p(0x100008)
+
+    def call(kc=FAKE, n=3, bs=16, hkv=8, d=128, dtype=pa.PA_BF16, ids=FAKE):
+        if fn == "copy":
+            return L.pa_copy_blocks(kc, FAKE, ids, FAKE, n, bs, hkv, d, 64, dtype, None)
+        return L.pa_zero_blocks(kc, FAKE, ids, n, bs, hkv, d, 64, dtype, None)
+
+    assert call(n=-1) == pa.PA_ERR_INVALID
+    assert call(ids=None) == pa.PA_ERR_INVALID
+    assert call(kc=unaligned) == pa.PA_ERR_INVALID
+    assert call(dtype=9) == pa.PA_ERR_INVALID
+    assert call(bs=1, hkv=1, d=3) == pa.PA_ERR_UNSUPPORTED   # 16-byte blocks only
+    assert call(n=0, ids=None) == pa.PA_OK                   # nothing to do, nothing launched
+
+
 def test_cache_write_rejects_short_stride_and_bad_dtype():
     L = pa.lib()
     assert L.pa_cache_write(FAKE, FAKE, 100, FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, pa.PA_BF16,
