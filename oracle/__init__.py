@@ -24,6 +24,15 @@ Parity status of each function (how it is pinned, in ``tests/test_oracle.py``):
   (after a copy and a table remap, the diverging beam attends over exactly
   what it attended over before, and its new token no longer reaches the
   other beam).
+* ``e4m3_decode`` / ``e4m3_encode`` -- pinned by PyTorch's float8_e4m3fn
+  conversions (every code; random values inside the finite range), closed
+  forms (448, 2^-6, 2^-9, 1), round trips of every finite code, ties to even
+  and saturation.
+* ``cache_write_fp8`` -- pinned by PyTorch's fp32 division and float8 rounding
+  of the same elements and untouched-slot preservation.
+* ``attention(kv_cache_dtype="fp8_e4m3")`` -- pinned by equality with
+  attention over 16-bit pools holding the same values (power-of-two scales
+  keep them exact).
 * ``cache_write`` -- pinned by bit equality against a direct per-slot copy,
   untouched-slot preservation and write-then-gather round trips.
 * ``attention`` -- pinned by closed forms (one visible key, K = 0, constant V,
@@ -110,6 +119,23 @@ def _load():
                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                 ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int32,
                 ctypes.POINTER(ctypes.c_double), i32p, ctypes.c_int32, ctypes.c_int32]
+            lib.oracle_attention_ex.restype = ctypes.c_int
+            lib.oracle_attention_ex.argtypes = [
+                u16p, u16p, u16p, i32p, ctypes.c_int32, i32p, i32p, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_double, ctypes.c_double,
+                ctypes.POINTER(ctypes.c_double), i32p, ctypes.c_int32, ctypes.c_int32]
+            lib.oracle_cache_write_fp8.restype = ctypes.c_int
+            lib.oracle_cache_write_fp8.argtypes = [
+                u16p, u16p, ctypes.c_int64, u16p, u16p, i32p, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_float, ctypes.c_float]
+            lib.oracle_e4m3_decode.restype = ctypes.c_int
+            lib.oracle_e4m3_decode.argtypes = [u16p, ctypes.c_int64,
+                                               ctypes.POINTER(ctypes.c_double)]
+            lib.oracle_e4m3_encode.restype = ctypes.c_int
+            lib.oracle_e4m3_encode.argtypes = [u16p, ctypes.c_int64, u16p]
             lib.oracle_num_cpus.restype = ctypes.c_int
             lib.oracle_num_cpus.argtypes = []
             _lib = lib
@@ -133,6 +159,32 @@ def _bits(a) -> np.ndarray:
     import torch  # local: torch only as a carrier of bf16 bit patterns
     t = a.detach().to("cpu").contiguous()
     return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _bytes8(a) -> np.ndarray:
+    """Byte patterns of an FP8 pool (torch uint8 / float8 tensor or NumPy)."""
+    if isinstance(a, np.ndarray):
+        return np.ascontiguousarray(a).view(np.uint8)
+    import torch  # local: torch only as a carrier of the pool's bytes
+    return a.detach().to("cpu").contiguous().view(torch.uint8).numpy()
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Exact values (float64) of E4M3 byte codes."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e4m3_decode(c.ctypes.data, c.size,
+                               out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 byte codes of float32 values (nearest, ties to even, +-448
+    saturation)."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty(f.shape, np.uint8)
+    _load().oracle_e4m3_encode(f.ctypes.data, f.size, out.ctypes.data)
+    return out
 
 
 def num_cpus() -> int:
@@ -283,24 +335,53 @@ def cache_write(key, value, key_cache, value_cache, slot_mapping, num_kv_heads, 
     return kcb, vcb, int(rc)
 
 
+def cache_write_fp8(key, value, key_cache, value_cache, slot_mapping, num_kv_heads, head_dim,
+                    block_size, num_blocks, dtype, k_scale, v_scale, kv_token_stride=None,
+                    check=True):
+    """The write into FP8 pools: returns (key bytes, value bytes, status),
+    uint8 arrays shaped like the input pools."""
+    lib = _load()
+    kb, vb = _bits(key), _bits(value)
+    stride = num_kv_heads * head_dim if kv_token_stride is None else int(kv_token_stride)
+    kcb = _bytes8(key_cache).copy()
+    vcb = _bytes8(value_cache).copy()
+    slots = _i32(slot_mapping)
+    rc = lib.oracle_cache_write_fp8(kb.ctypes.data, vb.ctypes.data, stride, kcb.ctypes.data,
+                                    vcb.ctypes.data, _p32(slots), slots.shape[0],
+                                    int(num_kv_heads), int(head_dim), int(block_size),
+                                    int(num_blocks), DTYPES[dtype], float(k_scale),
+                                    float(v_scale))
+    if check and rc != 0:
+        raise OracleError(f"oracle_cache_write_fp8 rejected the inputs ({rc})")
+    return kcb, vcb, int(rc)
+
+
 def attention(q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
               num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
-              tokens=None, num_threads=0):
+              tokens=None, num_threads=0, kv_cache_dtype="auto", k_scale=1.0, v_scale=1.0):
     """fp64 attention output [T, Hq, D].  With ``tokens`` (ascending flat token
-    indices) only those rows are computed; the others are NaN."""
+    indices) only those rows are computed; the others are NaN.  With
+    ``kv_cache_dtype="fp8_e4m3"`` the pools hold E4M3 bytes and the cached
+    values are element * k_scale / * v_scale."""
     lib = _load()
     qb = _bits(q)
-    kcb, vcb = _bits(key_cache), _bits(value_cache)
+    fp8 = kv_cache_dtype == "fp8_e4m3"
+    if fp8:
+        kcb, vcb = _bytes8(key_cache), _bytes8(value_cache)
+        cdt = 2
+    else:
+        kcb, vcb = _bits(key_cache), _bits(value_cache)
+        cdt = DTYPES[dtype]
     qsl, sl = _i32(query_start_loc), _i32(seq_lens)
     r = sl.shape[0]
     bt = _i32(block_table).reshape(r, -1) if r else _i32(block_table).reshape(0, 1)
     t = int(qsl[r]) if r else 0
     out = np.full((t, num_q_heads, head_dim), np.nan, np.float64)
     sel = None if tokens is None else _i32(np.sort(np.asarray(tokens)))
-    rc = lib.oracle_attention(
+    rc = lib.oracle_attention_ex(
         qb.ctypes.data, kcb.ctypes.data, vcb.ctypes.data, _p32(bt), bt.shape[1], _p32(qsl),
         _p32(sl), r, t, int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
-        int(num_blocks), float(scale), DTYPES[dtype],
+        int(num_blocks), float(scale), DTYPES[dtype], cdt, float(k_scale), float(v_scale),
         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
         None if sel is None else _p32(sel), 0 if sel is None else sel.shape[0],
         int(num_threads))
@@ -314,10 +395,19 @@ def step(w, vals, qsl_capacity=None, tokens=None, num_threads=0):
     write, attention.  Returns (indices dict, key_cache', value_cache', out)."""
     idx = prepare_inputs(w.num_scheduled_tokens, w.num_computed_tokens, w.block_table,
                          w.block_size, w.num_tokens, w.num_blocks, qsl_capacity)
-    kc, vc, _ = cache_write(vals["key"], vals["value"], vals["key_cache"],
-                            vals["value_cache"], idx["slot_mapping"], w.num_kv_heads,
-                            w.head_dim, w.block_size, w.num_blocks)
+    fp8 = getattr(w, "kv_cache_dtype", "auto") == "fp8_e4m3"
+    if fp8:
+        kc, vc, _ = cache_write_fp8(vals["key"], vals["value"], vals["key_cache"],
+                                    vals["value_cache"], idx["slot_mapping"], w.num_kv_heads,
+                                    w.head_dim, w.block_size, w.num_blocks, w.dtype,
+                                    w.k_scale, w.v_scale)
+    else:
+        kc, vc, _ = cache_write(vals["key"], vals["value"], vals["key_cache"],
+                                vals["value_cache"], idx["slot_mapping"], w.num_kv_heads,
+                                w.head_dim, w.block_size, w.num_blocks)
     out = attention(vals["q"], kc, vc, w.block_table, idx["query_start_loc"][: w.num_reqs + 1],
                     idx["seq_lens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
-                    w.block_size, w.num_blocks, w.scale, w.dtype, tokens, num_threads)
+                    w.block_size, w.num_blocks, w.scale, w.dtype, tokens, num_threads,
+                    kv_cache_dtype="fp8_e4m3" if fp8 else "auto",
+                    k_scale=getattr(w, "k_scale", 1.0), v_scale=getattr(w, "v_scale", 1.0))
     return idx, kc, vc, out

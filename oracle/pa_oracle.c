@@ -6,7 +6,7 @@
  * this library; the CUDA library never links, includes or calls it, and it
  * shares no code with the CUDA library.  Floating point is fp64 throughout.
  *
- * Eight functions, each citing the passage it follows:
+ * The functions, each citing the passage it follows:
  *
  *   oracle_prepare_inputs  -- the per-step index tensors
  *       ("Building the Batch", sections "How they are computed" and
@@ -38,6 +38,17 @@
  *        scheduler output's new_block_ids_to_zero: freshly allocated blocks
  *        are cleared before the forward pass.  Every byte of the block, in
  *        both pools, becomes 0.
+ *   oracle_e4m3_decode / oracle_e4m3_encode -- the FP8 E4M3 format
+ *        ("How vLLM Works Internally", section "FP8 KV Cache": the cache may
+ *        hold FP8 instead of FP16), written from the format's definition:
+ *        decode exactly; encode by round to nearest, ties to even, with
+ *        saturation to +-448.
+ *   oracle_cache_write_fp8 -- the write op with kv_cache_dtype FP8 ("Inside
+ *        vLLM: Following One Request", reshape_and_cache_flash's
+ *        kv_cache_dtype, k_scale, v_scale): element / scale in single
+ *        precision, then E4M3.
+ *   oracle_attention_ex    -- oracle_attention over pools of any element
+ *        type: the cached value is pool element * k_scale (or v_scale).
  *   oracle_cache_write     -- "Inside vLLM: Following One Request", section
  *        on reshape_and_cache_flash: token i's K and V are copied to slot
  *        slot_mapping[i].  A bit copy.
@@ -57,6 +68,8 @@
  *     (slot * Hkv + h) * D + d.
  *   - a negative slot means "no write" for that token.
  *   - a request must schedule at least one token.
+ *   - FP8 cache: E4M3 with one scale per pool (k_scale, v_scale); the write
+ *     stores round(x / scale) and a read returns element * scale.
  *
  * Return value: 0 on success, a negative number when an input breaks the
  * problem's rules (the outputs for the offending items are then unspecified).
@@ -71,6 +84,7 @@
 
 #define ORACLE_BF16 0
 #define ORACLE_FP16 1
+#define ORACLE_FP8_E4M3 2
 
 /* ------------------------------------------------------------------------ */
 /* Element decoding: the raw 16-bit patterns of bf16 / IEEE half to double.  */
@@ -103,6 +117,75 @@ static double fp16_to_double(uint16_t h)
 static double elem(uint16_t x, int dtype)
 {
     return dtype == ORACLE_FP16 ? fp16_to_double(x) : bf16_to_double(x);
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 (the OCP "fn" variant: 1 sign, 4 exponent bits with bias 7, 3    */
+/* mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448).     */
+/* ------------------------------------------------------------------------ */
+
+static double e4m3_to_double(uint8_t b)
+{
+    int sign = b >> 7;
+    int expo = (b >> 3) & 0xf;
+    int mant = b & 7;
+    double v;
+    if (expo == 15 && mant == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)mant, -9);                  /* 2^-6 * m/8 */
+    else
+        v = ldexp((double)(8 + mant), expo - 10);     /* 2^(e-7) * (1 + m/8) */
+    return sign ? -v : v;
+}
+
+/* Round a float to the nearest E4M3 value, ties to the even mantissa;
+ * magnitudes past the largest finite value give +-448 (saturation), NaN gives
+ * the NaN code. */
+static uint8_t float_to_e4m3(float x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7e;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; 8 * 2^-9 is the first normal */
+        double units = nearbyint(a * 512.0);
+        return sign | (uint8_t)units;
+    }
+    int e2;
+    frexp(a, &e2);                  /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;                 /* a in [2^e, 2^(e+1)) */
+    double steps = nearbyint(ldexp(a, 3 - e));     /* in [8, 16] */
+    if (steps == 16.0) {
+        steps = 8.0;
+        e += 1;
+    }
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)steps - 8));
+}
+
+/* Pool element `i` of a cache in `cache_dtype` (bf16, fp16, or fp8 e4m3). */
+static double cache_elem(const void *pool, int64_t i, int cache_dtype)
+{
+    if (cache_dtype == ORACLE_FP8_E4M3)
+        return e4m3_to_double(((const uint8_t *)pool)[i]);
+    return elem(((const uint16_t *)pool)[i], cache_dtype);
+}
+
+int oracle_e4m3_decode(const uint8_t *codes, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_to_double(codes[i]);
+    return 0;
+}
+
+int oracle_e4m3_encode(const float *x, int64_t n, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = float_to_e4m3(x[i]);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -332,6 +415,42 @@ int oracle_cache_write(const uint16_t *key, const uint16_t *value,
     return err;
 }
 
+/* The write into an FP8 cache ("Inside vLLM: Following One Request", the
+ * write op's kv_cache_dtype, k_scale and v_scale arguments): each element of
+ * the new key is divided by k_scale in single precision and rounded to E4M3
+ * (values of V likewise with v_scale).  src_dtype is the type of key/value. */
+int oracle_cache_write_fp8(const uint16_t *key, const uint16_t *value,
+                           int64_t kv_token_stride, uint8_t *key_cache,
+                           uint8_t *value_cache, const int32_t *slot_mapping,
+                           int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, int32_t src_dtype,
+                           float k_scale, float v_scale)
+{
+    int err = 0;
+    int64_t num_slots = (int64_t)num_blocks * block_size;
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f))
+        return -1;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots) {
+            err = -8;
+            continue;
+        }
+        for (int32_t h = 0; h < num_kv_heads; ++h)
+            for (int32_t d = 0; d < head_dim; ++d) {
+                int64_t src = (int64_t)t * kv_token_stride + (int64_t)h * head_dim + d;
+                int64_t dst = (slot * num_kv_heads + h) * head_dim + d;
+                float kq = (float)elem(key[src], src_dtype) / k_scale;
+                float vq = (float)elem(value[src], src_dtype) / v_scale;
+                key_cache[dst] = float_to_e4m3(kq);
+                value_cache[dst] = float_to_e4m3(vq);
+            }
+    }
+    return err;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Attention                                                                 */
 /* ------------------------------------------------------------------------ */
@@ -344,10 +463,13 @@ typedef struct {
 } work_item;
 
 typedef struct {
-    const uint16_t *q, *key_cache, *value_cache;
+    const uint16_t *q;
+    const void *key_cache, *value_cache;
     const int32_t *block_table, *query_start_loc, *seq_lens;
     int32_t max_blocks_per_req, num_q_heads, num_kv_heads, head_dim, block_size;
-    int32_t dtype;
+    int32_t dtype;                /* q */
+    int32_t cache_dtype;          /* K/V pools */
+    double k_scale, v_scale;      /* pool element * scale = the cached value */
     double scale;
     double *out;
     const int32_t *sel;           /* selected tokens, ascending */
@@ -381,8 +503,8 @@ static void run_item(const attn_job *jb, const work_item *it, double *kc, double
         int64_t slot = (int64_t)phys * jb->block_size + j % jb->block_size;
         for (int32_t d = 0; d < D; ++d) {
             int64_t a = (slot * Hkv + g) * D + d;
-            kc[(int64_t)j * D + d] = elem(jb->key_cache[a], jb->dtype);
-            vc[(int64_t)j * D + d] = elem(jb->value_cache[a], jb->dtype);
+            kc[(int64_t)j * D + d] = cache_elem(jb->key_cache, a, jb->cache_dtype) * jb->k_scale;
+            vc[(int64_t)j * D + d] = cache_elem(jb->value_cache, a, jb->cache_dtype) * jb->v_scale;
         }
     }
 
@@ -462,14 +584,15 @@ int oracle_num_cpus(void)
  * at most `chunk` tokens per (request, kv head) so that the threads share a
  * long prefill.
  */
-int oracle_attention(const uint16_t *q, const uint16_t *key_cache,
-                     const uint16_t *value_cache, const int32_t *block_table,
-                     int32_t max_blocks_per_req, const int32_t *query_start_loc,
-                     const int32_t *seq_lens, int32_t num_reqs, int32_t num_tokens,
-                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                     int32_t block_size, int32_t num_blocks, double scale,
-                     int32_t dtype, double *out, const int32_t *tokens,
-                     int32_t num_selected, int32_t num_threads)
+int oracle_attention_ex(const uint16_t *q, const void *key_cache,
+                        const void *value_cache, const int32_t *block_table,
+                        int32_t max_blocks_per_req, const int32_t *query_start_loc,
+                        const int32_t *seq_lens, int32_t num_reqs, int32_t num_tokens,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int32_t num_blocks, double scale,
+                        int32_t dtype, int32_t cache_dtype, double k_scale, double v_scale,
+                        double *out, const int32_t *tokens, int32_t num_selected,
+                        int32_t num_threads)
 {
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads || head_dim <= 0 || block_size <= 0)
         return -1;
@@ -542,7 +665,7 @@ int oracle_attention(const uint16_t *q, const uint16_t *key_cache,
 
     attn_job jb = {q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
                    max_blocks_per_req, num_q_heads, num_kv_heads, head_dim, block_size,
-                   dtype, scale, out, sel, items, n_items, 0, 0};
+                   dtype, cache_dtype, k_scale, v_scale, scale, out, sel, items, n_items, 0, 0};
     int nt = num_threads > 0 ? num_threads : oracle_num_cpus();
     if (nt > n_items)
         nt = n_items > 0 ? (int)n_items : 1;
@@ -560,4 +683,20 @@ int oracle_attention(const uint16_t *q, const uint16_t *key_cache,
     free(sel);
     free(sel_req);
     return jb.failed ? -6 : 0;
+}
+
+/* Attention over 16-bit pools of the same type as q (scales 1). */
+int oracle_attention(const uint16_t *q, const uint16_t *key_cache,
+                     const uint16_t *value_cache, const int32_t *block_table,
+                     int32_t max_blocks_per_req, const int32_t *query_start_loc,
+                     const int32_t *seq_lens, int32_t num_reqs, int32_t num_tokens,
+                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                     int32_t block_size, int32_t num_blocks, double scale,
+                     int32_t dtype, double *out, const int32_t *tokens,
+                     int32_t num_selected, int32_t num_threads)
+{
+    return oracle_attention_ex(q, key_cache, value_cache, block_table, max_blocks_per_req,
+                               query_start_loc, seq_lens, num_reqs, num_tokens, num_q_heads,
+                               num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                               dtype, 1.0, 1.0, out, tokens, num_selected, num_threads);
 }

@@ -435,6 +435,112 @@ def test_beam_fork_copy_on_write_scenario():
 
 
 # ---------------------------------------------------------------------------
+# FP8 (E4M3) cache
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3(codes):
+    return torch.from_numpy(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn)
+
+
+def test_e4m3_decode_every_code_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    want = _torch_e4m3(codes).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert nan.tolist() == np.isnan(got).tolist() and nan.sum() == 2     # 0x7f, 0xff
+    np.testing.assert_array_equal(got[~nan], want[~nan])
+    np.testing.assert_array_equal(np.signbit(got[~nan]), codes[~nan] >= 0x80)
+
+
+def test_e4m3_closed_forms():
+    got = oracle.e4m3_decode([0x7E, 0x08, 0x07, 0x01, 0x38, 0xC0, 0x00, 0x77])
+    assert got.tolist() == [448.0, 2.0 ** -6, 7 * 2.0 ** -9, 2.0 ** -9, 1.0, -2.0, 0.0, 240.0]
+
+
+def test_e4m3_round_trip_every_finite_code():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    np.testing.assert_array_equal(oracle.e4m3_encode(vals), codes)
+
+
+def test_e4m3_encode_matches_torch_inside_the_finite_range():
+    rng = np.random.default_rng(13)
+    mag = np.exp2(rng.uniform(-14, np.log2(463.9), size=200_000)).astype(np.float32)
+    x = np.where(rng.random(mag.size) < 0.5, -mag, mag).astype(np.float32)
+    # and every midpoint between neighbouring finite codes (the ties)
+    pos = np.sort(oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8)))
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, -mids, [0.0, -0.0]]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(x), want)
+
+
+def test_e4m3_ties_go_to_the_even_code():
+    pos = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)
+    got = oracle.e4m3_encode(mids)
+    assert np.all(got % 2 == 0)                     # even mantissa
+    assert np.all((got == np.arange(0, 0x7E)) | (got == np.arange(1, 0x7F)))
+
+
+def test_e4m3_encode_saturates_and_keeps_nan():
+    got = oracle.e4m3_encode([448.0, 463.99, 464.0, 1e30, np.inf, -500.0, -np.inf, np.nan])
+    assert got[:7].tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert got[7] & 0x7F == 0x7F
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_cache_write_fp8_matches_torch_division_and_rounding(dtype):
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    rng = np.random.default_rng(3)
+    t, hkv, d, bs, nb = 9, 2, 16, 4, 6
+    key = torch.randn(t, hkv, d).to(tdt)
+    value = (torch.randn(t, hkv, d) * 3).to(tdt)
+    slots = rng.permutation(nb * bs)[:t].astype(np.int32)
+    slots[4] = -1                                     # a padding row: no write
+    kc0 = rng.integers(0, 256, size=(nb, bs, hkv, d)).astype(np.uint8)
+    vc0 = rng.integers(0, 256, size=(nb, bs, hkv, d)).astype(np.uint8)
+    ks, vs = 0.0625, 0.3
+    kc, vc, st = oracle.cache_write_fp8(key, value, kc0, vc0, slots, hkv, d, bs, nb, dtype, ks,
+                                        vs)
+    assert st == 0
+    kq = (key.float() / torch.tensor(ks, dtype=torch.float32)).to(torch.float8_e4m3fn)
+    vq = (value.float() / torch.tensor(vs, dtype=torch.float32)).to(torch.float8_e4m3fn)
+    flat_k = kc.reshape(nb * bs, hkv, d)
+    flat_v = vc.reshape(nb * bs, hkv, d)
+    written = slots >= 0
+    np.testing.assert_array_equal(flat_k[slots[written]], kq.view(torch.uint8).numpy()[written])
+    np.testing.assert_array_equal(flat_v[slots[written]], vq.view(torch.uint8).numpy()[written])
+    untouched = np.setdiff1d(np.arange(nb * bs), slots[written])
+    np.testing.assert_array_equal(flat_k[untouched], kc0.reshape(nb * bs, hkv, d)[untouched])
+
+
+def test_attention_over_fp8_pools_equals_16_bit_pools_of_the_same_values():
+    rng = np.random.default_rng(17)
+    nb, bs, hkv, hq, d = 12, 4, 2, 4, 16
+    def pool():
+        x = torch.randn(nb, bs, hkv, d) * 12
+        return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    k8, v8 = pool(), pool()
+    ks, vs = 2.0 ** -4, 2.0 ** -3                     # powers of two: exact in bf16
+    kb = (_torch_e4m3(k8).float() * ks).to(torch.bfloat16)
+    vb = (_torch_e4m3(v8).float() * vs).to(torch.bfloat16)
+    assert torch.equal(kb.double(), torch.from_numpy(oracle.e4m3_decode(k8) * ks))
+    bt = rng.permutation(nb)[:9].astype(np.int32).reshape(3, 3)
+    nst, sl = [3, 1, 2], [9, 12, 5]
+    qsl = np.concatenate([[0], np.cumsum(nst)]).astype(np.int32)
+    q = torch.randn(6, hq, d).to(torch.bfloat16)
+    got = oracle.attention(q, k8, v8, bt, qsl, sl, hq, hkv, d, bs, nb, 0.25, "bf16",
+                           kv_cache_dtype="fp8_e4m3", k_scale=ks, v_scale=vs)
+    want = oracle.attention(q, kb, vb, bt, qsl, sl, hq, hkv, d, bs, nb, 0.25, "bf16")
+    np.testing.assert_array_equal(got, want)
+    # a scale on V scales the output; a scale on K acts like a softmax scale
+    got2 = oracle.attention(q, k8, v8, bt, qsl, sl, hq, hkv, d, bs, nb, 0.25 * ks, "bf16",
+                            kv_cache_dtype="fp8_e4m3", k_scale=1.0, v_scale=1.0)
+    np.testing.assert_allclose(got2 * vs, want, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
 # Cache write
 # ---------------------------------------------------------------------------
 

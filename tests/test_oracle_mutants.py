@@ -51,6 +51,16 @@ MUTANTS = {
     "copy_half_block": ("        for (int64_t b = 0; b < block_bytes; ++b) {\n            key_cache[(int64_t)d",
                         "        for (int64_t b = 0; b < block_bytes / 2; ++b) {\n            key_cache[(int64_t)d"),
     "zero_k_only": ("            value_cache[(int64_t)blk * block_bytes + b] = 0;\n", ""),
+    "e4m3_bias": ("ldexp((double)(8 + mant), expo - 10)", "ldexp((double)(8 + mant), expo - 11)"),
+    "e4m3_subnormal_scale": ("ldexp((double)mant, -9);", "ldexp((double)mant, -10);"),
+    "e4m3_no_saturation": ("if (a >= 448.0)\n        return sign | 0x7e;",
+                           "if (a >= 1e300)\n        return sign | 0x7e;"),
+    "e4m3_ties_away": ("double steps = nearbyint(ldexp(a, 3 - e));",
+                       "double steps = round(ldexp(a, 3 - e));"),
+    "fp8_write_multiplies": ("float kq = (float)elem(key[src], src_dtype) / k_scale;",
+                             "float kq = (float)elem(key[src], src_dtype) * k_scale;"),
+    "fp8_v_scale_ignored": ("cache_elem(jb->value_cache, a, jb->cache_dtype) * jb->v_scale;",
+                            "cache_elem(jb->value_cache, a, jb->cache_dtype);"),
     "gather_wrong_offset": ("int64_t slot = (int64_t)phys * jb->block_size + j % jb->block_size;",
                             "int64_t slot = (int64_t)phys * jb->block_size + j / jb->block_size;"),
 }

@@ -54,6 +54,9 @@ class Workload:
     head_dim: int
     dtype: str                        # "bf16" | "fp16"
     unique_blocks: int = 0            # distinct physical blocks referenced by the tables
+    kv_cache_dtype: str = "auto"      # "auto" (the q dtype) | "fp8_e4m3"
+    k_scale: float = 1.0              # FP8 pools: cached value = element * scale
+    v_scale: float = 1.0
 
     @property
     def num_reqs(self) -> int:
