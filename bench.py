@@ -276,9 +276,18 @@ def oracle_sample(w, vals_host, seconds: float):
     idx = oracle.prepare_inputs(w.num_scheduled_tokens, w.num_computed_tokens, w.block_table,
                                 w.block_size, w.num_tokens, w.num_blocks)
     t1 = time.perf_counter()
-    kc, vc, _ = oracle.cache_write(vals_host["key"], vals_host["value"], vals_host["key_cache"],
-                                   vals_host["value_cache"], idx["slot_mapping"], w.num_kv_heads,
-                                   w.head_dim, w.block_size, w.num_blocks)
+    fp8 = w.kv_cache_dtype == "fp8_e4m3"
+    if fp8:
+        kc, vc, _ = oracle.cache_write_fp8(vals_host["key"], vals_host["value"],
+                                           vals_host["key_cache"], vals_host["value_cache"],
+                                           idx["slot_mapping"], w.num_kv_heads, w.head_dim,
+                                           w.block_size, w.num_blocks, w.dtype, w.k_scale,
+                                           w.v_scale)
+    else:
+        kc, vc, _ = oracle.cache_write(vals_host["key"], vals_host["value"],
+                                       vals_host["key_cache"], vals_host["value_cache"],
+                                       idx["slot_mapping"], w.num_kv_heads, w.head_dim,
+                                       w.block_size, w.num_blocks)
     t2 = time.perf_counter()
     rng = np.random.default_rng(0)
     n, spent, done = max(1, nthreads), 0.0, 0
@@ -289,7 +298,8 @@ def oracle_sample(w, vals_host, seconds: float):
         oracle.attention(vals_host["q"], kc, vc, w.block_table, idx["query_start_loc"],
                          idx["seq_lens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
                          w.block_size, w.num_blocks, w.scale, w.dtype, tokens=take,
-                         num_threads=nthreads)
+                         num_threads=nthreads, kv_cache_dtype=w.kv_cache_dtype,
+                         k_scale=w.k_scale, v_scale=w.v_scale)
         spent += time.perf_counter() - a
         done += len(take)
         n = min(n * 2, w.num_tokens - done) if spent < seconds / 4 else n
@@ -361,6 +371,7 @@ def run_ours(args):
     sl, li = torch.empty(R, dtype=i32, device=dev), torch.empty(R, dtype=i32, device=dev)
     q, key, value = vals["q"], vals["key"], vals["value"]
     kc, vc = vals["key_cache"], vals["value_cache"]
+    ks, vs = vals.get("k_scale"), vals.get("v_scale")   # FP8 pools only
     out = torch.empty_like(q)
     ws_bytes = pa.pa_attention_workspace_size(R, T, w.max_query_len, w.max_seq_len,
                                               w.num_q_heads, w.num_kv_heads, w.head_dim)
@@ -371,10 +382,11 @@ def run_ours(args):
     def step(nst=nst, nct=nct, bt=bt, q=q, key=key, value=value, timed=True):
         pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot, qsl,
                              sl, li)
-        pa.pa_cache_write(key, value, kc, vc, slot)
+        pa.pa_cache_write(key, value, kc, vc, slot, k_scale=ks, v_scale=vs)
         if timed:
             a0.record(stream)
-        pa.pa_attention(q, kc, vc, bt, qsl, sl, w.max_query_len, w.max_seq_len, w.scale, out, ws)
+        pa.pa_attention(q, kc, vc, bt, qsl, sl, w.max_query_len, w.max_seq_len, w.scale, out, ws,
+                        k_scale=ks, v_scale=vs)
         if timed:
             a1.record(stream)
 
@@ -552,7 +564,8 @@ def run_ours(args):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            pa.pa_attention(qs, kc, vc, bt_s, qsl_s, sl_s, mq, ms, w.scale, os_, ws)
+            pa.pa_attention(qs, kc, vc, bt_s, qsl_s, sl_s, mq, ms, w.scale, os_, ws, k_scale=ks,
+                            v_scale=vs)
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize()
@@ -561,7 +574,8 @@ def run_ours(args):
     logical, unique = kv_bytes(w)
     if long_mask.any() and short_mask.any():
         decode_s = time_sub(short_mask)
-        alg = (int(sl_host[short_mask].sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+        cache_elt = 1 if w.kv_cache_dtype == "fp8_e4m3" else 2
+        alg = (int(sl_host[short_mask].sum()) * 2 * w.num_kv_heads * w.head_dim * cache_elt
                + int(short_mask.sum()) * w.num_q_heads * w.head_dim * 4)
         what = "decode-class requests alone (paged_decode_kernel + merge_kernel)"
     else:

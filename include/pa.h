@@ -15,7 +15,8 @@
  *                      the zeroing of newly allocated blocks;
  *   pa_attention       causal grouped-query attention of every token over
  *                      its own request's context, read through the block
- *                      table.
+ *                      table;
+ *   pa_cache_write_ex / pa_attention_ex  the same over FP8 (E4M3) pools;
  *
  * Conventions shared by every call:
  *   - Ownership: the caller allocates and owns every buffer.  The library
@@ -68,7 +69,10 @@ typedef enum {
     PA_ERR_WORKSPACE = 6
 } pa_status;
 
-typedef enum { PA_BF16 = 0, PA_FP16 = 1 } pa_dtype;
+/* Element types.  PA_FP8_E4M3 (the OCP E4M3 "fn" format: bias 7, no
+ * infinities, largest finite 448) is a cache element type only: q, k, v and
+ * out stay bf16 or fp16. */
+typedef enum { PA_BF16 = 0, PA_FP16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 /* Bits of the detail word returned by pa_get_status(). */
 enum {
@@ -226,6 +230,30 @@ pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_st
                          int32_t num_blocks, pa_dtype dtype, pa_stream_t stream);
 
 /*
+ * pa_cache_write_ex -- pa_cache_write into pools of another element type.
+ *
+ * Defined by "Inside vLLM: Following One Request", the write op's
+ * kv_cache_dtype, k_scale and v_scale arguments, and "How vLLM Works
+ * Internally", section "FP8 KV Cache" (the cache may hold FP8 instead of
+ * 16-bit values).  cache_dtype == dtype: exactly pa_cache_write.
+ * cache_dtype == PA_FP8_E4M3: the pools hold one byte per element, and
+ *   key_cache[slot][h][d] = E4M3(key[t][h][d] / *k_scale)
+ *   value_cache[slot][h][d] = E4M3(value[t][h][d] / *v_scale)
+ * with the division in IEEE single precision and E4M3() rounding to nearest,
+ * ties to even, magnitudes past 448 saturating to +-448 (NaN stays NaN).
+ * k_scale / v_scale are device pointers to one float each (> 0); NULL means
+ * 1.0.  The 16-bit sources need 16-byte aligned rows and token stride, the
+ * pools 8-byte aligned rows (else PA_ERR_UNSUPPORTED).  Other arguments and
+ * errors as pa_cache_write.
+ */
+pa_status pa_cache_write_ex(const void *key, const void *value, int64_t kv_token_stride,
+                            void *key_cache, void *value_cache, const int32_t *slot_mapping,
+                            int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                            pa_dtype cache_dtype, const float *k_scale, const float *v_scale,
+                            pa_stream_t stream);
+
+/*
  * pa_copy_blocks -- copy-on-write: make whole cache blocks copies of others.
  *
  * Defined by "How vLLM Works Internally", section "Copy-on-Write for Beam
@@ -241,6 +269,7 @@ pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_st
  *
  * Arguments: key_cache, value_cache device pools as in pa_cache_write
  * (16-byte aligned); src_blocks, dst_blocks device int32 [num_pairs].
+ * dtype is the pools' element type (PA_BF16, PA_FP16 or PA_FP8_E4M3).
  * Errors: PA_ERR_INVALID for negative sizes, NULL buffers with num_pairs > 0,
  * unaligned pools or a bad dtype; PA_ERR_UNSUPPORTED when a block is not a
  * multiple of 16 bytes.  Data check: PA_CHECK_BLOCK_ID (that pair skipped).
@@ -320,6 +349,29 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
                        int32_t head_dim, int32_t block_size, int32_t num_blocks,
                        float scale, pa_dtype dtype, void *out, void *workspace,
                        size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_attention_ex -- pa_attention over pools of another element type.
+ *
+ * Defined as pa_attention, with the cached values read as in "How vLLM Works
+ * Internally", section "FP8 KV Cache": cache_dtype == dtype is exactly
+ * pa_attention; cache_dtype == PA_FP8_E4M3 reads one-byte E4M3 pools whose
+ * cached key is element * *k_scale and cached value element * *v_scale
+ * (device scalars; NULL = 1.0).  Every request runs on the split-K kernel
+ * with its tensor-core MMAs in f16 (E4M3 widens to f16 exactly; bf16 q is
+ * rounded to f16, exact inside f16's range); the output is dtype.  Errors as
+ * pa_attention, plus PA_ERR_INVALID for a cache_dtype that is neither dtype
+ * nor PA_FP8_E4M3.
+ */
+pa_status pa_attention_ex(const void *q, const void *key_cache, const void *value_cache,
+                          const int32_t *block_table, int32_t max_blocks_per_req,
+                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                          int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                          int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                          pa_dtype dtype, pa_dtype cache_dtype, const float *k_scale,
+                          const float *v_scale, void *out, void *workspace,
+                          size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * pa_attention_noalloc -- pa_attention for callers that cannot allocate.

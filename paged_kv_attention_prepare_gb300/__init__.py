@@ -7,8 +7,9 @@ CUDA kernels; there is no CPU or PyTorch fallback, and using the package
 without the built library raises immediately.
 
 Functions carry the C names: ``pa_prepare_inputs``, ``pa_prepare_inputs_ex``,
-``pa_cache_write``, ``pa_copy_blocks``, ``pa_zero_blocks``,
-``pa_attention_workspace_size``, ``pa_attention``, ``pa_attention_noalloc``,
+``pa_cache_write`` (over ``pa_cache_write_ex``), ``pa_copy_blocks``, ``pa_zero_blocks``,
+``pa_attention_workspace_size``, ``pa_attention`` (over ``pa_attention_ex``),
+``pa_attention_noalloc``,
 ``pa_get_status``, ``pa_launch_count``.
 """
 
@@ -25,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 
 PA_OK, PA_ERR_INVALID, PA_ERR_CUDA, PA_ERR_UNSUPPORTED = 0, 1, 2, 3
 PA_ERR_DEVICE_CHECK, PA_ERR_TIMEOUT, PA_ERR_WORKSPACE = 4, 5, 6
-PA_BF16, PA_FP16 = 0, 1
+PA_BF16, PA_FP16, PA_FP8_E4M3 = 0, 1, 2
 
 CHECK_BITS = {
     "empty_request": 1 << 0, "token_count": 1 << 1, "block_id": 1 << 2,
@@ -34,6 +35,8 @@ CHECK_BITS = {
 }
 
 _DTYPES = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16}
+# FP8 (E4M3) pools may be held as uint8 or float8_e4m3fn tensors
+_FP8_POOL = {torch.uint8, torch.float8_e4m3fn}
 _lock = threading.Lock()
 _lib = None
 
@@ -80,6 +83,13 @@ def lib():
             L.pa_attention.restype = ctypes.c_int
             L.pa_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                        i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, vp, sz, vp]
+            L.pa_cache_write_ex.restype = ctypes.c_int
+            L.pa_cache_write_ex.argtypes = [vp, vp, i64, vp, vp, vp, i32, i32, i32, i32, i32,
+                                            ctypes.c_int, ctypes.c_int, vp, vp, vp]
+            L.pa_attention_ex.restype = ctypes.c_int
+            L.pa_attention_ex.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                          i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
+                                          ctypes.c_int, vp, vp, vp, vp, sz, vp]
             L.pa_attention_noalloc.restype = ctypes.c_int
             L.pa_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                                i32, i32, i32, i32, i32, ctypes.c_float,
@@ -191,31 +201,56 @@ def pa_prepare_inputs_ex(num_scheduled_tokens, num_computed_tokens, block_table,
     _check(rc, "pa_prepare_inputs_ex")
 
 
+def _scale_ptr(t, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 \
+            or t.numel() != 1:
+        raise TypeError(f"{name} must be a one-element float32 CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _cache_dtype(q_dtype, key_cache, value_cache):
+    """The pools' pa_dtype: the q dtype, or PA_FP8_E4M3 for byte pools."""
+    if key_cache.dtype in _FP8_POOL and value_cache.dtype in _FP8_POOL:
+        return PA_FP8_E4M3
+    if key_cache.dtype != q_dtype or value_cache.dtype != q_dtype:
+        raise TypeError("caches must have the q/key dtype, or be FP8 (uint8/float8_e4m3fn)")
+    return _DTYPES[q_dtype]
+
+
 def pa_cache_write(key, value, key_cache, value_cache, slot_mapping, num_blocks=None,
-                   stream=None):
+                   stream=None, k_scale=None, v_scale=None):
     """Scatter key/value [T, Hkv, D] (token stride may exceed Hkv*D) into the
-    [NB, bs, Hkv, D] pools at slot_mapping."""
+    [NB, bs, Hkv, D] pools at slot_mapping.  FP8 pools (uint8 or
+    float8_e4m3fn) take E4M3(x / scale) with ``k_scale``/``v_scale`` one-element
+    float32 CUDA tensors (None = 1.0)."""
     T, hkv, d = key.shape
     if key.stride(1) != d or key.stride(2) != 1 or value.stride() != key.stride():
         raise ValueError("key/value rows must be [Hkv, D]-contiguous with equal strides")
     dt = _DTYPES.get(key.dtype)
-    if dt is None or value.dtype != key.dtype or key_cache.dtype != key.dtype:
-        raise TypeError("key, value and caches must share a bf16/fp16 dtype")
+    if dt is None or value.dtype != key.dtype:
+        raise TypeError("key and value must share a bf16/fp16 dtype")
+    cdt = _cache_dtype(key.dtype, key_cache, value_cache)
     nb, bs = key_cache.shape[0], key_cache.shape[1]
-    rc = lib().pa_cache_write(
+    rc = lib().pa_cache_write_ex(
         _dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
         int(key.stride(0)) if T else hkv * d, _dev(key_cache, "key_cache"),
         _dev(value_cache, "value_cache"), _dev(slot_mapping, "slot_mapping", torch.int32), T,
-        hkv, d, bs, nb if num_blocks is None else int(num_blocks), dt, _stream(stream))
+        hkv, d, bs, nb if num_blocks is None else int(num_blocks), dt, cdt,
+        _scale_ptr(k_scale, "k_scale"), _scale_ptr(v_scale, "v_scale"), _stream(stream))
     _check(rc, "pa_cache_write")
 
 
 def _pools(key_cache, value_cache):
     if key_cache.shape != value_cache.shape or key_cache.dim() != 4:
         raise ValueError("key/value caches must both be [NB, bs, Hkv, D]")
-    dt = _DTYPES.get(key_cache.dtype)
-    if dt is None or value_cache.dtype != key_cache.dtype:
-        raise TypeError("caches must share a bf16/fp16 dtype")
+    if key_cache.dtype in _FP8_POOL and value_cache.dtype in _FP8_POOL:
+        dt = PA_FP8_E4M3
+    else:
+        dt = _DTYPES.get(key_cache.dtype)
+        if dt is None or value_cache.dtype != key_cache.dtype:
+            raise TypeError("caches must share a bf16/fp16/FP8 dtype")
     nb, bs, hkv, d = key_cache.shape
     return nb, bs, hkv, d, dt
 
@@ -250,25 +285,28 @@ def pa_attention_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len
 
 
 def pa_attention(q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
-                 max_query_len, max_seq_len, scale, out, workspace=None, stream=None):
-    """Paged causal GQA attention: q [T, Hq, D] -> out [T, Hq, D]."""
+                 max_query_len, max_seq_len, scale, out, workspace=None, stream=None,
+                 k_scale=None, v_scale=None):
+    """Paged causal GQA attention: q [T, Hq, D] -> out [T, Hq, D].  FP8 pools
+    (uint8 / float8_e4m3fn) read element * k_scale / * v_scale."""
     T, hq, d = q.shape
     nb, bs, hkv, _ = key_cache.shape
     R = seq_lens.shape[0]
     dt = _DTYPES.get(q.dtype)
-    if dt is None or key_cache.dtype != q.dtype or out.dtype != q.dtype:
-        raise TypeError("q, caches and out must share a bf16/fp16 dtype")
+    if dt is None or out.dtype != q.dtype:
+        raise TypeError("q and out must share a bf16/fp16 dtype")
+    cdt = _cache_dtype(q.dtype, key_cache, value_cache)
     ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
     if workspace is not None and workspace.numel() > 0:
         ws_ptr = _dev(workspace, "workspace")
         ws_bytes = workspace.numel() * workspace.element_size()
-    rc = lib().pa_attention(
+    rc = lib().pa_attention_ex(
         _dev(q, "q"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
         _dev(block_table, "block_table", torch.int32), block_table.shape[1],
         _dev(query_start_loc, "query_start_loc", torch.int32),
         _dev(seq_lens, "seq_lens", torch.int32), R, T, int(max_query_len), int(max_seq_len),
-        hq, hkv, d, bs, nb, float(scale), dt, _dev(out, "out"), ws_ptr, ws_bytes,
-        _stream(stream))
+        hq, hkv, d, bs, nb, float(scale), dt, cdt, _scale_ptr(k_scale, "k_scale"),
+        _scale_ptr(v_scale, "v_scale"), _dev(out, "out"), ws_ptr, ws_bytes, _stream(stream))
     _check(rc, "pa_attention")
 
 

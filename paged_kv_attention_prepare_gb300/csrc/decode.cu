@@ -32,6 +32,8 @@
 #include <cstring>
 #include <type_traits>
 
+#include <cuda_fp8.h>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -41,15 +43,6 @@ constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kCtasPerSm = 3;
-constexpr int kStages = 16;
-// Page pairs (K, V) are dealt round-robin to the consumer warps.  With
-// (kStages / 2) a multiple of the warp count, pair n always lands on stages
-// 2n mod kStages and 2n+1 mod kStages owned by warp n mod 4 alone, so every
-// round of a stage is consumed by the same warp in order: a warp can never run
-// a whole ring round ahead on a stage (where mbarrier parity could not tell
-// the rounds apart).
-static_assert((kStages / 2) % kConsumerWarps == 0, "stages must split evenly among warps");
-static_assert((kStages & (kStages - 1)) == 0, "ring index arithmetic uses a power-of-two ring");
 constexpr int kPage = 16;         // tokens per cache block
 constexpr int kCandidates = 8;    // partition lengths p_min << k
 constexpr int kSingle = INT_MAX / 2;
@@ -70,28 +63,61 @@ struct Params {
     int tau;              // requests with more query tokens are not handled here
     int p_min;            // preferred partition length in keys (multiple of 256)
     float qscale;         // softmax scale * log2(e)
+    const float *k_scale; // FP8 pools: cached value = element * scale (device scalars)
+    const float *v_scale;
     unsigned int *status;
 };
 
-// Compile-time shape of the consumer work for head_dim D and RPI rows.
-template <int D, int RPI>
+// Marker for an FP8 E4M3 cache element.
+struct Fp8E4M3 {};
+
+// Shared-memory layout of one cache page (16 slots of one kv head) as the
+// TMA writes it: rows of min(128, D * elt) bytes with the matching TMA
+// swizzle (128 B, or 64 B for 64-byte rows); a 256-byte row is split into two
+// 16-row boxes, one per 128-byte half, stored back to back.
+template <typename TC, int D>
+struct Lay {
+    static constexpr int E = std::is_same<TC, Fp8E4M3>::value ? 1 : 2;  // bytes per element
+    static constexpr int RB = D * E;                  // bytes per slot row
+    static constexpr int SR = RB >= 128 ? 128 : RB;   // bytes per smem row
+    static constexpr int NSUB = RB / SR;              // TMA boxes per page
+    static constexpr int kSubBytes = kPage * SR;
+    static constexpr int kPageBytes = kPage * RB;
+    static constexpr int CPR = SR / 16;               // 16-byte chunks per smem row
+    static constexpr int NCH = RB / 64;               // chunks of a key row per lane (4 lanes per key)
+    static constexpr int KPC = 4 / E;                 // MMA k-steps per chunk (4 dims per lane per step)
+    static constexpr int KS = D / 16;                 // k-steps of QK = m-tiles of PV
+    static constexpr int kSwzMask = SR == 128 ? 7 : 3;
+    static_assert(RB % 64 == 0 && (SR == 128 || SR == 64), "head_dim 64 or 128");
+    // byte offset of 16-byte chunk c of page row `key`
+    __device__ __forceinline__ static int chunk_off(int key, int c) {
+        const int off = (c / CPR) * kSubBytes + key * SR + (c % CPR) * 16;
+        return off ^ (((off >> 7) & kSwzMask) << 4);
+    }
+};
+
+// The MMA's input type: the cache's own type for 16-bit caches (the same as
+// q's); f16 for an FP8 cache (E4M3 widens to f16 exactly).
+template <typename TQ, typename TC> struct MmaIn { using type = TC; };
+template <typename TQ> struct MmaIn<TQ, Fp8E4M3> { using type = __half; };
+
+template <typename TC, int D, int RPI>
 struct Cfg {
-    // QK: LPT lanes share one key; each holds DQ dims of q for every row.
-    static constexpr int LPT = (D == 128 && RPI >= 4) ? 16 : 8;
-    static constexpr int TPP = 32 / LPT;           // keys per pass of a warp
-    static constexpr int NPASS = kPage / TPP;      // passes per page
-    static constexpr int CPL = D / 8 / LPT;        // 16-byte chunks per lane per key row
-    static constexpr int DQ = CPL * 8;             // q dims per lane
-    // PV: lanes over dims.
-    static constexpr int DPL = D / 32;
-    static constexpr int kPageBytes = kPage * D * 2;
-    static constexpr int kStageBytes = kStages * kPageBytes;
-    // per warp: p[key][row], alpha[row]; padded to 16 bytes so every warp's
-    // buffer (and the float4 reads of it) stays aligned for any RPI
-    static constexpr int kPbuf = (kPage * RPI + RPI + 3) / 4 * 4;
+    using L = Lay<TC, D>;
+    // 64 KB of pages in flight per CTA at head_dim 128
+    static constexpr int kStages = L::E == 1 ? 32 : 16;
+    // Page pairs (K, V) are dealt round-robin to the consumer warps.  With
+    // (kStages / 2) a multiple of the warp count, pair n always lands on stages
+    // 2n mod kStages and 2n+1 mod kStages owned by warp n mod 4 alone, so every
+    // round of a stage is consumed by the same warp in order: a warp can never
+    // run a whole ring round ahead on a stage (where mbarrier parity could not
+    // tell the rounds apart).
+    static_assert((kStages / 2) % kConsumerWarps == 0, "stages must split evenly among warps");
+    static_assert((kStages & (kStages - 1)) == 0, "ring index arithmetic uses a power-of-two ring");
+    static constexpr int kStageBytes = kStages * L::kPageBytes;
     static constexpr int kComb = RPI * (D + 2);       // per warp: acc[row][D], m[row], l[row]
-    static constexpr int kBytes = kStageBytes + kConsumerWarps * (kPbuf + kComb) * 4 +
-                                  (2 * kStages + 2) * 8 + kCandidates * 8 + 256;
+    static constexpr int kBytes = kStageBytes + kConsumerWarps * kComb * 4 +
+                                  (2 * kStages + 2) * 8 + kCandidates * 8 + 1024;
 };
 
 // Per-warp walk over the request list: maps a global item index to its
@@ -203,34 +229,6 @@ __device__ __forceinline__ void item_keys(const Params &p, const typename Walker
     k1 = max(k0, min(min(k0 + part, it.L), max_pos + 1));
 }
 
-// Reduce v[RPI] across the LPT lanes of a key group so that each row's full
-// sum ends in v[0] of the lanes whose low log2(LPT/RPI) bits are zero.  Each
-// halving step trades half of the rows with the partner lane; the lane's q
-// rows are stored XOR-permuted by the row it ends up holding (slot i holds
-// row i ^ myrow), which makes "keep the low half, send the high half" right
-// for every lane and needs no selects.  RPI rows cost RPI - 1 + log2(LPT/RPI)
-// shuffles.
-template <int RPI, int LPT>
-__device__ __forceinline__ void reduce_scatter(float (&v)[RPI]) {
-#pragma unroll
-    for (int step = 0; (1 << step) < RPI; ++step) {
-        const int half = RPI >> (step + 1);
-        const int mask = (LPT / 2) >> step;
-#pragma unroll
-        for (int i = 0; i < half; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + half], mask);
-    }
-#pragma unroll
-    for (int m = LPT / RPI / 2; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
-}
-
-// Unpack a word of two 16-bit elements into a float pair (element order kept).
-template <typename T>
-__device__ __forceinline__ float2 unpack_pair(uint32_t w) {
-    float2 f;
-    Elt<T>::unpack2(w, f.x, f.y);
-    return f;
-}
-
 // Bounded barrier among the consumer warps (an mbarrier with one arrival per
 // warp): a warp that timed out elsewhere cannot leave the others waiting.
 __device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &parity, int lane) {
@@ -241,29 +239,107 @@ __device__ __forceinline__ bool consumer_sync(uint64_t *bar, uint32_t &parity, i
     return ok;
 }
 
-template <typename T, int D, int RPI>
+// ---- warp-level tensor-core helpers (mma.sync m16n8k16, f32 accumulate) ----
+
+template <typename TM> struct Mma;
+template <> struct Mma<__nv_bfloat16> {
+    __device__ __forceinline__ static void run(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+template <> struct Mma<__half> {
+    __device__ __forceinline__ static void run(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr));
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Four E4M3 codes (bytes 0..3 of w) to two f16 pairs, exactly: bytes (0, 1)
+// -> lo (byte 0 in the low half), bytes (2, 3) -> hi.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n"
+        ".reg .b16 l, h;\n"
+        "mov.b32 {l, h}, %2;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n"
+        "}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// 16-bit Q elements to the MMA's input type (the f16 path of an FP8 cache
+// takes bf16 q through float: exact inside f16's range).
+template <typename TQ, typename TM> struct QConv {
+    __device__ __forceinline__ static uint32_t run(uint32_t w) { return w; }
+};
+template <> struct QConv<__nv_bfloat16, __half> {
+    __device__ __forceinline__ static uint32_t run(uint32_t w) {
+        const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+// Logical key k (the MMA's index, 0..15) of a page lives in page row
+// perm16(k): rows 0,5,3,6,4,1,7,2 then the same + 8.  With this order every
+// shared-memory load of the consumer below is free of bank conflicts under
+// the TMA swizzle, for each element size and head_dim.
+__device__ __forceinline__ int perm16(int k) { return ((0x27146350u >> (4 * (k & 7))) & 0xf) | (k & 8); }
+
+template <typename TQ, typename TC, int D, int RPI>
 __global__ void __launch_bounds__(kThreads, RPI == 8 ? 2 : kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ Params p) {
-    using C = Cfg<D, RPI>;
-    constexpr int LPT = C::LPT, TPP = C::TPP, NPASS = C::NPASS, CPL = C::CPL, DQ = C::DQ;
-    constexpr int DPL = C::DPL;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
+    using L = Lay<TC, D>;
+    using TM = typename MmaIn<TQ, TC>::type;
+    using C = Cfg<TC, D, RPI>;
+    constexpr int kSt = C::kStages;
+    constexpr int KS = L::KS, NCH = L::NCH, KPC = L::KPC;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *stages = base;
-    float *pbuf = reinterpret_cast<float *>(base + C::kStageBytes);
-    float *comb = pbuf + kConsumerWarps * C::kPbuf;
+    float *comb = reinterpret_cast<float *>(base + C::kStageBytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(
         (reinterpret_cast<uintptr_t>(comb + kConsumerWarps * C::kComb) + 7) & ~uintptr_t(7));
-    uint64_t *empty = full + kStages;
-    uint64_t *cbar = empty + kStages;
+    uint64_t *empty = full + kSt;
+    uint64_t *cbar = empty + kSt;
     unsigned long long *cand = reinterpret_cast<unsigned long long *>(cbar + 2);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid < kCandidates) cand[tid] = 0;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kSt; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -331,6 +407,8 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     if (warp == kConsumerWarps) {
         // =================== producer warp ===================
         // Ring order: K page 0, V page 0, K page 1, V page 1, ... of each item.
+        // A page is L::NSUB swizzled boxes of 16 rows (one per 128 bytes of a
+        // row), landing back to back.
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -358,12 +436,15 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                                 flag(p.status, PA_CHECK_TIMEOUT);
                                 ok = false;
                             } else {
-                                mbar_arrive_expect_tx(&full[stage], C::kPageBytes);
-                                tma_load_3d(stages + stage * C::kPageBytes, kv ? &p.tmV : &p.tmK,
-                                            &full[stage], 0, it.g, b * kPage);
+                                mbar_arrive_expect_tx(&full[stage], L::kPageBytes);
+#pragma unroll
+                                for (int sub = 0; sub < L::NSUB; ++sub)
+                                    tma_load_3d(stages + stage * L::kPageBytes + sub * L::kSubBytes,
+                                                kv ? &p.tmV : &p.tmK, &full[stage],
+                                                sub * (L::SR / L::E), it.g, b * kPage);
                             }
                         }
-                        if (++stage == kStages) {
+                        if (++stage == kSt) {
                             stage = 0;
                             phase ^= 1;
                         }
@@ -375,12 +456,12 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         // Drain: wait (bounded) until the consumers have released every stage,
         // so no copy is still landing when the CTA exits.
         if (lane == 0) {
-            for (int s = 0; s < kStages; ++s) {
+            for (int s = 0; s < kSt; ++s) {
                 if (!mbar_wait(&empty[stage], phase ^ 1)) {
                     flag(p.status, PA_CHECK_TIMEOUT);
                     break;
                 }
-                if (++stage == kStages) {
+                if (++stage == kSt) {
                     stage = 0;
                     phase ^= 1;
                 }
@@ -391,17 +472,44 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
     // =================== consumer warps ===================
     // Warp w takes the page pairs whose running index (over all items of this
-    // CTA) is w mod 4, and keeps its own online-softmax state for its rows;
-    // the four states are combined once per item.
-    const T *q = reinterpret_cast<const T *>(p.q);
-    const int j = lane % LPT;        // lane within its key group
-    const int tq = lane / LPT;       // key group: keys tq, tq + TPP, ... of a page
-    const int dup = j & (LPT / RPI - 1);
-    int myrow = 0;                   // the row whose score this lane ends up holding
+    // CTA) is w mod 4 and keeps its own online-softmax state; the four states
+    // are combined once per item.  Per page pair, on the tensor cores:
+    //   S^T (16 keys x 8 rows) = K (16 x D) . Q^T      (D/16 MMAs, k = dims)
+    //   O^T (D x 8 rows)      += V^T (D x 16) . P^T    (D/16 MMAs, k = keys)
+    // Lane (gq = lane/4, tq = lane%4) holds S^T for keys perm16(gq), perm16(gq+8)
+    // and rows 2tq, 2tq+1; the rows of an item (its (token, head) pairs, at most
+    // 8) are the MMAs' N.  P^T is moved from the S^T layout to the B-operand
+    // layout by two 8x8 transposes (movmatrix).
+    const TQ *q = reinterpret_cast<const TQ *>(p.q);
+    const int gq = lane >> 2, tq = lane & 3;
+    const float qs = p.qscale * (p.k_scale ? *p.k_scale : 1.f);
+    const float vs = p.v_scale ? *p.v_scale : 1.f;
+    const int key_a = perm16(gq), key_b = perm16(gq + 8);   // page rows of this lane's keys
+    // Byte offsets inside a page, fixed per lane.  K: the lane's chunks of
+    // keys key_a / key_b.  V (16-bit): the row this lane gives ldmatrix for
+    // m-tile mt (logical key (lane & 7) + 8 * (matrix >> 1), dims 16 mt +
+    // 8 * (matrix & 1)).  V (FP8): the lane's D/8 bytes (dims gq * D/8 ..) of
+    // keys 2tq, 2tq + 1, 2tq + 8, 2tq + 9.
+    // Offsets of later chunks follow from the first by flipping swizzle bits
+    // (chunk c + 4 of a 128-byte row: bit 6) and adding whole 16-row boxes,
+    // so each needs one register.  (A 64-byte row has one chunk per lane.)
+    static_assert(L::SR == 128 || NCH == 1, "one chunk per lane on 64-byte rows");
+    const int koff_a = L::chunk_off(key_a, tq), koff_b = L::chunk_off(key_b, tq);
+    auto koff = [&](int base, int jj) { return (base ^ (64 * (jj & 1))) + (jj >> 1) * L::kSubBytes; };
+    int vkey[4];                     // page rows of keys 2tq, 2tq + 1, 2tq + 8, 2tq + 9
+    vkey[0] = perm16(2 * tq);
+    vkey[1] = perm16(2 * tq + 1);
+    vkey[2] = perm16(2 * tq + 8);
+    vkey[3] = perm16(2 * tq + 9);
+    int voff[L::E == 2 ? 1 : 4];
+    if constexpr (L::E == 2) {
+        const int mi = lane >> 3;
+        voff[0] = L::chunk_off(perm16((lane & 7) + 8 * (mi >> 1)), mi & 1);
+    } else {
+        const int byte = gq * (D / 8);
 #pragma unroll
-    for (int step = 0; (1 << step) < RPI; ++step)
-        if (j & ((LPT / 2) >> step)) myrow += RPI >> (step + 1);
-    float *pb = pbuf + warp * C::kPbuf;
+        for (int e = 0; e < 4; ++e) voff[e] = L::chunk_off(vkey[e], byte / 16) + byte % 16;
+    }
     float *cw = comb + warp * C::kComb;
     int pair_base = 0;               // page pairs of earlier items
     uint32_t cpar = 0;
@@ -413,179 +521,213 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         const int qstart = p.qsl[it.r];
         const int nrows = it.n * p.G;
         const int pos0 = it.L - it.n;  // position of the request's first query token
-        int lim;                       // last key this lane's row may see
+        // last key each of this lane's two rows (2tq, 2tq + 1) may see; -1 for
+        // rows past the item
+        int lim0 = -1, lim1 = -1;
         {
-            const int rr = it.chunk * RPI + myrow;
-            lim = rr < nrows ? min(pos0 + rr / p.G, k1 - 1) : -1;
+            const int r0 = it.chunk * RPI + 2 * tq, r1 = r0 + 1;
+            if (2 * tq < RPI && r0 < nrows) lim0 = min(pos0 + r0 / p.G, k1 - 1);
+            if (2 * tq + 1 < RPI && r1 < nrows) lim1 = min(pos0 + r1 / p.G, k1 - 1);
         }
         // Pages whose last key every row of the item sees need no mask (rows
-        // past the request's end may then pick up scores, but they are never
-        // written out and stay in their own accumulators).
+        // past the item then pick up scores, but they are never written out).
         const int lim_all = min(pos0 + (it.chunk * RPI) / p.G, k1 - 1);
 
-        // q rows of this item, this lane's QK dims, pre-scaled by scale*log2(e);
-        // slot r holds row r ^ myrow (see reduce_scatter).
-        float2 qv[RPI][DQ / 2];
+        // Q^T fragments (B operand): row gq of the item, this lane's dims.
+        uint32_t qf[KS][2];
+        {
+            const int rr = it.chunk * RPI + gq;
+            const bool have = gq < RPI && rr < nrows;
+            const TQ *qrow = q + ((long long)(qstart + (have ? rr / p.G : 0)) * p.Hq + it.g * p.G +
+                                  (have ? rr % p.G : 0)) * D;
 #pragma unroll
-        for (int r = 0; r < RPI; ++r) {
-            const int rr = it.chunk * RPI + (r ^ myrow);
-            if (rr < nrows) {
-                const T *qrow = q + ((long long)(qstart + rr / p.G) * p.Hq + it.g * p.G + rr % p.G) * D;
+            for (int jj = 0; jj < NCH; ++jj) {
+                const int d0 = (tq + 4 * jj) * (16 / L::E);   // first dim of the lane's chunk
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (j + c * LPT) * 8);
+                for (int h = 0; h < 16 / L::E / 8; ++h) {   // 8 dims (16 bytes of q) at a time
+                    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+                    if (have) raw = *reinterpret_cast<const uint4 *>(qrow + d0 + 8 * h);
                     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float2 f = unpack_pair<T>(w4[e]);
-                        qv[r][c * 4 + e] = make_float2(f.x * p.qscale, f.y * p.qscale);
-                    }
+                    // 4 dims per k-step: pairs (0,1) -> b0b1, (2,3) -> b2b3
+                    qf[jj * KPC + 2 * h][0] = QConv<TQ, TM>::run(w4[0]);
+                    qf[jj * KPC + 2 * h][1] = QConv<TQ, TM>::run(w4[1]);
+                    qf[jj * KPC + 2 * h + 1][0] = QConv<TQ, TM>::run(w4[2]);
+                    qf[jj * KPC + 2 * h + 1][1] = QConv<TQ, TM>::run(w4[3]);
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < DQ / 2; ++e) qv[r][e] = make_float2(0.f, 0.f);
             }
         }
-        float2 acc[RPI][DPL / 2];
+        float o[KS][4];
 #pragma unroll
-        for (int r = 0; r < RPI; ++r)
-#pragma unroll
-            for (int e = 0; e < DPL / 2; ++e) acc[r][e] = make_float2(0.f, 0.f);
-        float m_run = -INFINITY, l_run = 0.f;
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY;   // reference max of rows 2tq, 2tq+1
+        float l0 = 0.f, l1 = 0.f;               // this lane's share of the row sums
 
         for (int pg = (warp - pair_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
              pg < npages; pg += kConsumerWarps) {
-            const int n2 = 2 * (pair_base + pg);
-            const int stK = n2 & (kStages - 1), stV = (n2 + 1) & (kStages - 1);
-            const uint32_t phK = (uint32_t)(n2 / kStages) & 1u, phV = (uint32_t)((n2 + 1) / kStages) & 1u;
+            const uint32_t n2 = 2u * (uint32_t)(pair_base + pg);
+            const uint32_t stK = n2 & (kSt - 1), stV = (n2 + 1) & (kSt - 1);
+            const uint32_t phK = (n2 / kSt) & 1u, phV = ((n2 + 1) / kSt) & 1u;
             const int key0 = k0 + pg * kPage;
             const bool page_visible = key0 + kPage - 1 <= lim_all;
 
-            // ---- scores of the page's 16 keys for this warp's rows
+            // ---- S^T = K Q^T for the page's 16 keys
             if (!mbar_wait_warp(&full[stK], phK)) {
                 flag(p.status, PA_CHECK_TIMEOUT);
                 ok = false;
                 break;
             }
-            const unsigned char *kpage = stages + stK * C::kPageBytes;
-            float sc[NPASS];
-            float alpha;
-            // Scores and the online-softmax update for this lane's row.  With
-            // every key of the page visible to every row (the common case) no
-            // mask is applied and the running max is always finite.
-            auto qk_softmax = [&](auto all_visible) {
-                constexpr bool kVis = decltype(all_visible)::value;
+            const unsigned char *kpage = stages + stK * L::kPageBytes;
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ps = 0; ps < NPASS; ++ps) {
-                    const int t = ps * TPP + tq;
-                    float2 kf[DQ / 2];
+            for (int jj = 0; jj < NCH; ++jj) {
+                const uint4 ka = *reinterpret_cast<const uint4 *>(kpage + koff(koff_a, jj));
+                const uint4 kb = *reinterpret_cast<const uint4 *>(kpage + koff(koff_b, jj));
+                const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-                    for (int c = 0; c < CPL; ++c) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(kpage + t * D * 2 + (j + c * LPT) * 16);
-                        kf[c * 4 + 0] = unpack_pair<T>(raw.x);
-                        kf[c * 4 + 1] = unpack_pair<T>(raw.y);
-                        kf[c * 4 + 2] = unpack_pair<T>(raw.z);
-                        kf[c * 4 + 3] = unpack_pair<T>(raw.w);
+                for (int sub = 0; sub < KPC; ++sub) {
+                    const int s = jj * KPC + sub;
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (L::E == 2) {
+                        a0 = wa[2 * sub];
+                        a1 = wb[2 * sub];
+                        a2 = wa[2 * sub + 1];
+                        a3 = wb[2 * sub + 1];
+                    } else {
+                        e4m3x4_to_f16x4(wa[sub], a0, a2);
+                        e4m3x4_to_f16x4(wb[sub], a1, a3);
                     }
-                    float sr[RPI];
-#pragma unroll
-                    for (int r = 0; r < RPI; ++r) {
-                        float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int e = 0; e < DQ / 2; ++e) a = __ffma2_rn(qv[r][e], kf[e], a);
-                        sr[r] = a.x + a.y;
-                    }
-                    reduce_scatter<RPI, LPT>(sr);
-                    sc[ps] = (kVis || key0 + t <= lim) ? sr[0] : -INFINITY;
+                    if (s & 1) Mma<TM>::run(sb, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                    else Mma<TM>::run(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stK]);
-                float mp = sc[0];
-#pragma unroll
-                for (int ps = 1; ps < NPASS; ++ps) mp = fmaxf(mp, sc[ps]);
-#pragma unroll
-                for (int m = LPT; m < 32; m <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, m));
-                const float m_new = fmaxf(m_run, mp);
-                float sum = 0.f;
-                if (kVis) {
-                    alpha = fast_exp2(m_run - m_new);
-#pragma unroll
-                    for (int ps = 0; ps < NPASS; ++ps) {
-                        sc[ps] = fast_exp2(sc[ps] - m_new);
-                        sum += sc[ps];
-                    }
-                } else {
-                    alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
-#pragma unroll
-                    for (int ps = 0; ps < NPASS; ++ps) {
-                        const float e = m_new == -INFINITY ? 0.f : fast_exp2(sc[ps] - m_new);
-                        sc[ps] = e;
-                        sum += e;
-                    }
-                }
-#pragma unroll
-                for (int m = LPT; m < 32; m <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
-                l_run = l_run * alpha + sum;
-                m_run = m_new;
-            };
-            if (page_visible) qk_softmax(std::true_type{});
-            else qk_softmax(std::false_type{});
-            if (dup == 0) {
-#pragma unroll
-                for (int ps = 0; ps < NPASS; ++ps) pb[(ps * TPP + tq) * RPI + myrow] = sc[ps];
-                if (tq == 0) pb[kPage * RPI + myrow] = alpha;
             }
             __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stK]);
+            // sv: (key_a, row 2tq), (key_a, row 2tq+1), (key_b, row 2tq), (key_b, row 2tq+1)
+            float sv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sv[e] = (sa[e] + sb[e]) * qs;
 
-            // ---- weighted values
+            // ---- online softmax with a lazily moved reference max: P stays
+            //      below 2^8, so the 16-bit P and the f32 sums are exact enough,
+            //      and O is rescaled only when a row's max grows by more than 8
+            //      (in log2 units).
+            if (!page_visible) {
+                const int pa = key0 + key_a, pb = key0 + key_b;
+                sv[0] = pa <= lim0 ? sv[0] : -INFINITY;
+                sv[1] = pa <= lim1 ? sv[1] : -INFINITY;
+                sv[2] = pb <= lim0 ? sv[2] : -INFINITY;
+                sv[3] = pb <= lim1 ? sv[3] : -INFINITY;
+            }
+            float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+            }
+            const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
+            if (up0 || up1) {
+                const float al0 = up0 ? fast_exp2(m0 - mx0) : 1.f;
+                const float al1 = up1 ? fast_exp2(m1 - mx1) : 1.f;
+                if (up0) m0 = mx0;
+                if (up1) m1 = mx1;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                }
+                l0 *= al0;
+                l1 *= al1;
+            }
+            float pv[4];
+            if (page_visible) {
+                pv[0] = fast_exp2(sv[0] - m0);
+                pv[1] = fast_exp2(sv[1] - m1);
+                pv[2] = fast_exp2(sv[2] - m0);
+                pv[3] = fast_exp2(sv[3] - m1);
+            } else {
+                pv[0] = m0 == -INFINITY ? 0.f : fast_exp2(sv[0] - m0);
+                pv[1] = m1 == -INFINITY ? 0.f : fast_exp2(sv[1] - m1);
+                pv[2] = m0 == -INFINITY ? 0.f : fast_exp2(sv[2] - m0);
+                pv[3] = m1 == -INFINITY ? 0.f : fast_exp2(sv[3] - m1);
+            }
+            l0 += pv[0] + pv[2];
+            l1 += pv[1] + pv[3];
+            const uint32_t pb0 = movmatrix_trans(Mma<TM>::pack(pv[0], pv[1]));
+            const uint32_t pb1 = movmatrix_trans(Mma<TM>::pack(pv[2], pv[3]));
+
+            // ---- O^T += V^T P^T
             if (!mbar_wait_warp(&full[stV], phV)) {
                 flag(p.status, PA_CHECK_TIMEOUT);
                 ok = false;
                 break;
             }
-            const unsigned char *vpage = stages + stV * C::kPageBytes;
+            const unsigned char *vpage = stages + stV * L::kPageBytes;
+            // Slots past the context hold stale data (maybe NaN): on a partial
+            // page their V is zeroed in registers (their P is already 0).
+            auto pv_page = [&](auto full_page) {
+                constexpr bool kFull = decltype(full_page)::value;
+                const int nvalid = min(kPage, k1 - key0);
+                if constexpr (L::E == 2) {
+                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // keys (2tq, 2tq+1), (+8, +9)
+                    if constexpr (!kFull) {
+                        mlo = (vkey[0] < nvalid ? 0x0000ffffu : 0u) | (vkey[1] < nvalid ? 0xffff0000u : 0u);
+                        mhi = (vkey[2] < nvalid ? 0x0000ffffu : 0u) | (vkey[3] < nvalid ? 0xffff0000u : 0u);
+                    }
+                    const uint32_t vbase = smem_u32(vpage);
 #pragma unroll
-            for (int r = 0; r < RPI; ++r) {
-                const float a = pb[kPage * RPI + r];
-#pragma unroll
-                for (int e = 0; e < DPL / 2; ++e) acc[r][e] = __fmul2_rn(acc[r][e], make_float2(a, a));
-            }
-            const int nvalid = min(kPage, k1 - key0);  // never touch slots past the context
-            auto pv_key = [&](int t) {
-                float2 vf[DPL / 2];
-                if constexpr (DPL == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(vpage + t * D * 2 + lane * 8);
-                    vf[0] = unpack_pair<T>(raw.x);
-                    vf[1] = unpack_pair<T>(raw.y);
-                } else {
-                    vf[0] = unpack_pair<T>(*reinterpret_cast<const uint32_t *>(vpage + t * D * 2 + lane * 4));
-                }
-                float pr[RPI];
-                if constexpr (RPI >= 4) {
-#pragma unroll
-                    for (int r = 0; r < RPI; r += 4) {
-                        const float4 v4 = *reinterpret_cast<const float4 *>(pb + t * RPI + r);
-                        pr[r] = v4.x;
-                        pr[r + 1] = v4.y;
-                        pr[r + 2] = v4.z;
-                        pr[r + 3] = v4.w;
+                    for (int mt = 0; mt < KS; ++mt) {
+                        uint32_t a[4];
+                        // chunk 2 mt + (matrix & 1): flip bits 5-6 by 2 mt mod 8, add boxes
+                        ldmatrix_x4_trans(a, vbase + ((voff[0] ^ (((2 * mt) & 7) << 4)) +
+                                                      (mt >> 2) * L::kSubBytes));
+                        if constexpr (!kFull) {
+                            a[0] &= mlo;
+                            a[1] &= mlo;
+                            a[2] &= mhi;
+                            a[3] &= mhi;
+                        }
+                        Mma<TM>::run(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
                     }
                 } else {
+                    // D/32 words per key: dims gq*D/8 + 4 tp .. + 3; byte-interleave
+                    // the key pairs, widen to f16, two m-tiles per word
+                    constexpr int NW = D / 32;
+                    uint32_t w[4][NW];
 #pragma unroll
-                    for (int r = 0; r < RPI; ++r) pr[r] = pb[t * RPI + r];
+                    for (int e = 0; e < 4; ++e) {
+                        if constexpr (NW == 4) {
+                            const uint4 v4 = *reinterpret_cast<const uint4 *>(vpage + voff[e]);
+                            w[e][0] = v4.x;
+                            w[e][1] = v4.y;
+                            w[e][2] = v4.z;
+                            w[e][3] = v4.w;
+                        } else {
+                            const uint2 v2 = *reinterpret_cast<const uint2 *>(vpage + voff[e]);
+                            w[e][0] = v2.x;
+                            w[e][1] = v2.y;
+                        }
+                        if constexpr (!kFull) {
+                            const uint32_t keep = vkey[e] < nvalid ? 0xffffffffu : 0u;
+#pragma unroll
+                            for (int tp = 0; tp < NW; ++tp) w[e][tp] &= keep;
+                        }
+                    }
+#pragma unroll
+                    for (int tp = 0; tp < NW; ++tp) {
+                        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+                        e4m3x4_to_f16x4(__byte_perm(w[0][tp], w[1][tp], 0x5140), a0, a1);
+                        e4m3x4_to_f16x4(__byte_perm(w[2][tp], w[3][tp], 0x5140), a2, a3);
+                        e4m3x4_to_f16x4(__byte_perm(w[0][tp], w[1][tp], 0x7362), c0, c1);
+                        e4m3x4_to_f16x4(__byte_perm(w[2][tp], w[3][tp], 0x7362), c2, c3);
+                        Mma<TM>::run(o[2 * tp], a0, a1, a2, a3, pb0, pb1);
+                        Mma<TM>::run(o[2 * tp + 1], c0, c1, c2, c3, pb0, pb1);
+                    }
                 }
-#pragma unroll
-                for (int r = 0; r < RPI; ++r)
-#pragma unroll
-                    for (int e = 0; e < DPL / 2; ++e)
-                        acc[r][e] = __ffma2_rn(make_float2(pr[r], pr[r]), vf[e], acc[r][e]);
             };
-            if (nvalid == kPage) {
-#pragma unroll
-                for (int t = 0; t < kPage; ++t) pv_key(t);
-            } else {
-                for (int t = 0; t < nvalid; ++t) pv_key(t);
-            }
+            if (key0 + kPage <= k1) pv_page(std::true_type{});
+            else pv_page(std::false_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stV]);
         }
@@ -594,22 +736,48 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
         // ---- combine the four warps' states and write the item out
 #pragma unroll
-        for (int r = 0; r < RPI; ++r)
+        for (int x = 4; x < 32; x <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+        }
+        // O^T element (dim row, item row): rows 2tq, 2tq+1 of this lane
 #pragma unroll
-            for (int e = 0; e < DPL / 2; ++e)
-                *reinterpret_cast<float2 *>(cw + r * D + lane * DPL + 2 * e) = acc[r][e];
-        if (dup == 0 && tq == 0) {
-            cw[RPI * D + myrow] = m_run;
-            cw[RPI * D + RPI + myrow] = l_run;
+        for (int mt = 0; mt < KS; ++mt) {
+            int dlo, dhi;   // dims of the m-tile's rows gq and gq + 8
+            if constexpr (L::E == 2) {
+                dlo = 16 * mt + gq;
+                dhi = dlo + 8;
+            } else {
+                dlo = gq * (D / 8) + 4 * (mt >> 1) + 2 * (mt & 1);
+                dhi = dlo + 1;
+            }
+            if (2 * tq < RPI) {
+                cw[(2 * tq) * D + dlo] = o[mt][0];
+                cw[(2 * tq) * D + dhi] = o[mt][2];
+            }
+            if (2 * tq + 1 < RPI) {
+                cw[(2 * tq + 1) * D + dlo] = o[mt][1];
+                cw[(2 * tq + 1) * D + dhi] = o[mt][3];
+            }
+        }
+        if (gq == 0) {
+            if (2 * tq < RPI) {
+                cw[RPI * D + 2 * tq] = m0;
+                cw[RPI * D + RPI + 2 * tq] = l0;
+            }
+            if (2 * tq + 1 < RPI) {
+                cw[RPI * D + 2 * tq + 1] = m1;
+                cw[RPI * D + RPI + 2 * tq + 1] = l1;
+            }
         }
         if (!consumer_sync(cbar, cpar, lane)) {
             flag(p.status, PA_CHECK_TIMEOUT);
             ok = false;
             break;
         }
-        for (int o = tid; o < RPI * D / 2; o += kConsumers) {
-            const int r = o / (D / 2);
-            const int d = (o % (D / 2)) * 2;
+        for (int o2 = tid; o2 < RPI * D / 2; o2 += kConsumers) {
+            const int r = o2 / (D / 2);
+            const int d = (o2 % (D / 2)) * 2;
             const int rr = it.chunk * RPI + r;
             if (rr >= nrows) continue;
             float M = -INFINITY;
@@ -626,12 +794,14 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 s0 += sw * a.x;
                 s1 += sw * a.y;
             }
+            s0 *= vs;   // an FP8 pool's V scale; 1 otherwise
+            s1 *= vs;
             if (it.pslot < 0) {
                 const float inv = 1.f / Ls;
                 const int h = it.g * p.G + rr % p.G;
-                T *dst = reinterpret_cast<T *>(p.out) +
-                         ((long long)(qstart + rr / p.G) * p.Hq + h) * D + d;
-                *reinterpret_cast<uint32_t *>(dst) = Elt<T>::pack2(s0 * inv, s1 * inv);
+                TQ *dst = reinterpret_cast<TQ *>(p.out) +
+                          ((long long)(qstart + rr / p.G) * p.Hq + h) * D + d;
+                *reinterpret_cast<uint32_t *>(dst) = Elt<TQ>::pack2(s0 * inv, s1 * inv);
             } else {
                 float *po = p.part_o + (it.pslot * RPI + r) * D + d;
                 *reinterpret_cast<float2 *>(po) = make_float2(s0, s1);
@@ -650,7 +820,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     // the item barrier once, so the others' bounded waits and the producer's
     // drain can finish.
     if (!ok && lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_arrive(&empty[s]);
+        for (int s = 0; s < kSt; ++s) mbar_arrive(&empty[s]);
         mbar_arrive(cbar);
     }
 }
@@ -737,18 +907,18 @@ __global__ void __launch_bounds__(32 * kMergeHeadsPerCta) merge_kernel(const __g
         *reinterpret_cast<uint32_t *>(dst + d) = Elt<T>::pack2(o[d] * inv, o[d + 1] * inv);
 }
 
-template <typename T, int D, int RPI>
+template <typename TQ, typename TC, int D, int RPI>
 pa_status launch_typed(Params &prm, long long max_items, bool merge, cudaStream_t stream) {
-    using S = Cfg<D, RPI>;
+    using S = Cfg<TC, D, RPI>;
     static int resident[64] = {};  // CTAs per SM, per device
     int dev = 0;
     PA_TRY_CUDA(cudaGetDevice(&dev));
     int per_sm = dev < 64 ? resident[dev] : 0;
     if (per_sm == 0) {
-        PA_TRY_CUDA(cudaFuncSetAttribute(paged_decode_kernel<T, D, RPI>,
+        PA_TRY_CUDA(cudaFuncSetAttribute(paged_decode_kernel<TQ, TC, D, RPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes));
         PA_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, paged_decode_kernel<T, D, RPI>, kThreads, S::kBytes));
+            &per_sm, paged_decode_kernel<TQ, TC, D, RPI>, kThreads, S::kBytes));
         if (per_sm < 1) return PA_ERR_UNSUPPORTED;
         if (dev < 64) resident[dev] = per_sm;
     }
@@ -756,26 +926,36 @@ pa_status launch_typed(Params &prm, long long max_items, bool merge, cudaStream_
     long long grid = (long long)per_sm * num_sms();
     if (max_items < grid) grid = max_items;
     if (grid < 1) grid = 1;
-    paged_decode_kernel<T, D, RPI><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
+    paged_decode_kernel<TQ, TC, D, RPI><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
     if (merge && prm.T > 0) {
         const long long groups = (prm.Hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta;
-        merge_kernel<T, D, RPI><<<(unsigned)(prm.T * groups), 32 * kMergeHeadsPerCta, 0, stream>>>(prm);
+        merge_kernel<TQ, D, RPI><<<(unsigned)(prm.T * groups), 32 * kMergeHeadsPerCta, 0, stream>>>(prm);
         PA_TRY_CUDA(cudaGetLastError());
         note_launch();
     }
     return PA_OK;
 }
 
-template <typename T, int D>
+template <typename TQ, typename TC, int D>
 pa_status dispatch_rpi(int rpi, Params &prm, long long grid, bool merge, cudaStream_t stream) {
     switch (rpi) {
-        case 1: return launch_typed<T, D, 1>(prm, grid, merge, stream);
-        case 2: return launch_typed<T, D, 2>(prm, grid, merge, stream);
-        case 4: return launch_typed<T, D, 4>(prm, grid, merge, stream);
-        default: return launch_typed<T, D, 8>(prm, grid, merge, stream);
+        case 1: return launch_typed<TQ, TC, D, 1>(prm, grid, merge, stream);
+        case 2: return launch_typed<TQ, TC, D, 2>(prm, grid, merge, stream);
+        case 4: return launch_typed<TQ, TC, D, 4>(prm, grid, merge, stream);
+        default: return launch_typed<TQ, TC, D, 8>(prm, grid, merge, stream);
     }
+}
+
+template <typename TQ>
+pa_status dispatch_cache(bool fp8, int D, int rpi, Params &prm, long long grid, bool merge,
+                         cudaStream_t stream) {
+    if (fp8)
+        return D == 128 ? dispatch_rpi<TQ, Fp8E4M3, 128>(rpi, prm, grid, merge, stream)
+                        : dispatch_rpi<TQ, Fp8E4M3, 64>(rpi, prm, grid, merge, stream);
+    return D == 128 ? dispatch_rpi<TQ, TQ, 128>(rpi, prm, grid, merge, stream)
+                    : dispatch_rpi<TQ, TQ, 64>(rpi, prm, grid, merge, stream);
 }
 
 // Rows per item: all heads of a kv group (at most 8, the register budget).
@@ -821,9 +1001,13 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     Params prm;
     memset(&prm, 0, sizeof prm);
     const int64_t slots = (int64_t)a.NB * a.bs;
-    if (!encode_pool_map(&prm.tmK, a.kc, slots, a.Hkv, a.D, kPage) ||
-        !encode_pool_map(&prm.tmV, a.vc, slots, a.Hkv, a.D, kPage))
+    const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
+    const int elt = fp8 ? 1 : 2;
+    if (!encode_pool_map_swizzled(&prm.tmK, a.kc, slots, a.Hkv, a.D, elt, kPage) ||
+        !encode_pool_map_swizzled(&prm.tmV, a.vc, slots, a.Hkv, a.D, elt, kPage))
         return PA_ERR_CUDA;
+    prm.k_scale = a.k_scale;
+    prm.v_scale = a.v_scale;
     prm.q = a.q;
     prm.out = a.out;
     prm.bt = a.bt;
@@ -870,12 +1054,9 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     const long long chunks = (long long)a.R + ((long long)a.T * prm.G + rpi - 1) / rpi;
     const long long grid = (long long)a.Hkv * chunks * splits;
 
-    const bool bf16 = a.dtype == PA_BF16;
-    if (a.D == 128)
-        return bf16 ? dispatch_rpi<__nv_bfloat16, 128>(rpi, prm, grid, merge, stream)
-                    : dispatch_rpi<__half, 128>(rpi, prm, grid, merge, stream);
-    return bf16 ? dispatch_rpi<__nv_bfloat16, 64>(rpi, prm, grid, merge, stream)
-                : dispatch_rpi<__half, 64>(rpi, prm, grid, merge, stream);
+    return a.dtype == PA_BF16
+               ? dispatch_cache<__nv_bfloat16>(fp8, a.D, rpi, prm, grid, merge, stream)
+               : dispatch_cache<__half>(fp8, a.D, rpi, prm, grid, merge, stream);
 }
 
 }  // namespace pa

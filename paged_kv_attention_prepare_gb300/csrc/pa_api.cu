@@ -58,8 +58,8 @@ int num_sms() {
     return g_sms[dev];
 }
 
-bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv, int D,
-                     int box_rows) {
+bool encode_pool_map_swizzled(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv,
+                              int D, int elt, int box_rows) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_encode) {
@@ -72,14 +72,18 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_slots, int 
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
     }
+    const int row = D * elt;
+    const int inner = row >= 128 ? 128 : row;  // bytes of one box row
+    if (inner != 128 && inner != 64) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_slots};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)box_rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)row, (cuuint64_t)Hkv * row};
+    const cuuint32_t box[3] = {(cuuint32_t)(inner / elt), 1u, (cuuint32_t)box_rows};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(pool), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(map, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                          3, const_cast<void *>(pool), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -219,11 +223,12 @@ pa_status pa_prepare_inputs_ex(const int32_t *num_scheduled_tokens,
 static pa_status check_block_op(void *kc, void *vc, const void *a, const void *b, int32_t n,
                                 int32_t bs, int32_t hkv, int32_t d, int32_t nb, pa_dtype dtype,
                                 int64_t *block_bytes) {
-    if (n < 0 || bs <= 0 || hkv <= 0 || d <= 0 || nb < 0 || (dtype != PA_BF16 && dtype != PA_FP16))
+    if (n < 0 || bs <= 0 || hkv <= 0 || d <= 0 || nb < 0 ||
+        (dtype != PA_BF16 && dtype != PA_FP16 && dtype != PA_FP8_E4M3))
         return PA_ERR_INVALID;
     if (n > 0 && (!kc || !vc || !a || !b)) return PA_ERR_INVALID;
     if (n > 0 && (!aligned(kc, 16) || !aligned(vc, 16))) return PA_ERR_INVALID;
-    const int64_t bb = (int64_t)bs * hkv * d * 2;
+    const int64_t bb = (int64_t)bs * hkv * d * (dtype == PA_FP8_E4M3 ? 1 : 2);
     if (bb % 16 != 0) return PA_ERR_UNSUPPORTED;
     *block_bytes = bb;
     return PA_OK;
@@ -251,6 +256,30 @@ pa_status pa_zero_blocks(void *key_cache, void *value_cache, const int32_t *bloc
     if (st != PA_OK) return st;
     return launch_zero_blocks(key_cache, value_cache, bb, num_blocks, block_ids, num_ids,
                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_cache_write_ex(const void *key, const void *value, int64_t kv_token_stride,
+                            void *key_cache, void *value_cache, const int32_t *slot_mapping,
+                            int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                            pa_dtype cache_dtype, const float *k_scale, const float *v_scale,
+                            pa_stream_t stream) {
+    if (cache_dtype == dtype)
+        return pa_cache_write(key, value, kv_token_stride, key_cache, value_cache, slot_mapping,
+                              num_tokens, num_kv_heads, head_dim, block_size, num_blocks, dtype,
+                              stream);
+    if (cache_dtype != PA_FP8_E4M3) return PA_ERR_INVALID;
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || (dtype != PA_BF16 && dtype != PA_FP16))
+        return PA_ERR_INVALID;
+    if (kv_token_stride < (int64_t)num_kv_heads * head_dim) return PA_ERR_INVALID;
+    if (num_tokens > 0 && (!key || !value || !key_cache || !value_cache || !slot_mapping))
+        return PA_ERR_INVALID;
+    if ((int64_t)num_kv_heads * head_dim > INT32_MAX / 2) return PA_ERR_UNSUPPORTED;
+    return launch_cache_write_fp8(key, value, kv_token_stride, key_cache, value_cache,
+                                  slot_mapping, num_tokens, num_kv_heads * head_dim,
+                                  (int64_t)num_blocks * block_size, dtype, k_scale, v_scale,
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 pa_status pa_cache_write(const void *key, const void *value, int64_t kv_token_stride,
@@ -286,10 +315,27 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                        int32_t block_size, int32_t num_blocks, float scale, pa_dtype dtype,
                        void *out, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return pa_attention_ex(q, key_cache, value_cache, block_table, max_blocks_per_req,
+                           query_start_loc, seq_lens, num_reqs, num_tokens, max_query_len,
+                           max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                           num_blocks, scale, dtype, dtype, nullptr, nullptr, out, workspace,
+                           workspace_bytes, stream);
+}
+
+pa_status pa_attention_ex(const void *q, const void *key_cache, const void *value_cache,
+                          const int32_t *block_table, int32_t max_blocks_per_req,
+                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                          int32_t num_reqs, int32_t num_tokens, int32_t max_query_len,
+                          int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                          pa_dtype dtype, pa_dtype cache_dtype, const float *k_scale,
+                          const float *v_scale, void *out, void *workspace,
+                          size_t workspace_bytes, pa_stream_t stream) {
     if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0 ||
         num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks < 0 || max_blocks_per_req < 0 || (dtype != PA_BF16 && dtype != PA_FP16))
         return PA_ERR_INVALID;
+    if (cache_dtype != dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_INVALID;
     if (workspace_bytes > 0 && (!workspace || !aligned(workspace, 256))) return PA_ERR_INVALID;
     if (num_tokens == 0 || num_reqs == 0) return PA_OK;
     if (!q || !key_cache || !value_cache || !block_table || !query_start_loc || !seq_lens || !out)
@@ -321,6 +367,9 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
     a.NB = num_blocks;
     a.scale = scale;
     a.dtype = dtype;
+    a.cache_dtype = cache_dtype;
+    a.k_scale = cache_dtype == PA_FP8_E4M3 ? k_scale : nullptr;
+    a.v_scale = cache_dtype == PA_FP8_E4M3 ? v_scale : nullptr;
     a.out = out;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;

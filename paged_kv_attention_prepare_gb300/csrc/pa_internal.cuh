@@ -54,6 +54,11 @@ pa_status launch_zero_blocks(void *kc, void *vc, int64_t block_bytes, int32_t nu
 pa_status launch_cache_write(const void *key, const void *value, int64_t stride_elems,
                              void *kc, void *vc, const int32_t *slots, int32_t T,
                              int32_t row_elems, int64_t num_slots, cudaStream_t stream);
+// The write into FP8 pools: element / scale, rounded to E4M3 (satfinite).
+pa_status launch_cache_write_fp8(const void *key, const void *value, int64_t stride_elems,
+                                 void *kc, void *vc, const int32_t *slots, int32_t T,
+                                 int32_t row_elems, int64_t num_slots, pa_dtype src,
+                                 const float *k_scale, const float *v_scale, cudaStream_t stream);
 
 struct AttnArgs {
     const void *q;
@@ -63,7 +68,10 @@ struct AttnArgs {
     const int32_t *qsl, *seq_lens;
     int32_t R, T, max_q, max_seq, Hq, Hkv, D, bs, NB;
     float scale;
-    pa_dtype dtype;
+    pa_dtype dtype;        // q and out
+    pa_dtype cache_dtype;  // the pools: dtype, or PA_FP8_E4M3
+    const float *k_scale;  // FP8 pools: device scalars (NULL = 1)
+    const float *v_scale;
     void *out;
     void *ws;
     size_t ws_bytes;
@@ -77,10 +85,11 @@ int prefill_tau(const AttnArgs &a);
 pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream);
 pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream);
 
-// Encode a 3-D TMA map over one pool viewed as [NB*bs][Hkv][D] elements with a
-// box of D x 1 kv head x `box_rows` slots.
-bool encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv, int D,
-                     int box_rows);
+// Encode a 3-D TMA map over one pool viewed as [NB*bs][Hkv][D] elements of
+// `elt` bytes, with a box of min(128 bytes, a row) x 1 kv head x `box_rows`
+// slots and the swizzle that matches the box's row (128 or 64 bytes).
+bool encode_pool_map_swizzled(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv,
+                              int D, int elt, int box_rows);
 
 // ---------------------------------------------------------------------------
 // Device side

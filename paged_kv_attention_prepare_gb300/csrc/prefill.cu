@@ -704,6 +704,8 @@ int prefill_tau(const AttnArgs &a) {
     const int G = a.Hq / a.Hkv;
     // The tensor-core kernel takes the row max of unscaled scores: scale > 0.
     if ((a.D != 64 && a.D != 128) || G < 1 || 128 % G != 0 || !(a.scale > 0.f)) return INT_MAX;
+    // FP8 pools: every request on the split-K kernel (its MMAs widen E4M3).
+    if (a.cache_dtype != a.dtype) return INT_MAX;
     return prefill::kTauDefault;
 }
 

@@ -36,7 +36,10 @@ def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda"):
     vc = vals["value_cache"].to(dev).clone()
     key = vals["key"].to(dev) if vals["key"].device.type != "cuda" else vals["key"]
     value = vals["value"].to(dev) if vals["value"].device.type != "cuda" else vals["value"]
-    pa.pa_cache_write(key, value, kc, vc, out["slot_mapping"])
+    ks, vs = vals.get("k_scale"), vals.get("v_scale")   # FP8 pools only
+    if ks is not None:
+        ks, vs = ks.to(dev), vs.to(dev)
+    pa.pa_cache_write(key, value, kc, vc, out["slot_mapping"], k_scale=ks, v_scale=vs)
     q = vals["q"].to(dev).contiguous()
     o = torch.full_like(q, float("nan"))
     if workspace_bytes is None:
@@ -46,7 +49,7 @@ def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda"):
     ws = torch.empty(max(int(workspace_bytes), 1), dtype=torch.uint8, device=dev)
     pa.pa_attention(q, kc, vc, bt, out["query_start_loc"][: R + 1], out["seq_lens"],
                     w.max_query_len, w.max_seq_len, w.scale, o,
-                    ws if workspace_bytes else None)
+                    ws if workspace_bytes else None, k_scale=ks, v_scale=vs)
     status, detail = pa.pa_get_status()
     res = {k: v.cpu().numpy() for k, v in out.items()}
     res.update(key_cache=kc, value_cache=vc, out=o, status=status, detail=detail)

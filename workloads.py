@@ -20,6 +20,9 @@ Recipe (the same for every named workload):
 * Values: every element of q, the new tokens' key/value and the whole cache
   pool is N(0, 1) drawn by a seeded ``torch.Generator`` on the requested
   device, rounded to bf16 / fp16 (round to nearest even).
+* FP8 pools (the ``*_fp8`` workloads, scales 0.25 for K and 0.125 for V):
+  N(0,1) / scale rounded by PyTorch's float8_e4m3fn conversion, so the cached
+  values (element * scale) are about N(0,1).
 * Request state for the rest of input preparation: a token buffer of random
   ids (vocabulary 128,256), each request's total known token count (caught
   up or mid-prompt, half each) and draft counts for speculative decoding
@@ -94,12 +97,12 @@ class Workload:
 
     def kv_read_bytes(self) -> int:
         """Bytes of K and V context every request's attention reads (logical)."""
-        elt = 2
+        elt = 1 if self.kv_cache_dtype == "fp8_e4m3" else 2
         return int(self.context_lens.sum()) * 2 * self.num_kv_heads * self.head_dim * elt
 
     def kv_unique_bytes(self) -> int:
         """Bytes of K and V in the distinct blocks the tables reference."""
-        elt = 2
+        elt = 1 if self.kv_cache_dtype == "fp8_e4m3" else 2
         return (self.unique_blocks * self.block_size * 2 * self.num_kv_heads
                 * self.head_dim * elt)
 
@@ -206,12 +209,20 @@ def shared_prefix(seed: int = 4) -> Workload:
                     _tables(rows), nb, bs, 32, 8, 128, "bf16", needed)
 
 
+def fp8(w: Workload, k_scale: float = 0.25, v_scale: float = 0.125) -> Workload:
+    """The same step over FP8 (E4M3) pools with per-pool scales."""
+    return dataclasses.replace(w, name=w.name + "_fp8", kv_cache_dtype="fp8_e4m3",
+                               k_scale=k_scale, v_scale=v_scale)
+
+
 NAMED = {
     "tiny": tiny,
     "decode": decode_batch,
     "mixed": mixed_step,
     "mha": mha_decode,
     "shared_prefix": shared_prefix,
+    "decode_fp8": lambda seed=1: fp8(decode_batch(seed)),
+    "mixed_fp8": lambda seed=2: fp8(mixed_step(seed)),
 }
 
 
@@ -332,6 +343,26 @@ def make_values(w: Workload, seed: int = 0, device="cpu", fused_qkv: bool = Fals
         out["key"] = _randn((max(t, 1), hkv, d), gen, dev, dt)[:t]
         out["value"] = _randn((max(t, 1), hkv, d), gen, dev, dt)[:t]
     shape = (w.num_blocks, w.block_size, hkv, d)
-    out["key_cache"] = _randn(shape, gen, dev, dt)
-    out["value_cache"] = _randn(shape, gen, dev, dt)
+    if w.kv_cache_dtype == "fp8_e4m3":
+        out["key_cache"] = _randn_fp8(shape, gen, dev, w.k_scale)
+        out["value_cache"] = _randn_fp8(shape, gen, dev, w.v_scale)
+        out["k_scale"] = torch.tensor([w.k_scale], dtype=torch.float32, device=dev)
+        out["v_scale"] = torch.tensor([w.v_scale], dtype=torch.float32, device=dev)
+    else:
+        out["key_cache"] = _randn(shape, gen, dev, dt)
+        out["value_cache"] = _randn(shape, gen, dev, dt)
+    return out
+
+
+def _randn_fp8(shape, gen: torch.Generator, device, scale: float, chunk_elems: int = 1 << 27):
+    """Bytes of an FP8 (E4M3) pool whose cached values (element * scale) are
+    about N(0, 1): N(0,1) / scale converted by PyTorch's float8_e4m3fn."""
+    out = torch.empty(shape, dtype=torch.uint8, device=device)
+    flat = out.view(shape[0], -1)
+    row = flat.shape[1]
+    step = max(1, chunk_elems // max(row, 1))
+    for i in range(0, shape[0], step):
+        j = min(shape[0], i + step)
+        x = torch.randn((j - i, row), generator=gen, device=device, dtype=torch.float32)
+        flat[i:j] = (x / scale).to(torch.float8_e4m3fn).view(torch.uint8)
     return out
