@@ -104,8 +104,12 @@ template <typename TQ> struct MmaIn<TQ, Fp8E4M3> { using type = __half; };
 template <typename TC, int D, int RPI>
 struct Cfg {
     using L = Lay<TC, D>;
+    // Pages per ring stage: an FP8 page is half the bytes of a 16-bit one, so
+    // two consecutive pages of a request share a stage and one handoff.
+    static constexpr int kSP = L::E == 1 ? 2 : 1;
+    static constexpr int kUnitBytes = kSP * L::kPageBytes;
     // 64 KB of pages in flight per CTA at head_dim 128
-    static constexpr int kStages = L::E == 1 ? 32 : 16;
+    static constexpr int kStages = 16;
     // Page pairs (K, V) are dealt round-robin to the consumer warps.  With
     // (kStages / 2) a multiple of the warp count, pair n always lands on stages
     // 2n mod kStages and 2n+1 mod kStages owned by warp n mod 4 alone, so every
@@ -114,7 +118,7 @@ struct Cfg {
     // tell the rounds apart).
     static_assert((kStages / 2) % kConsumerWarps == 0, "stages must split evenly among warps");
     static_assert((kStages & (kStages - 1)) == 0, "ring index arithmetic uses a power-of-two ring");
-    static constexpr int kStageBytes = kStages * L::kPageBytes;
+    static constexpr int kStageBytes = kStages * kUnitBytes;
     static constexpr int kComb = RPI * (D + 2);       // per warp: acc[row][D], m[row], l[row]
     static constexpr int kBytes = kStageBytes + kConsumerWarps * kComb * 4 +
                                   (2 * kStages + 2) * 8 + kCandidates * 8 + 1024;
@@ -406,9 +410,11 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
     if (warp == kConsumerWarps) {
         // =================== producer warp ===================
-        // Ring order: K page 0, V page 0, K page 1, V page 1, ... of each item.
-        // A page is L::NSUB swizzled boxes of 16 rows (one per 128 bytes of a
-        // row), landing back to back.
+        // Ring order: K unit 0, V unit 0, K unit 1, V unit 1, ... of each item,
+        // a unit being C::kSP consecutive pages of the request.  A page is
+        // L::NSUB swizzled boxes of 16 rows (one per 128 bytes of a row),
+        // landing back to back.
+        constexpr int kSP = C::kSP;
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -427,8 +433,11 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                     }
                 }
                 const int n = min(32, npages - g0);
-                for (int pg = 0; ok && pg < n; ++pg) {
-                    const int b = __shfl_sync(0xffffffffu, blk, pg);
+                for (int pu = 0; ok && pu < n; pu += kSP) {
+                    const int cnt = min(kSP, n - pu);   // pages in this unit
+                    int b[kSP];
+#pragma unroll
+                    for (int sp = 0; sp < kSP; ++sp) b[sp] = __shfl_sync(0xffffffffu, blk, min(pu + sp, 31));
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
                         if (lane == 0) {
@@ -436,12 +445,17 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                                 flag(p.status, PA_CHECK_TIMEOUT);
                                 ok = false;
                             } else {
-                                mbar_arrive_expect_tx(&full[stage], L::kPageBytes);
+                                mbar_arrive_expect_tx(&full[stage], cnt * L::kPageBytes);
 #pragma unroll
-                                for (int sub = 0; sub < L::NSUB; ++sub)
-                                    tma_load_3d(stages + stage * L::kPageBytes + sub * L::kSubBytes,
-                                                kv ? &p.tmV : &p.tmK, &full[stage],
-                                                sub * (L::SR / L::E), it.g, b * kPage);
+                                for (int sp = 0; sp < kSP; ++sp) {
+                                    if (sp >= cnt) break;
+#pragma unroll
+                                    for (int sub = 0; sub < L::NSUB; ++sub)
+                                        tma_load_3d(stages + stage * C::kUnitBytes + sp * L::kPageBytes +
+                                                        sub * L::kSubBytes,
+                                                    kv ? &p.tmV : &p.tmK, &full[stage],
+                                                    sub * (L::SR / L::E), it.g, b[sp] * kPage);
+                                }
                             }
                         }
                         if (++stage == kSt) {
@@ -562,21 +576,27 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         float m0 = -INFINITY, m1 = -INFINITY;   // reference max of rows 2tq, 2tq+1
         float l0 = 0.f, l1 = 0.f;               // this lane's share of the row sums
 
-        for (int pg = (warp - pair_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-             pg < npages; pg += kConsumerWarps) {
-            const uint32_t n2 = 2u * (uint32_t)(pair_base + pg);
+        constexpr int kSP = C::kSP;
+        const int nunits = (npages + kSP - 1) / kSP;
+        for (int pu = (warp - pair_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+             pu < nunits; pu += kConsumerWarps) {
+            const uint32_t n2 = 2u * (uint32_t)(pair_base + pu);
             const uint32_t stK = n2 & (kSt - 1), stV = (n2 + 1) & (kSt - 1);
             const uint32_t phK = (n2 / kSt) & 1u, phV = ((n2 + 1) / kSt) & 1u;
-            const int key0 = k0 + pg * kPage;
-            const bool page_visible = key0 + kPage - 1 <= lim_all;
-
-            // ---- S^T = K Q^T for the page's 16 keys
-            if (!mbar_wait_warp(&full[stK], phK)) {
+            if (!mbar_wait_warp(&full[stK], phK) || !mbar_wait_warp(&full[stV], phV)) {
                 flag(p.status, PA_CHECK_TIMEOUT);
                 ok = false;
                 break;
             }
-            const unsigned char *kpage = stages + stK * L::kPageBytes;
+#pragma unroll
+          for (int sp = 0; sp < kSP; ++sp) {
+            const int pg = pu * kSP + sp;
+            if (pg >= npages) break;
+            const int key0 = k0 + pg * kPage;
+            const bool page_visible = key0 + kPage - 1 <= lim_all;
+
+            // ---- S^T = K Q^T for the page's 16 keys
+            const unsigned char *kpage = stages + stK * C::kUnitBytes + sp * L::kPageBytes;
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int jj = 0; jj < NCH; ++jj) {
@@ -600,8 +620,6 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                     else Mma<TM>::run(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stK]);
             // sv: (key_a, row 2tq), (key_a, row 2tq+1), (key_b, row 2tq), (key_b, row 2tq+1)
             float sv[4];
 #pragma unroll
@@ -658,12 +676,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             const uint32_t pb1 = movmatrix_trans(Mma<TM>::pack(pv[2], pv[3]));
 
             // ---- O^T += V^T P^T
-            if (!mbar_wait_warp(&full[stV], phV)) {
-                flag(p.status, PA_CHECK_TIMEOUT);
-                ok = false;
-                break;
-            }
-            const unsigned char *vpage = stages + stV * L::kPageBytes;
+            const unsigned char *vpage = stages + stV * C::kUnitBytes + sp * L::kPageBytes;
             // Slots past the context hold stale data (maybe NaN): on a partial
             // page their V is zeroed in registers (their P is already 0).
             auto pv_page = [&](auto full_page) {
@@ -728,11 +741,15 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             };
             if (key0 + kPage <= k1) pv_page(std::true_type{});
             else pv_page(std::false_type{});
+          }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stV]);
+            if (lane == 0) {
+                mbar_arrive(&empty[stK]);
+                mbar_arrive(&empty[stV]);
+            }
         }
         if (!ok) break;
-        pair_base += npages;
+        pair_base += nunits;
 
         // ---- combine the four warps' states and write the item out
 #pragma unroll
