@@ -588,55 +588,70 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 ok = false;
                 break;
             }
+            // The unit's pages: QK of each (independent MMA chains), one
+            // softmax update over all their keys, then PV of each.
+            bool have[kSP];
+            int keyb[kSP];                 // first key of each page
+            float sv[kSP][4];              // (key_a, row 2tq), (key_a, 2tq+1), (key_b, 2tq), (key_b, 2tq+1)
 #pragma unroll
-          for (int sp = 0; sp < kSP; ++sp) {
-            const int pg = pu * kSP + sp;
-            if (pg >= npages) break;
-            const int key0 = k0 + pg * kPage;
-            const bool page_visible = key0 + kPage - 1 <= lim_all;
-
-            // ---- S^T = K Q^T for the page's 16 keys
-            const unsigned char *kpage = stages + stK * C::kUnitBytes + sp * L::kPageBytes;
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int jj = 0; jj < NCH; ++jj) {
-                const uint4 ka = *reinterpret_cast<const uint4 *>(kpage + koff(koff_a, jj));
-                const uint4 kb = *reinterpret_cast<const uint4 *>(kpage + koff(koff_b, jj));
-                const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
-#pragma unroll
-                for (int sub = 0; sub < KPC; ++sub) {
-                    const int s = jj * KPC + sub;
-                    uint32_t a0, a1, a2, a3;
-                    if constexpr (L::E == 2) {
-                        a0 = wa[2 * sub];
-                        a1 = wb[2 * sub];
-                        a2 = wa[2 * sub + 1];
-                        a3 = wb[2 * sub + 1];
-                    } else {
-                        e4m3x4_to_f16x4(wa[sub], a0, a2);
-                        e4m3x4_to_f16x4(wb[sub], a1, a3);
-                    }
-                    if (s & 1) Mma<TM>::run(sb, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-                    else Mma<TM>::run(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
-                }
+            for (int sp = 0; sp < kSP; ++sp) {
+                have[sp] = pu * kSP + sp < npages;
+                keyb[sp] = k0 + (pu * kSP + sp) * kPage;
             }
-            // sv: (key_a, row 2tq), (key_a, row 2tq+1), (key_b, row 2tq), (key_b, row 2tq+1)
-            float sv[4];
+            // ---- S^T = K Q^T for each page's 16 keys
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sv[e] = (sa[e] + sb[e]) * qs;
+            for (int sp = 0; sp < kSP; ++sp) {
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                if (have[sp]) {
+                    const unsigned char *kpage = stages + stK * C::kUnitBytes + sp * L::kPageBytes;
+#pragma unroll
+                    for (int jj = 0; jj < NCH; ++jj) {
+                        const uint4 ka = *reinterpret_cast<const uint4 *>(kpage + koff(koff_a, jj));
+                        const uint4 kb = *reinterpret_cast<const uint4 *>(kpage + koff(koff_b, jj));
+                        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+                        for (int sub = 0; sub < KPC; ++sub) {
+                            const int s = jj * KPC + sub;
+                            uint32_t a0, a1, a2, a3;
+                            if constexpr (L::E == 2) {
+                                a0 = wa[2 * sub];
+                                a1 = wb[2 * sub];
+                                a2 = wa[2 * sub + 1];
+                                a3 = wb[2 * sub + 1];
+                            } else {
+                                e4m3x4_to_f16x4(wa[sub], a0, a2);
+                                e4m3x4_to_f16x4(wb[sub], a1, a3);
+                            }
+                            if (s & 1) Mma<TM>::run(sb, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                            else Mma<TM>::run(sa, a0, a1, a2, a3, qf[s][0], qf[s][1]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sv[sp][e] = have[sp] ? (sa[e] + sb[e]) * qs : -INFINITY;
+            }
+            const bool unit_visible = keyb[kSP - 1] + kPage - 1 <= lim_all && have[kSP - 1];
 
             // ---- online softmax with a lazily moved reference max: P stays
             //      below 2^8, so the 16-bit P and the f32 sums are exact enough,
             //      and O is rescaled only when a row's max grows by more than 8
             //      (in log2 units).
-            if (!page_visible) {
-                const int pa = key0 + key_a, pb = key0 + key_b;
-                sv[0] = pa <= lim0 ? sv[0] : -INFINITY;
-                sv[1] = pa <= lim1 ? sv[1] : -INFINITY;
-                sv[2] = pb <= lim0 ? sv[2] : -INFINITY;
-                sv[3] = pb <= lim1 ? sv[3] : -INFINITY;
+            if (!unit_visible) {
+#pragma unroll
+                for (int sp = 0; sp < kSP; ++sp) {
+                    const int pa = keyb[sp] + key_a, pb = keyb[sp] + key_b;
+                    sv[sp][0] = pa <= lim0 ? sv[sp][0] : -INFINITY;
+                    sv[sp][1] = pa <= lim1 ? sv[sp][1] : -INFINITY;
+                    sv[sp][2] = pb <= lim0 ? sv[sp][2] : -INFINITY;
+                    sv[sp][3] = pb <= lim1 ? sv[sp][3] : -INFINITY;
+                }
             }
-            float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+            float mx0 = fmaxf(sv[0][0], sv[0][2]), mx1 = fmaxf(sv[0][1], sv[0][3]);
+#pragma unroll
+            for (int sp = 1; sp < kSP; ++sp) {
+                mx0 = fmaxf(mx0, fmaxf(sv[sp][0], sv[sp][2]));
+                mx1 = fmaxf(mx1, fmaxf(sv[sp][1], sv[sp][3]));
+            }
 #pragma unroll
             for (int x = 4; x < 32; x <<= 1) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
@@ -658,24 +673,33 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 l0 *= al0;
                 l1 *= al1;
             }
-            float pv[4];
-            if (page_visible) {
-                pv[0] = fast_exp2(sv[0] - m0);
-                pv[1] = fast_exp2(sv[1] - m1);
-                pv[2] = fast_exp2(sv[2] - m0);
-                pv[3] = fast_exp2(sv[3] - m1);
-            } else {
-                pv[0] = m0 == -INFINITY ? 0.f : fast_exp2(sv[0] - m0);
-                pv[1] = m1 == -INFINITY ? 0.f : fast_exp2(sv[1] - m1);
-                pv[2] = m0 == -INFINITY ? 0.f : fast_exp2(sv[2] - m0);
-                pv[3] = m1 == -INFINITY ? 0.f : fast_exp2(sv[3] - m1);
+            uint32_t pb[kSP][2];
+#pragma unroll
+            for (int sp = 0; sp < kSP; ++sp) {
+                float pv[4];
+                if (unit_visible) {
+                    pv[0] = fast_exp2(sv[sp][0] - m0);
+                    pv[1] = fast_exp2(sv[sp][1] - m1);
+                    pv[2] = fast_exp2(sv[sp][2] - m0);
+                    pv[3] = fast_exp2(sv[sp][3] - m1);
+                } else {
+                    pv[0] = m0 == -INFINITY ? 0.f : fast_exp2(sv[sp][0] - m0);
+                    pv[1] = m1 == -INFINITY ? 0.f : fast_exp2(sv[sp][1] - m1);
+                    pv[2] = m0 == -INFINITY ? 0.f : fast_exp2(sv[sp][2] - m0);
+                    pv[3] = m1 == -INFINITY ? 0.f : fast_exp2(sv[sp][3] - m1);
+                }
+                l0 += pv[0] + pv[2];
+                l1 += pv[1] + pv[3];
+                pb[sp][0] = movmatrix_trans(Mma<TM>::pack(pv[0], pv[1]));
+                pb[sp][1] = movmatrix_trans(Mma<TM>::pack(pv[2], pv[3]));
             }
-            l0 += pv[0] + pv[2];
-            l1 += pv[1] + pv[3];
-            const uint32_t pb0 = movmatrix_trans(Mma<TM>::pack(pv[0], pv[1]));
-            const uint32_t pb1 = movmatrix_trans(Mma<TM>::pack(pv[2], pv[3]));
 
-            // ---- O^T += V^T P^T
+            // ---- O^T += V^T P^T, page by page
+#pragma unroll
+            for (int sp = 0; sp < kSP; ++sp) {
+            if (!have[sp]) break;
+            const int key0 = keyb[sp];
+            const uint32_t pb0 = pb[sp][0], pb1 = pb[sp][1];
             const unsigned char *vpage = stages + stV * C::kUnitBytes + sp * L::kPageBytes;
             // Slots past the context hold stale data (maybe NaN): on a partial
             // page their V is zeroed in registers (their P is already 0).
