@@ -29,6 +29,13 @@
 // Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM allocation), 2..5 = slot A
 // softmax and epilogue, 6..9 = slot B; warp w reads TMEM lanes 32*(w%4)..+31.
 // Every mbarrier wait is bounded.
+//
+// FP8 (E4M3) pools, head_dim 128: the MMAs run in f16 (E4M3 widens to f16
+// exactly; a bf16 q is rounded to f16).  Each FP8 page lands (one 128-byte
+// row per slot, swizzled) in the upper half of its f16 tile buffer, where
+// an FP8 row takes exactly the bytes of its own upper-half f16 row; two more
+// warps (10, 11) widen the tile in place, row by row, and only then signal
+// the tile full.  K's scale joins the softmax scale, V's scales the output.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -45,7 +52,10 @@ constexpr int kBN = 128;          // keys per KV tile
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kBN / kPage;
 constexpr int kSoftmaxWarps = 8;   // four per slot
-constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
+constexpr int kConvWarps = 2;      // FP8 pools: widening E4M3 -> f16 in shared memory
+__host__ __device__ constexpr int threads_for(bool f8) {
+    return (2 + kSoftmaxWarps + (f8 ? kConvWarps : 0)) * 32;
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kTauDefault = 16;           // longer query chunks take this kernel
@@ -61,6 +71,7 @@ struct Params {
     int R, T, MB, NB, Hq, Hkv, G;
     int tau;        // requests with more than tau query tokens are handled here
     float qscale;   // softmax scale * log2(e)
+    const float *k_scale, *v_scale;   // FP8 pools (device scalars; NULL = 1)
     unsigned int *status;
 };
 
@@ -86,6 +97,8 @@ enum {
     B_ODONE = B_PFULL + 2,   // [2] per slot: PV_X done
     B_OFREE = B_ODONE + 2,   // [2] per slot: O_X read out by the epilogue
     B_DRAIN = B_OFREE + 2,
+    B_QLAND,      // FP8 pools: TMA bytes landed, before widening
+    B_KLAND, B_KLAND1, B_VLAND, B_VLAND1,
     B_COUNT
 };
 
@@ -270,9 +283,64 @@ __device__ __forceinline__ int slot_tiles(const Params &p, const Item &it, int s
     return (max_pos + kBN) / kBN;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid_constant__ Params p) {
+// Widen the E4M3 rows [r0, r1) of a 128-row tile in place: the FP8 tile sits
+// in the upper 64-dim half (row r at half1 + 128 r, 128-byte swizzle); each
+// row becomes two f16 rows (dims 0-63 in the lower half, 64-127 in the upper),
+// same swizzle.  A warp reads 16 rows whole (four 16-byte loads in flight per
+// lane) before it writes them; r1 - r0 is a multiple of 16.
+__device__ __forceinline__ void widen_e4m3_tile(unsigned char *tile, int half_bytes, int r0, int r1,
+                                                int lane) {
+    const int c = lane & 7;                 // 16 dims 16c .. 16c+15 of the row
+    const int fc = 2 * (c & 3);             // f16 chunks fc, fc+1 of a half row
+    for (int rb = r0; rb < r1; rb += 16) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = rb + 4 * u + (lane >> 3);
+            v[u] = *reinterpret_cast<const uint4 *>(tile + half_bytes + r * 128 + ((c ^ (r & 7)) << 4));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = rb + 4 * u + (lane >> 3), x = r & 7;
+            uint32_t h[8];
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                asm("{\n.reg .b16 l, hh;\nmov.b32 {l, hh}, %2;\n"
+                    "cvt.rn.f16x2.e4m3x2 %0, l;\ncvt.rn.f16x2.e4m3x2 %1, hh;\n}"
+                    : "=r"(h[2 * e]), "=r"(h[2 * e + 1])
+                    : "r"(w[e]));
+            }
+            unsigned char *dst_row = tile + (c >> 2) * half_bytes + r * 128;
+            *reinterpret_cast<uint4 *>(dst_row + ((fc ^ x) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(dst_row + (((fc + 1) ^ x) << 4)) =
+                make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        __syncwarp();
+    }
+}
+
+// Round a bf16 tile to f16 in place (same positions, same swizzle).
+__device__ __forceinline__ void bf16_tile_to_f16(unsigned char *tile, int bytes, int t, int nt) {
+    for (int o = t * 16; o < bytes; o += nt * 16) {
+        uint4 v = *reinterpret_cast<const uint4 *>(tile + o);
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(w[e] << 16),
+                                                __uint_as_float(w[e] & 0xffff0000u));
+            w[e] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        *reinterpret_cast<uint4 *>(tile + o) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <typename T, int D, bool F8>
+__global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const __grid_constant__ Params p) {
     using C = Cfg<D>;
+    using TM = typename std::conditional<F8, __half, T>::type;   // the MMAs' input type
+    static_assert(!F8 || D == 128, "FP8 pools: head_dim 128");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -295,7 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i) {
             const bool per_warp = (i >= B_PFULL && i < B_PFULL + 2) || (i >= B_OFREE && i < B_OFREE + 2);
-            mbar_init(&bar[i], per_warp ? kSoftmaxWarps / 2 : 1);
+            // FP8: Q/K/V full are signalled by the widening warps
+            const bool widened = F8 && (i == B_QFULL || (i >= B_KFULL && i <= B_KFULL1) ||
+                                        (i >= B_VFULL && i <= B_VFULL1));
+            mbar_init(&bar[i], per_warp ? kSoftmaxWarps / 2 : (widened ? kConvWarps : 1));
         }
         fence_mbar_init();
         prefetch_tensor_map(&p.tmQ);
@@ -331,13 +402,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                 if (!mbar_wait(&bar[B_QEMPTY], (items & 1) ^ 1)) ok = false;
                 else {
                     const int nslots = ntB > 0 ? 2 : 1;
-                    mbar_arrive_expect_tx(&bar[B_QFULL], nslots * C::kQBytes);
+                    uint64_t *qb = &bar[F8 ? B_QLAND : B_QFULL];
+                    mbar_arrive_expect_tx(qb, nslots * C::kQBytes);
                     for (int sl = 0; sl < nslots; ++sl) {
                         const int tok0 = it.qstart + (it.mt * 2 + sl) * (kBM / p.G);
 #pragma unroll
                         for (int h = 0; h < C::kHalves; ++h)
-                            tma_load_3d(sQ + sl * C::kQBytes + h * (kBM * 128), &p.tmQ,
-                                        &bar[B_QFULL], h * 64, it.g * p.G, tok0);
+                            tma_load_3d(sQ + sl * C::kQBytes + h * (kBM * 128), &p.tmQ, qb, h * 64,
+                                        it.g * p.G, tok0);
                     }
                 }
             }
@@ -355,10 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                 }
                 const int st = (int)(t & 1);
                 const uint32_t ph = (uint32_t)((t >> 1) & 1);
-                const uint32_t bytes = (uint32_t)npg * C::kHalves * C::kPageHalfBytes;
+                // FP8: one 128-byte row per slot, into the tile's upper half
+                const uint32_t bytes = F8 ? (uint32_t)npg * kPage * 128
+                                          : (uint32_t)npg * C::kHalves * C::kPageHalfBytes;
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv) {
-                    uint64_t *fullb = &bar[(kv ? B_VFULL : B_KFULL) + st];
+                    uint64_t *fullb = &bar[(F8 ? (kv ? B_VLAND : B_KLAND) : (kv ? B_VFULL : B_KFULL)) + st];
                     uint64_t *emptyb = &bar[(kv ? B_VEMPTY : B_KEMPTY) + st];
                     unsigned char *dst = (kv ? sV : sK) + st * C::kTileBytes;
                     if (lane == 0) {
@@ -368,10 +442,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     if (lane < npg) {
+                        if constexpr (F8) {
+                            tma_load_3d(dst + C::kHalfBytes + lane * kPage * 128, kv ? &p.tmV : &p.tmK,
+                                        fullb, 0, it.g, blk * kPage);
+                        } else {
 #pragma unroll
-                        for (int h = 0; h < C::kHalves; ++h)
-                            tma_load_3d(dst + h * C::kHalfBytes + lane * C::kPageHalfBytes,
-                                        kv ? &p.tmV : &p.tmK, fullb, h * 64, it.g, blk * kPage);
+                            for (int h = 0; h < C::kHalves; ++h)
+                                tma_load_3d(dst + h * C::kHalfBytes + lane * C::kPageHalfBytes,
+                                            kv ? &p.tmV : &p.tmK, fullb, h * 64, it.g, blk * kPage);
+                        }
                     }
                     if (kv) lastV = t; else lastK = t;
                 }
@@ -381,13 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
         if (!ok) fail();
         // Drain: the last copies issued into each ring must have landed.
         if (lane == 0) {
-            if (lastK >= 0) mbar_wait(&bar[B_KFULL + (int)(lastK & 1)], (uint32_t)((lastK >> 1) & 1));
-            if (lastV >= 0) mbar_wait(&bar[B_VFULL + (int)(lastV & 1)], (uint32_t)((lastV >> 1) & 1));
+            const int kf = F8 ? B_KLAND : B_KFULL, vf = F8 ? B_VLAND : B_VFULL;
+            if (lastK >= 0) mbar_wait(&bar[kf + (int)(lastK & 1)], (uint32_t)((lastK >> 1) & 1));
+            if (lastV >= 0) mbar_wait(&bar[vf + (int)(lastV & 1)], (uint32_t)((lastV >> 1) & 1));
         }
     } else if (warp == 1) {
         // =================== MMA issuer ===================
-        const uint32_t idQK = instr_desc<T>(kBM, kBN, 0);
-        const uint32_t idPV = instr_desc<T>(kBM, D, 1);
+        const uint32_t idQK = instr_desc<TM>(kBM, kBN, 0);
+        const uint32_t idPV = instr_desc<TM>(kBM, D, 1);
         long long t0 = 0;           // KV tiles of earlier items
         long long cnt[2] = {0, 0};  // tiles processed per slot (barrier phases)
         int its[2] = {0, 0};        // items processed per slot
@@ -477,6 +557,47 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
             mma_commit(&bar[B_DRAIN]);
             mbar_wait(&bar[B_DRAIN], 0);
         }
+    } else if (warp >= 2 + kSoftmaxWarps) {
+        // =================== FP8: widen landed tiles to f16 (warps 10, 11) ===================
+        if constexpr (F8) {
+            const int cw = warp - (2 + kSoftmaxWarps);   // rows 64 cw .. 64 cw + 63 of each tile
+            long long t = 0;
+            int items = 0;
+            bool ok = true;
+            for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k, ++items) {
+                const int ntB = slot_tiles(p, it, 1);
+                const int nt = max(slot_tiles(p, it, 0), ntB);
+                if (!mbar_wait_warp(&bar[B_QLAND], items & 1)) {
+                    ok = false;
+                    break;
+                }
+                if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                    const int nslots = ntB > 0 ? 2 : 1;
+                    bf16_tile_to_f16(sQ, nslots * C::kQBytes, cw * 32 + lane, kConvWarps * 32);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_QFULL]);
+                for (int j = 0; ok && j < nt; ++j, ++t) {
+                    const int st = (int)(t & 1);
+                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
+                        if (!mbar_wait_warp(&bar[(kv ? B_VLAND : B_KLAND) + st], ph)) {
+                            ok = false;
+                            break;
+                        }
+                        widen_e4m3_tile((kv ? sV : sK) + st * C::kTileBytes, C::kHalfBytes, cw * 64,
+                                        cw * 64 + 64, lane);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[(kv ? B_VFULL : B_KFULL) + st]);
+                    }
+                }
+                if (*abort_flag) ok = false;
+            }
+            if (!ok) fail();
+        }
     } else {
         // =================== softmax + epilogue (warps 2..9) ===================
         const int slot = (warp - 2) >> 2;          // 0 = A, 1 = B
@@ -485,7 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
         const uint32_t lane_addr = (uint32_t)(sub * 32) << 16;
         const uint32_t colS = tmem + lane_addr + C::col_s(slot);
         const uint32_t colO = tmem + lane_addr + C::col_o(slot);
-        const float2 c2 = make_float2(p.qscale, p.qscale);
+        const float ks = (F8 && p.k_scale) ? *p.k_scale : 1.f;
+        const float vs = (F8 && p.v_scale) ? *p.v_scale : 1.f;
+        const float2 c2 = make_float2(p.qscale * ks, p.qscale * ks);
         long long cnt = 0;   // tiles this slot processed (barrier phases)
         long long t0 = 0;    // KV tiles of earlier items (V ring phases)
         bool ok = true;
@@ -576,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                         y.x = fast_exp2(y.x);
                         y.y = fast_exp2(y.y);
                         acc[e & 1] = __fadd2_rn(acc[e & 1], y);
-                        w[e] = Elt<T>::pack2(y.x, y.y);
+                        w[e] = Elt<TM>::pack2(y.x, y.y);
                     }
                     tmem_st32(colS + hh * 32, w);
                 }
@@ -619,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
                 break;
             }
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? vs / l : 0.f;
             T *dst = reinterpret_cast<T *>(p.out) +
                      ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + rr % p.G) * D;
 #pragma unroll
@@ -658,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const __grid
 // 3-D TMA map, 128-byte swizzle, 64-element inner box: q as [T][Hq][D] with a
 // {64, G, 128/G} box, or a pool as [NB*bs][Hkv][D] with a {64, 1, 16} box.
 bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
-                  uint32_t b1, uint32_t b2) {
+                  uint32_t b1, uint32_t b2, int elt = 2) {
     static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     if (!enc) {
         void *fn = nullptr;
@@ -670,29 +793,30 @@ bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, u
         enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-    const cuuint32_t box[3] = {64u, b1, b2};
+    const cuuint64_t strides[2] = {d0 * elt, d0 * d1 * elt};
+    const cuuint32_t box[3] = {128u / (cuuint32_t)elt, b1, b2};   // 128 bytes per box row
     const cuuint32_t es[3] = {1u, 1u, 1u};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(ptr), dims, strides, box,
+    return enc(map, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+               const_cast<void *>(ptr), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F8>
 pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) {
     using C = Cfg<D>;
     static bool configured[64] = {};
     int dev = 0;
     PA_TRY_CUDA(cudaGetDevice(&dev));
     if (dev >= 64 || !configured[dev]) {
-        PA_TRY_CUDA(cudaFuncSetAttribute(paged_prefill_kernel<T, D>,
+        PA_TRY_CUDA(cudaFuncSetAttribute(paged_prefill_kernel<T, D, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem));
         if (dev < 64) configured[dev] = true;
     }
     long long grid = num_sms();
     if (items < grid) grid = items;
     if (grid < 1) return PA_OK;
-    paged_prefill_kernel<T, D><<<(int)grid, kThreads, C::kSmem, stream>>>(prm);
+    paged_prefill_kernel<T, D, F8><<<(int)grid, threads_for(F8), C::kSmem, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
     return PA_OK;
@@ -704,8 +828,9 @@ int prefill_tau(const AttnArgs &a) {
     const int G = a.Hq / a.Hkv;
     // The tensor-core kernel takes the row max of unscaled scores: scale > 0.
     if ((a.D != 64 && a.D != 128) || G < 1 || 128 % G != 0 || !(a.scale > 0.f)) return INT_MAX;
-    // FP8 pools: every request on the split-K kernel (its MMAs widen E4M3).
-    if (a.cache_dtype != a.dtype) return INT_MAX;
+    // FP8 pools: the tensor-core kernel widens E4M3 tiles at head_dim 128;
+    // at 64 every request stays on the split-K kernel.
+    if (a.cache_dtype != a.dtype && a.D != 128) return INT_MAX;
     return prefill::kTauDefault;
 }
 
@@ -716,10 +841,14 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     memset(&prm, 0, sizeof prm);
     const int G = a.Hq / a.Hkv;
     const uint64_t slots = (uint64_t)a.NB * a.bs;
+    const bool f8 = a.cache_dtype == PA_FP8_E4M3;
+    const int elt = f8 ? 1 : 2;
     if (!encode_sw128(&prm.tmQ, a.q, a.D, a.Hq, a.T, G, kBM / G) ||
-        !encode_sw128(&prm.tmK, a.kc, a.D, a.Hkv, slots, 1, kPage) ||
-        !encode_sw128(&prm.tmV, a.vc, a.D, a.Hkv, slots, 1, kPage))
+        !encode_sw128(&prm.tmK, a.kc, a.D, a.Hkv, slots, 1, kPage, elt) ||
+        !encode_sw128(&prm.tmV, a.vc, a.D, a.Hkv, slots, 1, kPage, elt))
         return PA_ERR_CUDA;
+    prm.k_scale = a.k_scale;
+    prm.v_scale = a.v_scale;
     prm.out = a.out;
     prm.bt = a.bt;
     prm.qsl = a.qsl;
@@ -738,11 +867,14 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     // upper bound on the row tiles
     const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T * G + 2 * kBM - 1) / (2 * kBM));
     const bool bf16 = a.dtype == PA_BF16;
+    if (f8)   // head_dim 128 (prefill_tau keeps other FP8 shapes on the split-K kernel)
+        return bf16 ? launch_typed<__nv_bfloat16, 128, true>(prm, items, stream)
+                    : launch_typed<__half, 128, true>(prm, items, stream);
     if (a.D == 128)
-        return bf16 ? launch_typed<__nv_bfloat16, 128>(prm, items, stream)
-                    : launch_typed<__half, 128>(prm, items, stream);
-    return bf16 ? launch_typed<__nv_bfloat16, 64>(prm, items, stream)
-                : launch_typed<__half, 64>(prm, items, stream);
+        return bf16 ? launch_typed<__nv_bfloat16, 128, false>(prm, items, stream)
+                    : launch_typed<__half, 128, false>(prm, items, stream);
+    return bf16 ? launch_typed<__nv_bfloat16, 64, false>(prm, items, stream)
+                : launch_typed<__half, 64, false>(prm, items, stream);
 }
 
 }  // namespace pa
