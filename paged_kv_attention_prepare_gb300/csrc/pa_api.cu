@@ -304,8 +304,8 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens, int32_t
                                    int32_t max_seq_len, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_dim) {
     if (num_reqs <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
-    return decode_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len, num_q_heads,
-                                 num_kv_heads, head_dim);
+    return kCtrlBytes + decode_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len,
+                                              num_q_heads, num_kv_heads, head_dim);
 }
 
 pa_status pa_attention(const void *q, const void *key_cache, const void *value_cache,
@@ -371,8 +371,16 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
     a.k_scale = cache_dtype == PA_FP8_E4M3 ? k_scale : nullptr;
     a.v_scale = cache_dtype == PA_FP8_E4M3 ? v_scale : nullptr;
     a.out = out;
+    // The workspace starts with a small control block (the tensor-core
+    // kernel's item counter); the split-K partials take the rest.
+    a.ctrl = nullptr;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
+    if (workspace && workspace_bytes >= kCtrlBytes) {
+        a.ctrl = static_cast<unsigned int *>(workspace);
+        a.ws = static_cast<unsigned char *>(workspace) + kCtrlBytes;
+        a.ws_bytes = workspace_bytes - kCtrlBytes;
+    }
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int tau = prefill_tau(a);
     const pa_status r = launch_decode(a, tau, st);

@@ -73,9 +73,13 @@ struct AttnArgs {
     const float *k_scale;  // FP8 pools: device scalars (NULL = 1)
     const float *v_scale;
     void *out;
-    void *ws;
+    void *ws;              // decode partials (after the control block)
     size_t ws_bytes;
+    unsigned int *ctrl;    // control block at the workspace's start (NULL: none)
 };
+
+// Bytes at the start of a caller's workspace kept for per-call counters.
+constexpr size_t kCtrlBytes = 256;
 
 size_t decode_workspace_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq,
                              int32_t Hq, int32_t Hkv, int32_t D);

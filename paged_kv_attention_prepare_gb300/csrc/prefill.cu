@@ -72,6 +72,8 @@ struct Params {
     int tau;        // requests with more than tau query tokens are handled here
     float qscale;   // softmax scale * log2(e)
     const float *k_scale, *v_scale;   // FP8 pools (device scalars; NULL = 1)
+    unsigned int *item_counter;       // zeroed before launch: items are taken in order
+                                      // as CTAs free up (NULL: fixed snake order)
     unsigned int *status;
 };
 
@@ -99,8 +101,11 @@ enum {
     B_DRAIN = B_OFREE + 2,
     B_QLAND,      // FP8 pools: TMA bytes landed, before widening
     B_KLAND, B_KLAND1, B_VLAND, B_VLAND1,
-    B_COUNT
+    B_IFULL,                      // [kQueue] item queue entry written by the producer
+    B_IEMPTY = B_IFULL + 4,       // [kQueue] entry read by every other warp
+    B_COUNT = B_IEMPTY + 4
 };
+constexpr int kQueue = 4;         // items the producer may run ahead
 
 // ---------------------------------------------------------------------------
 // tcgen05 / TMA wrappers
@@ -350,6 +355,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
     uint64_t *bar = reinterpret_cast<uint64_t *>(sV + 2 * C::kTileBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *q_items = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [kQueue]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -366,7 +372,9 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
             // FP8: Q/K/V full are signalled by the widening warps
             const bool widened = F8 && (i == B_QFULL || (i >= B_KFULL && i <= B_KFULL1) ||
                                         (i >= B_VFULL && i <= B_VFULL1));
-            mbar_init(&bar[i], per_warp ? kSoftmaxWarps / 2 : (widened ? kConvWarps : 1));
+            const bool readers = i >= B_IEMPTY && i < B_IEMPTY + kQueue;   // every warp but 0
+            mbar_init(&bar[i], readers ? 1 + kSoftmaxWarps + (F8 ? kConvWarps : 0)
+                                       : per_warp ? kSoftmaxWarps / 2 : (widened ? kConvWarps : 1));
         }
         fence_mbar_init();
         prefetch_tensor_map(&p.tmQ);
@@ -386,6 +394,44 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         flag(p.status, PA_CHECK_TIMEOUT);
         *abort_flag = 1;
     };
+    // The k-th item of this CTA, as every warp but the producer sees it:
+    // with an item counter, the index the producer published in queue entry
+    // k % kQueue (-1: no more items); otherwise the fixed snake order.
+    auto item_at = [&](int k) -> long long {
+        if (!p.item_counter) return snake_item(k);
+        const int e = k % kQueue;
+        if (!mbar_wait_warp(&bar[B_IFULL + e], (uint32_t)((k / kQueue) & 1))) {
+            if (lane == 0) fail();
+            return -1;
+        }
+        const long long v = q_items[e];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[B_IEMPTY + e]);
+        return v;
+    };
+    // The producer's k-th item: the next index from the counter (the list is
+    // heaviest first, so CTAs that free up early take the next heaviest),
+    // published for the other warps.  False when the list is done (or a wait
+    // timed out; *timed_out tells which).
+    auto next_item = [&](int k, bool *timed_out) -> bool {
+        *timed_out = false;
+        if (!p.item_counter) return walk.find(snake_item(k), lane, it);
+        unsigned int cand = 0;
+        if (lane == 0) cand = atomicAdd(p.item_counter, 1u);
+        cand = __shfl_sync(0xffffffffu, cand, 0);
+        const bool valid = walk.find((long long)cand, lane, it);
+        const int e = k % kQueue;
+        if (!mbar_wait_warp(&bar[B_IEMPTY + e], (uint32_t)(((k / kQueue) & 1) ^ 1))) {
+            *timed_out = true;
+            return false;
+        }
+        if (lane == 0) {
+            q_items[e] = valid ? (int)cand : -1;
+            mbar_arrive(&bar[B_IFULL + e]);
+        }
+        __syncwarp();
+        return valid;
+    };
 
     if (warp == 0) {
         // =================== TMA producer ===================
@@ -393,7 +439,12 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         int items = 0;
         bool ok = true;
         long long lastK = -1, lastV = -1;
-        for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k, ++items) {
+        for (int k = 0; ok; ++k, ++items) {
+            bool timed_out = false;
+            if (!next_item(k, &timed_out)) {
+                if (timed_out) ok = false;
+                break;
+            }
             const int ntB = slot_tiles(p, it, 1);
             const int nt = max(slot_tiles(p, it, 0), ntB);
             const int32_t *row = p.bt + (long long)it.r * p.MB;
@@ -473,7 +524,9 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         int its[2] = {0, 0};        // items processed per slot
         int items = 0;
         bool ok = true;
-        for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k, ++items) {
+        for (int k = 0; ok; ++k, ++items) {
+            const long long ik = item_at(k);
+            if (ik < 0 || !walk.find(ik, lane, it)) break;
             int ns[2] = {slot_tiles(p, it, 0), slot_tiles(p, it, 1)};
             const int nt = max(ns[0], ns[1]);
             if (lane == 0) {
@@ -564,7 +617,9 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
             long long t = 0;
             int items = 0;
             bool ok = true;
-            for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k, ++items) {
+            for (int k = 0; ok; ++k, ++items) {
+                const long long ik = item_at(k);
+                if (ik < 0 || !walk.find(ik, lane, it)) break;
                 const int ntB = slot_tiles(p, it, 1);
                 const int nt = max(slot_tiles(p, it, 0), ntB);
                 if (!mbar_wait_warp(&bar[B_QLAND], items & 1)) {
@@ -612,7 +667,9 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         long long cnt = 0;   // tiles this slot processed (barrier phases)
         long long t0 = 0;    // KV tiles of earlier items (V ring phases)
         bool ok = true;
-        for (int k = 0; ok && walk.find(snake_item(k), lane, it); ++k) {
+        for (int k = 0; ok; ++k) {
+            const long long ik = item_at(k);
+            if (ik < 0 || !walk.find(ik, lane, it)) break;
             const int ntS = slot_tiles(p, it, slot);
             const int nt = max(slot_tiles(p, it, 0), slot_tiles(p, it, 1));
             if (ntS == 0) {
@@ -849,6 +906,10 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
         return PA_ERR_CUDA;
     prm.k_scale = a.k_scale;
     prm.v_scale = a.v_scale;
+    if (a.ctrl) {   // items in order as CTAs free up: the counter starts at 0
+        PA_TRY_CUDA(cudaMemsetAsync(a.ctrl, 0, sizeof(unsigned int), stream));
+        prm.item_counter = a.ctrl;
+    }
     prm.out = a.out;
     prm.bt = a.bt;
     prm.qsl = a.qsl;
