@@ -96,7 +96,7 @@ enum {
     B_VEMPTY, B_VEMPTY1,
     B_SFULL,      // [2] per slot: S_X ready
     B_PFULL = B_SFULL + 2,   // [2] per slot: P_X written (one arrive per softmax warp)
-    B_ODONE = B_PFULL + 2,   // [2] per slot: PV_X done
+    B_ODONE = B_PFULL + 2,   // [2] per slot: the item's last PV_X done
     B_OFREE = B_ODONE + 2,   // [2] per slot: O_X read out by the epilogue
     B_DRAIN = B_OFREE + 2,
     B_QLAND,      // FP8 pools: TMA bytes landed, before widening
@@ -538,12 +538,16 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 auto issue_qk = [&](int slot, int kst) {
                     const uint32_t qa = q0 + slot * C::kQBytes;
                     const uint32_t ka = smem_u32(sK + kst * C::kTileBytes);
+                    const uint64_t dq0 = smem_desc_sw128(qa, 16, 1024);
+                    const uint64_t dk0 = smem_desc_sw128(ka, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                         const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-                        mma_ss(tmem + C::col_s(slot), smem_desc_sw128(qa + off, 16, 1024),
-                               smem_desc_sw128(ka + koff, 16, 1024), idQK, kk > 0);
+                        // descriptors differ only in the start address (16-byte
+                        // units, a 14-bit field that never carries here)
+                        mma_ss(tmem + C::col_s(slot), dq0 + (off >> 4), dk0 + (koff >> 4), idQK,
+                               kk > 0);
                     }
                     mma_commit(&bar[B_SFULL + slot]);
                 };
@@ -570,13 +574,17 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                         if (j == 0 && !wait_or_fail(&bar[B_OFREE + sl], (uint32_t)((its[sl] & 1) ^ 1)))
                             break;
                         tc_fence_after();
-                        const uint32_t v0 = smem_u32(sV + st * C::kTileBytes);
+                        const uint64_t dv0 = smem_desc_sw128(smem_u32(sV + st * C::kTileBytes),
+                                                             C::kHalfBytes, 1024);
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk)
                             mma_ts(tmem + C::col_o(sl), tmem + C::col_s(sl) + 8 * kk,
-                                   smem_desc_sw128(v0 + kk * 2048, C::kHalfBytes, 1024), idPV,
+                                   dv0 + (uint64_t)(kk * 2048 >> 4), idPV,
                                    (j > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(&bar[B_ODONE + sl]);
+                        // O_X is read only by the epilogue, after the item's last
+                        // PV; a rescale before that is ordered by S_FULL, whose
+                        // commit covers every earlier MMA of this thread.
+                        if (j + 1 == ns[sl]) mma_commit(&bar[B_ODONE + sl]);
                         ++cnt[sl];
                         if (j + 1 < ns[sl]) {
                             if (!k_next_ready &&
@@ -666,6 +674,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         const float2 c2 = make_float2(p.qscale * ks, p.qscale * ks);
         long long cnt = 0;   // tiles this slot processed (barrier phases)
         long long t0 = 0;    // KV tiles of earlier items (V ring phases)
+        int items_done = 0;  // items this slot finished (O_DONE phases)
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const long long ik = item_at(k);
@@ -711,12 +720,8 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2.x;
                 const bool need = mx > m_ref + kRescaleThreshold;
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    // O holds PV of tiles < j (all complete once S_j is): rescale.
-                    if (!mbar_wait_warp(&bar[B_ODONE + slot], (uint32_t)((cnt - 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    // O holds PV of tiles < j, all complete: S_j's commit (waited
+                    // above) covers every MMA issued before it.  Rescale.
                     const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
 #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
@@ -793,11 +798,12 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 if (lane == 0) mbar_arrive(&bar[B_PFULL + slot]);
             }
             if (!ok) break;
-            // ---- epilogue: O / l for this row
-            if (!mbar_wait_warp(&bar[B_ODONE + slot], (uint32_t)((cnt - 1) & 1))) {
+            // ---- epilogue: O / l for this row (O_DONE: once per item and slot)
+            if (!mbar_wait_warp(&bar[B_ODONE + slot], (uint32_t)(items_done & 1))) {
                 ok = false;
                 break;
             }
+            ++items_done;
             tc_fence_after();
             const float inv = l > 0.f ? vs / l : 0.f;
             T *dst = reinterpret_cast<T *>(p.out) +
