@@ -882,15 +882,20 @@ __global__ void __launch_bounds__(32 * kMergeHeadsPerCta) merge_kernel(const __g
     const int h = (blockIdx.x % groups) * kMergeHeadsPerCta + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     __shared__ int s_r;
-    if (threadIdx.x == 0) {
-        // the last request whose start is <= t
-        int lo = 0, hi = p.R - 1;
+    if (threadIdx.x < 32) {
+        // The last request whose start is <= t, by a 32-way search: each round
+        // the warp probes 32 evenly spaced starts at once (two rounds for up
+        // to 1024 requests), instead of one dependent load per halving.
+        int lo = 0, hi = p.R - 1;   // qsl[lo] <= t throughout
         while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.qsl[mid] <= t) lo = mid;
-            else hi = mid - 1;
+            const int step = (hi - lo + 1 + 31) / 32;
+            const int idx = lo + lane * step;
+            const bool le = idx <= hi && p.qsl[idx] <= t;
+            const unsigned m = __ballot_sync(0xffffffffu, le);
+            lo += (31 - __clz(m)) * step;
+            hi = min(hi, lo + step - 1);
         }
-        s_r = lo;
+        if (lane == 0) s_r = lo;
     }
     __syncthreads();
     if (h >= p.Hq) return;
