@@ -1,4 +1,4 @@
-// Paged attention, split-K over KV partitions, on the CUDA cores.
+// Paged attention, split-K over KV partitions.
 //
 // "How vLLM Works Internally", section "How the Kernel Works": look up the
 // block table, fetch K from the scattered blocks, scores, softmax, weighted
@@ -10,21 +10,24 @@
 //     (query token, q head of group g) pair, so each K/V page is read once
 //     for all Hq/Hkv heads that share it and for all query tokens of a short
 //     chunk.  Rows per item (RPI) is a template parameter.
-//   * Persistent CTAs (3 per SM; 2 for 8-row items, which need more registers).  Every warp walks the request list itself
-//     (a warp-wide scan over 32 requests at a time) to map its CTA's next
-//     item index to (r, g, chunk, partition), so no work list is stored and
-//     no planning launch is needed.
-//   * One producer warp issues 3-D TMA copies of one 16-token page of one kv
-//     head (box D x 1 x 16) into a 16-stage shared-memory ring, driven by the
-//     block table, in the order K0 V0 K1 V1 ...; four consumer warps take the
-//     (K, V) page pairs round-robin.  mbarriers: full (TMA bytes) and empty
-//     (one arrive by the owning warp).  Every wait is bounded.
-//   * Keys are processed in chunks of 256 (16 pages): all K pages of the
-//     chunk -> scores in shared memory -> exact chunk max/sum, combined
-//     online across chunks -> all V pages of the chunk.  QK: one warp per
-//     key, D/32 dims per lane, reduce-scatter shuffles across lanes.  PV: one
-//     warp per key, lanes over dims, per-warp partial accumulators combined
-//     through shared memory once per item.
+//   * Persistent CTAs (3 per SM; 2 for 8-row items, which need more
+//     registers).  The producer warp takes each next item index from a
+//     counter in the workspace as its CTA frees up (a fixed stride when there
+//     is no workspace) and passes it to the consumer warps through a small
+//     shared-memory queue.  Every warp walks the request list itself (a
+//     warp-wide scan over 32 requests at a time) to map an item index to
+//     (r, g, chunk, partition), so no work list is stored and no planning
+//     launch is needed.
+//   * One producer warp issues swizzled 3-D TMA copies of 16-token pages of
+//     one kv head into a 16-stage shared-memory ring, driven by the block
+//     table: K unit, V unit, ... where a unit is one page (two for FP8
+//     pools).  Unit j of an item goes to consumer warp j mod 4.  mbarriers:
+//     full (TMA bytes) and empty (one arrive by the owning warp); every wait
+//     is bounded.
+//   * Consumers run on the tensor cores with mma.sync (m16n8k16, f32
+//     accumulate): S^T = K Q^T and O^T += V^T P^T per page, the item's rows
+//     as the MMA's N, an online softmax per warp, the four warps' states
+//     combined once per item.  FP8 E4M3 pages widen to f16 in registers.
 //   * A request whose context fits one partition writes its output directly;
 //     otherwise (m, l, unnormalised o) go to the workspace and the merge
 //     kernel combines them.
@@ -46,6 +49,7 @@ constexpr int kCtasPerSm = 3;
 constexpr int kPage = 16;         // tokens per cache block
 constexpr int kCandidates = 8;    // partition lengths p_min << k
 constexpr int kSingle = INT_MAX / 2;
+constexpr int kQueue = 8;         // item queue entries (producer -> consumer warps)
 
 struct Params {
     CUtensorMap tmK;
@@ -59,6 +63,8 @@ struct Params {
     float *part_ml;       // [pslot][RPI][2]
     int32_t *req_meta;    // [R][4]: pslot base (lo, hi), nsplit, nchunks
     long long pslot_cap;  // partial items the workspace holds
+    unsigned int *item_counter;  // zeroed before launch: CTAs take the next item as they
+                                 // free up (NULL: fixed stride over the items)
     int R, T, MB, NB, Hq, Hkv, G;
     int tau;              // requests with more query tokens are not handled here
     int p_min;            // preferred partition length in keys (multiple of 256)
@@ -110,19 +116,29 @@ struct Cfg {
     static constexpr int kUnitBytes = kSP * L::kPageBytes;
     // 64 KB of pages in flight per CTA at head_dim 128
     static constexpr int kStages = 16;
-    // Page pairs (K, V) are dealt round-robin to the consumer warps.  With
-    // (kStages / 2) a multiple of the warp count, pair n always lands on stages
-    // 2n mod kStages and 2n+1 mod kStages owned by warp n mod 4 alone, so every
-    // round of a stage is consumed by the same warp in order: a warp can never
-    // run a whole ring round ahead on a stage (where mbarrier parity could not
-    // tell the rounds apart).
-    static_assert((kStages / 2) % kConsumerWarps == 0, "stages must split evenly among warps");
-    static_assert((kStages & (kStages - 1)) == 0, "ring index arithmetic uses a power-of-two ring");
+    // Unit pairs (K, V) of an item are dealt to the consumer warps by their
+    // index in the item: unit j goes to warp j mod 4, so an item's arithmetic
+    // never depends on what the CTA ran before it.  Each warp owns
+    // kPairsPerWarp pairs of stages and fills them in turn (pair_stage), so
+    // every round of a stage is consumed by the same warp in order: a warp can
+    // never run a whole round ahead on a stage (where mbarrier parity could
+    // not tell the rounds apart).
+    static constexpr int kPairsPerWarp = kStages / 2 / kConsumerWarps;
+    static_assert(kPairsPerWarp * 2 * kConsumerWarps == kStages, "stages must split evenly among warps");
+    static_assert((kPairsPerWarp & (kPairsPerWarp - 1)) == 0, "per-warp counters wrap at a power of two");
     static constexpr int kStageBytes = kStages * kUnitBytes;
     static constexpr int kComb = RPI * (D + 2);       // per warp: acc[row][D], m[row], l[row]
     static constexpr int kBytes = kStageBytes + kConsumerWarps * kComb * 4 +
-                                  (2 * kStages + 2) * 8 + kCandidates * 8 + 1024;
+                                  (2 * kStages + 2) * 8 + kCandidates * 8 + kQueue * 3 * 8 +
+                                  1024;
 };
+
+// First stage of warp w's c-th (K, V) unit pair (the V unit takes the next
+// stage); that round's mbarrier parity is (c / kPW) & 1.
+template <int kPW>
+__device__ __forceinline__ int pair_stage(int w, uint32_t c) {
+    return 2 * (w + kConsumerWarps * (int)(c % kPW));
+}
 
 // Per-warp walk over the request list: maps a global item index to its
 // request and coordinates.  All warps of all CTAs compute the same mapping.
@@ -338,6 +354,9 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     uint64_t *empty = full + kSt;
     uint64_t *cbar = empty + kSt;
     unsigned long long *cand = reinterpret_cast<unsigned long long *>(cbar + 2);
+    uint64_t *qfull = reinterpret_cast<uint64_t *>(cand + kCandidates);
+    uint64_t *qempty = qfull + kQueue;
+    long long *qitem = reinterpret_cast<long long *>(qempty + kQueue);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -348,6 +367,10 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             mbar_init(&empty[s], 1);
         }
         mbar_init(cbar, kConsumerWarps);
+        for (int e = 0; e < kQueue; ++e) {
+            mbar_init(&qfull[e], 1);
+            mbar_init(&qempty[e], kConsumerWarps);
+        }
         fence_mbar_init();
     }
     if (warp == kConsumerWarps && lane == 0) {
@@ -407,18 +430,44 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     Walker<RPI> walk;
     walk.begin(&p, part, lane);
     typename Walker<RPI>::Item it;
+    // With an item counter the producer takes each next index from it and
+    // publishes it in queue entry k % kQueue (-1: no more items) for the
+    // consumer warps; without one, CTA b takes items b, b + grid, ...  Either
+    // way a CTA's indices rise, as the walker needs.
 
     if (warp == kConsumerWarps) {
         // =================== producer warp ===================
-        // Ring order: K unit 0, V unit 0, K unit 1, V unit 1, ... of each item,
-        // a unit being C::kSP consecutive pages of the request.  A page is
-        // L::NSUB swizzled boxes of 16 rows (one per 128 bytes of a row),
-        // landing back to back.
+        // Issue order: K unit 0, V unit 0, K unit 1, V unit 1, ... of each
+        // item, a unit being C::kSP consecutive pages of the request, unit j
+        // into the next stage pair of warp j mod 4.  A page is L::NSUB swizzled
+        // boxes of 16 rows (one per 128 bytes of a row), landing back to back.
         constexpr int kSP = C::kSP;
-        int stage = 0;
-        uint32_t phase = 0;
+        constexpr int kPW = C::kPairsPerWarp;
+        // pairs handed to each consumer warp so far, mod 256: one byte per warp
+        uint32_t handed = 0;
+        auto handed_to = [&](int w) { return (handed >> (8 * w)) & 0xffu; };
         bool ok = true;
-        for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x) {
+        for (long long k = 0; ok; ++k) {
+            if (p.item_counter) {
+                unsigned int cand = 0;
+                if (lane == 0) cand = atomicAdd(p.item_counter, 1u);
+                cand = __shfl_sync(0xffffffffu, cand, 0);
+                const bool valid = walk.find((long long)cand, lane, it);
+                const int e = (int)(k % kQueue);
+                if (lane == 0) {
+                    if (!mbar_wait(&qempty[e], (uint32_t)(((k / kQueue) & 1) ^ 1))) {
+                        flag(p.status, PA_CHECK_TIMEOUT);
+                        ok = false;
+                    } else {
+                        qitem[e] = valid ? (long long)cand : -1;
+                        mbar_arrive(&qfull[e]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok || !valid) break;
+            } else if (!walk.find(blockIdx.x + k * gridDim.x, lane, it)) {
+                break;
+            }
             int k0, k1;
             item_keys<RPI>(p, it, part, k0, k1);
             const int npages = (k1 - k0 + kPage - 1) / kPage;
@@ -438,8 +487,13 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                     int b[kSP];
 #pragma unroll
                     for (int sp = 0; sp < kSP; ++sp) b[sp] = __shfl_sync(0xffffffffu, blk, min(pu + sp, 31));
+                    const int w = ((g0 + pu) / kSP) % kConsumerWarps;
+                    const uint32_t c = handed_to(w);
+                    const uint32_t phase = (c / kPW) & 1u;
+                    handed = (handed & ~(0xffu << (8 * w))) | (((c + 1) & 0xffu) << (8 * w));
 #pragma unroll
                     for (int kv = 0; kv < 2; ++kv) {
+                        const int stage = pair_stage<kPW>(w, c) + kv;
                         if (lane == 0) {
                             if (!mbar_wait(&empty[stage], phase ^ 1)) {
                                 flag(p.status, PA_CHECK_TIMEOUT);
@@ -458,36 +512,33 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                                 }
                             }
                         }
-                        if (++stage == kSt) {
-                            stage = 0;
-                            phase ^= 1;
-                        }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                 }
             }
         }
-        // Drain: wait (bounded) until the consumers have released every stage,
-        // so no copy is still landing when the CTA exits.
+        // Drain: wait (bounded) until the consumers have released every stage
+        // (each warp's next kPW pairs find their stages free), so no copy is
+        // still landing when the CTA exits.
         if (lane == 0) {
-            for (int s = 0; s < kSt; ++s) {
-                if (!mbar_wait(&empty[stage], phase ^ 1)) {
-                    flag(p.status, PA_CHECK_TIMEOUT);
-                    break;
+            bool drained = true;
+            for (int w = 0; drained && w < kConsumerWarps; ++w)
+                for (int j = 0; drained && j < kPW; ++j) {
+                    const uint32_t c = handed_to(w) + j;
+                    for (int kv = 0; drained && kv < 2; ++kv)
+                        if (!mbar_wait(&empty[pair_stage<kPW>(w, c) + kv], ((c / kPW) & 1u) ^ 1)) {
+                            flag(p.status, PA_CHECK_TIMEOUT);
+                            drained = false;
+                        }
                 }
-                if (++stage == kSt) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
         }
         return;
     }
 
     // =================== consumer warps ===================
-    // Warp w takes the page pairs whose running index (over all items of this
-    // CTA) is w mod 4 and keeps its own online-softmax state; the four states
-    // are combined once per item.  Per page pair, on the tensor cores:
+    // Warp w takes the unit pairs w, w + 4, ... of each item and keeps its
+    // own online-softmax state; the four states are combined once per item
+    // (in warp order, so an item's result is the same whichever CTA runs it).  Per page pair, on the tensor cores:
     //   S^T (16 keys x 8 rows) = K (16 x D) . Q^T      (D/16 MMAs, k = dims)
     //   O^T (D x 8 rows)      += V^T (D x 16) . P^T    (D/16 MMAs, k = keys)
     // Lane (gq = lane/4, tq = lane%4) holds S^T for keys perm16(gq), perm16(gq+8)
@@ -525,10 +576,24 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         for (int e = 0; e < 4; ++e) voff[e] = L::chunk_off(vkey[e], byte / 16) + byte % 16;
     }
     float *cw = comb + warp * C::kComb;
-    int pair_base = 0;               // page pairs of earlier items
+    uint32_t taken = 0;              // unit pairs this warp has consumed
     uint32_t cpar = 0;
     bool ok = true;
-    for (long long i = blockIdx.x; ok && walk.find(i, lane, it); i += gridDim.x) {
+    for (long long k = 0; ok; ++k) {
+        long long i = blockIdx.x + k * gridDim.x;
+        if (p.item_counter) {
+            const int e = (int)(k % kQueue);
+            if (!mbar_wait_warp(&qfull[e], (uint32_t)((k / kQueue) & 1))) {
+                flag(p.status, PA_CHECK_TIMEOUT);
+                ok = false;
+                break;
+            }
+            i = qitem[e];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qempty[e]);
+            if (i < 0) break;
+        }
+        if (!walk.find(i, lane, it)) break;
         int k0, k1;
         item_keys<RPI>(p, it, part, k0, k1);
         const int npages = (k1 - k0 + kPage - 1) / kPage;
@@ -578,11 +643,9 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
         constexpr int kSP = C::kSP;
         const int nunits = (npages + kSP - 1) / kSP;
-        for (int pu = (warp - pair_base % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-             pu < nunits; pu += kConsumerWarps) {
-            const uint32_t n2 = 2u * (uint32_t)(pair_base + pu);
-            const uint32_t stK = n2 & (kSt - 1), stV = (n2 + 1) & (kSt - 1);
-            const uint32_t phK = (n2 / kSt) & 1u, phV = ((n2 + 1) / kSt) & 1u;
+        for (int pu = warp; pu < nunits; pu += kConsumerWarps, ++taken) {
+            const uint32_t stK = pair_stage<C::kPairsPerWarp>(warp, taken), stV = stK + 1;
+            const uint32_t phK = (taken / C::kPairsPerWarp) & 1u, phV = phK;
             if (!mbar_wait_warp(&full[stK], phK) || !mbar_wait_warp(&full[stV], phV)) {
                 flag(p.status, PA_CHECK_TIMEOUT);
                 ok = false;
@@ -773,7 +836,6 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             }
         }
         if (!ok) break;
-        pair_base += nunits;
 
         // ---- combine the four warps' states and write the item out
 #pragma unroll
@@ -857,11 +919,12 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             break;
         }
     }
-    // A consumer that stops early (a timed-out wait) releases every stage and
-    // the item barrier once, so the others' bounded waits and the producer's
-    // drain can finish.
+    // A consumer that stops early (a timed-out wait) releases every stage,
+    // every queue entry and the item barrier once, so the others' bounded
+    // waits and the producer's drain can finish.
     if (!ok && lane == 0) {
         for (int s = 0; s < kSt; ++s) mbar_arrive(&empty[s]);
+        for (int e = 0; e < kQueue; ++e) mbar_arrive(&qempty[e]);
         mbar_arrive(cbar);
     }
 }
@@ -1070,6 +1133,7 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     prm.qscale = a.scale * 1.4426950408889634f;
     prm.status = status_word();
     if (!prm.status) return PA_ERR_CUDA;
+    prm.item_counter = a.ctrl ? a.ctrl + kCtrlDecodeCounter : nullptr;
     const int rpi = rows_per_item(prm.G, a.max_q < tau ? a.max_q : tau);
 
     // Workspace: per-request metadata, then (m, l) and o partials.

@@ -371,8 +371,8 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
     a.k_scale = cache_dtype == PA_FP8_E4M3 ? k_scale : nullptr;
     a.v_scale = cache_dtype == PA_FP8_E4M3 ? v_scale : nullptr;
     a.out = out;
-    // The workspace starts with a small control block (the tensor-core
-    // kernel's item counter); the split-K partials take the rest.
+    // The workspace starts with a small control block (the kernels' item
+    // counters); the split-K partials take the rest.
     a.ctrl = nullptr;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
@@ -382,6 +382,7 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
         a.ws_bytes = workspace_bytes - kCtrlBytes;
     }
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (a.ctrl) PA_TRY_CUDA(cudaMemsetAsync(a.ctrl, 0, kCtrlWords * sizeof(unsigned int), st));
     const int tau = prefill_tau(a);
     const pa_status r = launch_decode(a, tau, st);
     if (r != PA_OK) return r;

@@ -80,6 +80,11 @@ struct AttnArgs {
 
 // Bytes at the start of a caller's workspace kept for per-call counters.
 constexpr size_t kCtrlBytes = 256;
+// Words of the control block: the kernels' item counters, zeroed by one
+// memset before each attention call's launches.
+constexpr int kCtrlPrefillCounter = 0;
+constexpr int kCtrlDecodeCounter = 1;
+constexpr int kCtrlWords = 2;
 
 size_t decode_workspace_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq,
                              int32_t Hq, int32_t Hkv, int32_t D);

@@ -912,10 +912,8 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
         return PA_ERR_CUDA;
     prm.k_scale = a.k_scale;
     prm.v_scale = a.v_scale;
-    if (a.ctrl) {   // items in order as CTAs free up: the counter starts at 0
-        PA_TRY_CUDA(cudaMemsetAsync(a.ctrl, 0, sizeof(unsigned int), stream));
-        prm.item_counter = a.ctrl;
-    }
+    // items in order as CTAs free up (the caller zeroed the counter)
+    prm.item_counter = a.ctrl ? a.ctrl + kCtrlPrefillCounter : nullptr;
     prm.out = a.out;
     prm.bt = a.bt;
     prm.qsl = a.qsl;
