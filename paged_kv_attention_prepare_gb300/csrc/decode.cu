@@ -517,6 +517,9 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 }
             }
         }
+        // No items left for this CTA: the merge pass may be scheduled (it
+        // still waits for this grid to finish before reading).
+        if (lane == 0) grid_launch_dependents();
         // Drain: wait (bounded) until the consumers have released every stage
         // (each warp's next kPW pairs find their stages free), so no copy is
         // still landing when the CTA exits.
@@ -931,89 +934,99 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
 // Second pass: for each (token, q head) of a request whose context was split,
 // combine the partitions' (m, l, o): M = max m_s, o = sum 2^(m_s-M) o_s /
-// sum 2^(m_s-M) l_s.  One CTA per (token, group of 8 heads), one warp per
-// head, so a long request's partitions are combined on many SMs at once.
-// Lanes take 32 partitions at a time for (m, l); the weighted sum then walks
-// those 32 with lanes over dims, eight independent partial-row loads in flight.
+// sum 2^(m_s-M) l_s.  One CTA per (request, group of 8 q heads), one warp per
+// head, looping over the request's few query tokens.  Latency, not bytes,
+// bounds it, so a warp issues its first kMergeBatch partial rows (lanes over
+// dims) before anything that depends on the (m, l) values, and loads each
+// partition's (m, l) once (lanes over partitions, 32 at a time).
+// Launched as a programmatic dependent of the split-K kernel: its CTAs can
+// become resident while that kernel's last items finish, and wait for all
+// of its writes before reading.
 constexpr int kMergeHeadsPerCta = 8;
+constexpr int kMergeBatch = 16;   // partial rows in flight per warp
+
+template <int DPL> struct MergeVec;
+template <> struct MergeVec<4> { using type = float4; };
+template <> struct MergeVec<2> { using type = float2; };
+
+template <typename V> __device__ __forceinline__ void fma_vec(float *o, float w, const V &v);
+template <> __device__ __forceinline__ void fma_vec<float4>(float *o, float w, const float4 &v) {
+    o[0] = fmaf(w, v.x, o[0]);
+    o[1] = fmaf(w, v.y, o[1]);
+    o[2] = fmaf(w, v.z, o[2]);
+    o[3] = fmaf(w, v.w, o[3]);
+}
+template <> __device__ __forceinline__ void fma_vec<float2>(float *o, float w, const float2 &v) {
+    o[0] = fmaf(w, v.x, o[0]);
+    o[1] = fmaf(w, v.y, o[1]);
+}
 
 template <typename T, int D, int RPI>
 __global__ void __launch_bounds__(32 * kMergeHeadsPerCta) merge_kernel(const __grid_constant__ Params p) {
     constexpr int DPL = D / 32;
+    using V = typename MergeVec<DPL>::type;
     const int groups = (p.Hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta;
-    const int t = blockIdx.x / groups;
+    const int r = blockIdx.x / groups;
     const int h = (blockIdx.x % groups) * kMergeHeadsPerCta + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    __shared__ int s_r;
-    if (threadIdx.x < 32) {
-        // The last request whose start is <= t, by a 32-way search: each round
-        // the warp probes 32 evenly spaced starts at once (two rounds for up
-        // to 1024 requests), instead of one dependent load per halving.
-        int lo = 0, hi = p.R - 1;   // qsl[lo] <= t throughout
-        while (lo < hi) {
-            const int step = (hi - lo + 1 + 31) / 32;
-            const int idx = lo + lane * step;
-            const bool le = idx <= hi && p.qsl[idx] <= t;
-            const unsigned m = __ballot_sync(0xffffffffu, le);
-            lo += (31 - __clz(m)) * step;
-            hi = min(hi, lo + step - 1);
-        }
-        if (lane == 0) s_r = lo;
-    }
-    __syncthreads();
-    if (h >= p.Hq) return;
-    const int r = s_r;
+    grid_dependency_wait();   // every write of the split-K kernel is visible past here
+    if (h >= p.Hq || r >= p.R) return;
     const int4 meta = reinterpret_cast<const int4 *>(p.req_meta)[r];
     const int nsplit = meta.z, nchunks = meta.w;
     if (nsplit <= 1) return;
-    const int tl = t - p.qsl[r];
-    if (tl < 0 || tl >= p.qsl[r + 1] - p.qsl[r]) return;
+    const int t0 = p.qsl[r], n = p.qsl[r + 1] - t0;
     const long long pbase = (long long)(unsigned)meta.x | ((long long)meta.y << 32);
     const int g = h / p.G;
-    const int rr = tl * p.G + h % p.G;
-    const int chunk = rr / RPI, j = rr % RPI;
-    const long long first = pbase + ((long long)g * nchunks + chunk) * nsplit;
     const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
-    float M = -INFINITY;
-    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, ml[(first + s) * RPI + j].x);
+    for (int tl = 0; tl < n; ++tl) {
+        const int rr = tl * p.G + h % p.G;
+        const int chunk = rr / RPI, j = rr % RPI;
+        const long long first = pbase + ((long long)g * nchunks + chunk) * nsplit;
+        auto row = [&](int s) {
+            return reinterpret_cast<const V *>(p.part_o + ((first + s) * RPI + j) * D) + lane;
+        };
+        // the first batch of partial rows, and (m, l) of partitions lane, lane + 32, ...
+        V v[kMergeBatch];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Lsum = 0.f;
-    float o[DPL];
+        for (int k = 0; k < kMergeBatch; ++k)
+            if (k < nsplit) v[k] = *row(k);
+        const float2 ml0 = lane < nsplit ? ml[(first + lane) * RPI + j] : make_float2(-INFINITY, 0.f);
+        float M = ml0.x;
+        for (int s = lane + 32; s < nsplit; s += 32) M = fmaxf(M, ml[(first + s) * RPI + j].x);
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) o[d] = 0.f;
-    for (int s0 = 0; s0 < nsplit; s0 += 32) {
-        float w = 0.f;
-        if (s0 + lane < nsplit) {
-            const float2 v = ml[(first + s0 + lane) * RPI + j];
-            w = v.x == -INFINITY ? 0.f : fast_exp2(v.x - M);
-            Lsum += w * v.y;
-        }
-        const int cnt = min(32, nsplit - s0);
-#pragma unroll 8
-        for (int k = 0; k < cnt; ++k) {
-            const float wk = __shfl_sync(0xffffffffu, w, k);
-            const float *po = p.part_o + ((first + s0 + k) * RPI + j) * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(po);
-                o[0] = fmaf(wk, v.x, o[0]);
-                o[1] = fmaf(wk, v.y, o[1]);
-                o[2] = fmaf(wk, v.z, o[2]);
-                o[3] = fmaf(wk, v.w, o[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(po);
-                o[0] = fmaf(wk, v.x, o[0]);
-                o[1] = fmaf(wk, v.y, o[1]);
+        for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+        float o[DPL];
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[d] = 0.f;
+        float Lsum = 0.f;
+        for (int s0 = 0; s0 < nsplit; s0 += 32) {
+            // weight of partition s0 + lane
+            float2 mv = ml0;
+            if (s0 > 0) mv = s0 + lane < nsplit ? ml[(first + s0 + lane) * RPI + j] : make_float2(-INFINITY, 0.f);
+            const float w = mv.x == -INFINITY ? 0.f : fast_exp2(mv.x - M);
+            Lsum += w * mv.y;
+            const int cnt = min(32, nsplit - s0);
+            for (int k0 = 0; k0 < cnt; k0 += kMergeBatch) {
+                if (s0 + k0 > 0) {   // later batches (the first was issued above)
+#pragma unroll
+                    for (int k = 0; k < kMergeBatch; ++k)
+                        if (k0 + k < cnt) v[k] = *row(s0 + k0 + k);
+                }
+#pragma unroll
+                for (int k = 0; k < kMergeBatch; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+                    if (k0 + k < cnt) fma_vec(o, wk, v[k]);
+                }
             }
         }
+#pragma unroll
+        for (int x = 16; x >= 1; x >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, x);
+        const float inv = 1.f / Lsum;
+        T *dst = reinterpret_cast<T *>(p.out) + ((long long)(t0 + tl) * p.Hq + h) * D + lane * DPL;
+#pragma unroll
+        for (int d = 0; d < DPL; d += 2)
+            *reinterpret_cast<uint32_t *>(dst + d) = Elt<T>::pack2(o[d] * inv, o[d + 1] * inv);
     }
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, s);
-    const float inv = 1.f / Lsum;
-    T *dst = reinterpret_cast<T *>(p.out) + ((long long)t * p.Hq + h) * D + lane * DPL;
-#pragma unroll
-    for (int d = 0; d < DPL; d += 2)
-        *reinterpret_cast<uint32_t *>(dst + d) = Elt<T>::pack2(o[d] * inv, o[d + 1] * inv);
 }
 
 template <typename TQ, typename TC, int D, int RPI>
@@ -1038,10 +1051,18 @@ pa_status launch_typed(Params &prm, long long max_items, bool merge, cudaStream_
     paged_decode_kernel<TQ, TC, D, RPI><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
-    if (merge && prm.T > 0) {
+    if (merge && prm.R > 0) {
         const long long groups = (prm.Hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta;
-        merge_kernel<TQ, D, RPI><<<(unsigned)(prm.T * groups), 32 * kMergeHeadsPerCta, 0, stream>>>(prm);
-        PA_TRY_CUDA(cudaGetLastError());
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(prm.R * groups));
+        cfg.blockDim = dim3(32 * kMergeHeadsPerCta);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, merge_kernel<TQ, D, RPI>, prm));
         note_launch();
     }
     return PA_OK;

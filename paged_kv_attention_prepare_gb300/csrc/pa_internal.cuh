@@ -180,6 +180,19 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// Programmatic dependent launch.  A grid launched with programmatic stream
+// serialization may start before the grid ahead of it in the stream ends;
+// grid_dependency_wait() returns once that grid has completed and its
+// memory writes are visible (at once for a grid launched without the
+// attribute).  grid_launch_dependents() lets the dependent grid be scheduled
+// once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
