@@ -934,15 +934,17 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
 // Second pass: for each (token, q head) of a request whose context was split,
 // combine the partitions' (m, l, o): M = max m_s, o = sum 2^(m_s-M) o_s /
-// sum 2^(m_s-M) l_s.  One CTA per (request, group of 8 q heads), one warp per
-// head, looping over the request's few query tokens.  Latency, not bytes,
-// bounds it, so a warp issues its first kMergeBatch partial rows (lanes over
-// dims) before anything that depends on the (m, l) values, and loads each
-// partition's (m, l) once (lanes over partitions, 32 at a time).
+// sum 2^(m_s-M) l_s.  One CTA of 8 warps per (request, group of 8 / WPH q
+// heads), looping over the request's few query tokens; WPH warps share a
+// head, warp k of them taking partitions k, k + WPH, ...  Latency, not
+// bytes, bounds it, so a warp issues its first kMergeBatch partial rows
+// (lanes over dims) before anything that depends on the (m, l) values and
+// loads each partition's (m, l) once (lanes over partitions); the WPH
+// partial merges then combine the same way through shared memory.
 // Launched as a programmatic dependent of the split-K kernel: its CTAs can
 // become resident while that kernel's last items finish, and wait for all
 // of its writes before reading.
-constexpr int kMergeHeadsPerCta = 8;
+constexpr int kMergeWarps = 8;
 constexpr int kMergeBatch = 16;   // partial rows in flight per warp
 
 template <int DPL> struct MergeVec;
@@ -961,76 +963,143 @@ template <> __device__ __forceinline__ void fma_vec<float2>(float *o, float w, c
     o[1] = fmaf(w, v.y, o[1]);
 }
 
-template <typename T, int D, int RPI>
-__global__ void __launch_bounds__(32 * kMergeHeadsPerCta) merge_kernel(const __grid_constant__ Params p) {
+template <typename T, int D, int RPI, int WPH>
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_constant__ Params p) {
     constexpr int DPL = D / 32;
+    constexpr int kHeads = kMergeWarps / WPH;   // heads per CTA
     using V = typename MergeVec<DPL>::type;
-    const int groups = (p.Hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta;
+    __shared__ __align__(16) float sh_o[WPH > 1 ? kMergeWarps : 1][D];
+    __shared__ float2 sh_ml[kMergeWarps];
+    const int groups = (p.Hq + kHeads - 1) / kHeads;
     const int r = blockIdx.x / groups;
-    const int h = (blockIdx.x % groups) * kMergeHeadsPerCta + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = (blockIdx.x % groups) * kHeads + warp / WPH;
+    const int sub = warp % WPH;
     grid_dependency_wait();   // every write of the split-K kernel is visible past here
-    if (h >= p.Hq || r >= p.R) return;
+    if (r >= p.R) return;
     const int4 meta = reinterpret_cast<const int4 *>(p.req_meta)[r];
     const int nsplit = meta.z, nchunks = meta.w;
-    if (nsplit <= 1) return;
+    if (nsplit <= 1) return;                    // the same for the whole CTA
+    const bool active = h < p.Hq;               // a CTA's last heads may be past Hq
     const int t0 = p.qsl[r], n = p.qsl[r + 1] - t0;
     const long long pbase = (long long)(unsigned)meta.x | ((long long)meta.y << 32);
     const int g = h / p.G;
+    const int cnt_w = nsplit > sub ? (nsplit - sub + WPH - 1) / WPH : 0;   // this warp's partitions
     const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml);
     for (int tl = 0; tl < n; ++tl) {
         const int rr = tl * p.G + h % p.G;
         const int chunk = rr / RPI, j = rr % RPI;
         const long long first = pbase + ((long long)g * nchunks + chunk) * nsplit;
-        auto row = [&](int s) {
-            return reinterpret_cast<const V *>(p.part_o + ((first + s) * RPI + j) * D) + lane;
+        // this warp's i-th partition
+        auto split = [&](int i) { return first + sub + (long long)i * WPH; };
+        auto row = [&](int i) {
+            return reinterpret_cast<const V *>(p.part_o + (split(i) * RPI + j) * D) + lane;
         };
-        // the first batch of partial rows, and (m, l) of partitions lane, lane + 32, ...
-        V v[kMergeBatch];
-#pragma unroll
-        for (int k = 0; k < kMergeBatch; ++k)
-            if (k < nsplit) v[k] = *row(k);
-        const float2 ml0 = lane < nsplit ? ml[(first + lane) * RPI + j] : make_float2(-INFINITY, 0.f);
-        float M = ml0.x;
-        for (int s = lane + 32; s < nsplit; s += 32) M = fmaxf(M, ml[(first + s) * RPI + j].x);
-#pragma unroll
-        for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
         float o[DPL];
 #pragma unroll
         for (int d = 0; d < DPL; ++d) o[d] = 0.f;
-        float Lsum = 0.f;
-        for (int s0 = 0; s0 < nsplit; s0 += 32) {
-            // weight of partition s0 + lane
-            float2 mv = ml0;
-            if (s0 > 0) mv = s0 + lane < nsplit ? ml[(first + s0 + lane) * RPI + j] : make_float2(-INFINITY, 0.f);
-            const float w = mv.x == -INFINITY ? 0.f : fast_exp2(mv.x - M);
-            Lsum += w * mv.y;
-            const int cnt = min(32, nsplit - s0);
-            for (int k0 = 0; k0 < cnt; k0 += kMergeBatch) {
-                if (s0 + k0 > 0) {   // later batches (the first was issued above)
+        float M = -INFINITY, Lsum = 0.f;
+        if (active && cnt_w > 0) {
+            // the first batch of partial rows, and (m, l) of partitions lane, lane + 32, ...
+            V v[kMergeBatch];
 #pragma unroll
-                    for (int k = 0; k < kMergeBatch; ++k)
-                        if (k0 + k < cnt) v[k] = *row(s0 + k0 + k);
-                }
+            for (int k = 0; k < kMergeBatch; ++k)
+                if (k < cnt_w) v[k] = *row(k);
+            const float2 ml0 = lane < cnt_w ? ml[split(lane) * RPI + j] : make_float2(-INFINITY, 0.f);
+            M = ml0.x;
+            for (int i = lane + 32; i < cnt_w; i += 32) M = fmaxf(M, ml[split(i) * RPI + j].x);
 #pragma unroll
-                for (int k = 0; k < kMergeBatch; ++k) {
-                    const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
-                    if (k0 + k < cnt) fma_vec(o, wk, v[k]);
+            for (int x = 16; x >= 1; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+            for (int i0 = 0; i0 < cnt_w; i0 += 32) {
+                // weight of partition i0 + lane
+                float2 mv = ml0;
+                if (i0 > 0) mv = i0 + lane < cnt_w ? ml[split(i0 + lane) * RPI + j] : make_float2(-INFINITY, 0.f);
+                const float w = mv.x == -INFINITY ? 0.f : fast_exp2(mv.x - M);
+                Lsum += w * mv.y;
+                const int cnt = min(32, cnt_w - i0);
+                for (int k0 = 0; k0 < cnt; k0 += kMergeBatch) {
+                    if (i0 + k0 > 0) {   // later batches (the first was issued above)
+#pragma unroll
+                        for (int k = 0; k < kMergeBatch; ++k)
+                            if (k0 + k < cnt) v[k] = *row(i0 + k0 + k);
+                    }
+#pragma unroll
+                    for (int k = 0; k < kMergeBatch; ++k) {
+                        const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+                        if (k0 + k < cnt) fma_vec(o, wk, v[k]);
+                    }
                 }
             }
+#pragma unroll
+            for (int x = 16; x >= 1; x >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, x);
         }
+        if constexpr (WPH > 1) {
+            // combine the WPH warps of each head: M = max M_k, o = sum 2^(M_k - M) o_k
 #pragma unroll
-        for (int x = 16; x >= 1; x >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, x);
-        const float inv = 1.f / Lsum;
-        T *dst = reinterpret_cast<T *>(p.out) + ((long long)(t0 + tl) * p.Hq + h) * D + lane * DPL;
+            for (int d = 0; d < DPL; ++d) sh_o[warp][lane * DPL + d] = o[d];
+            if (lane == 0) sh_ml[warp] = make_float2(M, Lsum);
+            __syncthreads();
+            if (sub == 0 && active) {
+                float Mh = -INFINITY;
 #pragma unroll
-        for (int d = 0; d < DPL; d += 2)
-            *reinterpret_cast<uint32_t *>(dst + d) = Elt<T>::pack2(o[d] * inv, o[d + 1] * inv);
+                for (int k = 0; k < WPH; ++k) Mh = fmaxf(Mh, sh_ml[warp + k].x);
+                float acc[DPL], Lh = 0.f;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+#pragma unroll
+                for (int k = 0; k < WPH; ++k) {
+                    const float2 mk = sh_ml[warp + k];
+                    const float wk = mk.x == -INFINITY ? 0.f : fast_exp2(mk.x - Mh);
+                    Lh += wk * mk.y;
+                    fma_vec(acc, wk, reinterpret_cast<const V *>(sh_o[warp + k])[lane]);
+                }
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) o[d] = acc[d];
+                Lsum = Lh;
+            }
+            __syncthreads();   // shared memory is free for the next token
+        }
+        if (sub == 0 && active) {
+            const float inv = 1.f / Lsum;
+            T *dst = reinterpret_cast<T *>(p.out) + ((long long)(t0 + tl) * p.Hq + h) * D + lane * DPL;
+#pragma unroll
+            for (int d = 0; d < DPL; d += 2)
+                *reinterpret_cast<uint32_t *>(dst + d) = Elt<T>::pack2(o[d] * inv, o[d + 1] * inv);
+        }
     }
 }
 
+// Warps per head of the merge pass: enough that each warp's share of the
+// longest context's partitions fits one batch of in-flight rows, but no more
+// CTAs than about two waves (many short requests beside one long one keep
+// the grid small instead).
+static int merge_warps_per_head(long long max_splits, long long R, long long Hq) {
+    int wph = 1;
+    while (wph < kMergeWarps && max_splits > (long long)wph * kMergeBatch) wph *= 2;
+    while (wph > 1 && R * ((Hq * wph + kMergeWarps - 1) / kMergeWarps) > 4LL * num_sms()) wph /= 2;
+    return wph;
+}
+
+template <typename T, int D, int RPI, int WPH>
+static pa_status launch_merge(const Params &prm, cudaStream_t stream) {
+    constexpr int kHeads = kMergeWarps / WPH;
+    const long long groups = (prm.Hq + kHeads - 1) / kHeads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(prm.R * groups));
+    cfg.blockDim = dim3(32 * kMergeWarps);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, merge_kernel<T, D, RPI, WPH>, prm));
+    note_launch();
+    return PA_OK;
+}
+
 template <typename TQ, typename TC, int D, int RPI>
-pa_status launch_typed(Params &prm, long long max_items, bool merge, cudaStream_t stream) {
+pa_status launch_typed(Params &prm, long long max_items, long long merge_splits, cudaStream_t stream) {
     using S = Cfg<TC, D, RPI>;
     static int resident[64] = {};  // CTAs per SM, per device
     int dev = 0;
@@ -1051,25 +1120,19 @@ pa_status launch_typed(Params &prm, long long max_items, bool merge, cudaStream_
     paged_decode_kernel<TQ, TC, D, RPI><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
-    if (merge && prm.R > 0) {
-        const long long groups = (prm.Hq + kMergeHeadsPerCta - 1) / kMergeHeadsPerCta;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(prm.R * groups));
-        cfg.blockDim = dim3(32 * kMergeHeadsPerCta);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, merge_kernel<TQ, D, RPI>, prm));
-        note_launch();
+    if (merge_splits > 0 && prm.R > 0) {
+        switch (merge_warps_per_head(merge_splits, prm.R, prm.Hq)) {
+            case 1: return launch_merge<TQ, D, RPI, 1>(prm, stream);
+            case 2: return launch_merge<TQ, D, RPI, 2>(prm, stream);
+            case 4: return launch_merge<TQ, D, RPI, 4>(prm, stream);
+            default: return launch_merge<TQ, D, RPI, 8>(prm, stream);
+        }
     }
     return PA_OK;
 }
 
 template <typename TQ, typename TC, int D>
-pa_status dispatch_rpi(int rpi, Params &prm, long long grid, bool merge, cudaStream_t stream) {
+pa_status dispatch_rpi(int rpi, Params &prm, long long grid, long long merge, cudaStream_t stream) {
     switch (rpi) {
         case 1: return launch_typed<TQ, TC, D, 1>(prm, grid, merge, stream);
         case 2: return launch_typed<TQ, TC, D, 2>(prm, grid, merge, stream);
@@ -1079,7 +1142,7 @@ pa_status dispatch_rpi(int rpi, Params &prm, long long grid, bool merge, cudaStr
 }
 
 template <typename TQ>
-pa_status dispatch_cache(bool fp8, int D, int rpi, Params &prm, long long grid, bool merge,
+pa_status dispatch_cache(bool fp8, int D, int rpi, Params &prm, long long grid, long long merge,
                          cudaStream_t stream) {
     if (fp8)
         return D == 128 ? dispatch_rpi<TQ, Fp8E4M3, 128>(rpi, prm, grid, merge, stream)
@@ -1185,9 +1248,11 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     const long long chunks = (long long)a.R + ((long long)a.T * prm.G + rpi - 1) / rpi;
     const long long grid = (long long)a.Hkv * chunks * splits;
 
+    // the merge pass (when partitions exist) sizes itself by the most partitions a request can have
+    const long long merge_splits = merge ? splits : 0;
     return a.dtype == PA_BF16
-               ? dispatch_cache<__nv_bfloat16>(fp8, a.D, rpi, prm, grid, merge, stream)
-               : dispatch_cache<__half>(fp8, a.D, rpi, prm, grid, merge, stream);
+               ? dispatch_cache<__nv_bfloat16>(fp8, a.D, rpi, prm, grid, merge_splits, stream)
+               : dispatch_cache<__half>(fp8, a.D, rpi, prm, grid, merge_splits, stream);
 }
 
 }  // namespace pa

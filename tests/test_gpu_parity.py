@@ -96,6 +96,22 @@ def test_partition_choice_does_not_change_result(ws):
     _check_attention(res, ref)
 
 
+@pytest.mark.parametrize("longest,hq,hkv", [(10_000, 6, 2), (20_000, 5, 1), (40_000, 6, 2),
+                                             (90_000, 3, 3)])
+def test_many_partitions_merge(longest, hq, hkv):
+    # Long contexts split into 20-176 partitions: the merge pass spreads one
+    # head's partitions over 2-8 warps and combines them; head counts that
+    # leave a CTA's last heads unused, and short multi-token requests beside.
+    rng = np.random.default_rng(longest)
+    w = workloads._make("many-splits", [1, 3, 1, 2], [longest - 1, longest // 3, 300, 1000], rng,
+                        hq, hkv, 128, "bf16")
+    vals = workloads.make_values(w, 3)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_attention(res, ref)
+
+
 @pytest.mark.parametrize("group,ws", [(4, None), (8, None), (1, 0)])
 def test_prompt_chunk_longer_than_a_partition(group, ws):
     # A 600-token chunk at 300 computed spans two 512-key partitions: its first
