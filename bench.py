@@ -372,6 +372,9 @@ def run_ours(args):
     q, key, value = vals["q"], vals["key"], vals["value"]
     kc, vc = vals["key_cache"], vals["value_cache"]
     ks, vs = vals.get("k_scale"), vals.get("v_scale")   # FP8 pools only
+    # an engine that shares blocks across requests (copy-on-write forks,
+    # prefix caching) says so: PA_ATTN_SHARED_BLOCKS
+    shared = w.shares_blocks
     out = torch.empty_like(q)
     ws_bytes = pa.pa_attention_workspace_size(R, T, w.max_query_len, w.max_seq_len,
                                               w.num_q_heads, w.num_kv_heads, w.head_dim)
@@ -386,7 +389,7 @@ def run_ours(args):
         if timed:
             a0.record(stream)
         pa.pa_attention(q, kc, vc, bt, qsl, sl, w.max_query_len, w.max_seq_len, w.scale, out, ws,
-                        k_scale=ks, v_scale=vs)
+                        k_scale=ks, v_scale=vs, shared_blocks=shared)
         if timed:
             a1.record(stream)
 
@@ -536,7 +539,7 @@ def run_ours(args):
                              slot, qsl, sl, li)
         pa.pa_cache_write(d["key"], d["value"], kc, vc, slot, k_scale=ks, v_scale=vs)
         pa.pa_attention(d["q"], kc, vc, d["bt"], qsl, sl, w.max_query_len, w.max_seq_len,
-                        w.scale, outs[b], ws, k_scale=ks, v_scale=vs)
+                        w.scale, outs[b], ws, k_scale=ks, v_scale=vs, shared_blocks=shared)
 
     def e2e_h2d(b):
         with torch.cuda.stream(copy_stream):
@@ -622,7 +625,7 @@ def run_ours(args):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             pa.pa_attention(qs, kc, vc, bt_s, qsl_s, sl_s, mq, ms, w.scale, os_, ws, k_scale=ks,
-                            v_scale=vs)
+                            v_scale=vs, shared_blocks=shared)
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize()
@@ -706,7 +709,8 @@ def run_ours(args):
                        "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
                        "head_dim": w.head_dim, "block_size": w.block_size,
                        "kv_bytes": w.kv_read_bytes(), "parallelism": f"replicas x{world}",
-                       "l2": "flushed between steps (256 MB write outside the timed events)"},
+                       "l2": "flushed between steps (256 MB write outside the timed events)",
+                       "shared_blocks_flag": bool(shared)},
             "roofline": roofline,
             "roofline_prefill": roofline_prefill,
             "cpu_baseline": cpu,

@@ -364,7 +364,22 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
  * rounded to f16, exact inside f16's range); the output is dtype.  Errors as
  * pa_attention, plus PA_ERR_INVALID for a cache_dtype that is neither dtype
  * nor PA_FP8_E4M3.
+ *
+ * flags: 0, or PA_ATTN_SHARED_BLOCKS (any other bit: PA_ERR_INVALID).
+ * PA_ATTN_SHARED_BLOCKS declares that block tables may hold the same
+ * physical block for several requests -- the copy-on-write sharing of "How
+ * vLLM Works Internally", section "Copy-on-Write for Beam Search", or a
+ * prefix reused by "Prefix Caching (Automatic Prefix Caching)".  Results are
+ * the same with or without it.  With it, consecutive single-token requests
+ * whose tables hold the same blocks over a whole KV partition (512 keys
+ * with the workspace pa_attention_workspace_size() asks for) that their
+ * query sees completely -- up to 32 / (num_q_heads / num_kv_heads) such
+ * requests -- are computed together, reading those blocks once.  Without it
+ * the kernel carries no code for this (a few percent faster when nothing is
+ * shared).  The flag takes effect when a workspace is given and some context
+ * is longer than one partition.
  */
+#define PA_ATTN_SHARED_BLOCKS 1u
 pa_status pa_attention_ex(const void *q, const void *key_cache, const void *value_cache,
                           const int32_t *block_table, int32_t max_blocks_per_req,
                           const int32_t *query_start_loc, const int32_t *seq_lens,
@@ -372,7 +387,7 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
                           int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                           int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
                           pa_dtype dtype, pa_dtype cache_dtype, const float *k_scale,
-                          const float *v_scale, void *out, void *workspace,
+                          const float *v_scale, uint32_t flags, void *out, void *workspace,
                           size_t workspace_bytes, pa_stream_t stream);
 
 /*

@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 PA_OK, PA_ERR_INVALID, PA_ERR_CUDA, PA_ERR_UNSUPPORTED = 0, 1, 2, 3
 PA_ERR_DEVICE_CHECK, PA_ERR_TIMEOUT, PA_ERR_WORKSPACE = 4, 5, 6
 PA_BF16, PA_FP16, PA_FP8_E4M3 = 0, 1, 2
+PA_ATTN_SHARED_BLOCKS = 1
 
 CHECK_BITS = {
     "empty_request": 1 << 0, "token_count": 1 << 1, "block_id": 1 << 2,
@@ -89,7 +90,7 @@ def lib():
             L.pa_attention_ex.restype = ctypes.c_int
             L.pa_attention_ex.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                           i32, i32, i32, i32, ctypes.c_float, ctypes.c_int,
-                                          ctypes.c_int, vp, vp, vp, vp, sz, vp]
+                                          ctypes.c_int, vp, vp, ctypes.c_uint32, vp, vp, sz, vp]
             L.pa_attention_noalloc.restype = ctypes.c_int
             L.pa_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                                i32, i32, i32, i32, i32, ctypes.c_float,
@@ -286,9 +287,12 @@ def pa_attention_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len
 
 def pa_attention(q, key_cache, value_cache, block_table, query_start_loc, seq_lens,
                  max_query_len, max_seq_len, scale, out, workspace=None, stream=None,
-                 k_scale=None, v_scale=None):
+                 k_scale=None, v_scale=None, shared_blocks=False):
     """Paged causal GQA attention: q [T, Hq, D] -> out [T, Hq, D].  FP8 pools
-    (uint8 / float8_e4m3fn) read element * k_scale / * v_scale."""
+    (uint8 / float8_e4m3fn) read element * k_scale / * v_scale.
+    ``shared_blocks``: block tables may share physical blocks across requests
+    (PA_ATTN_SHARED_BLOCKS); requests sharing whole partitions are computed
+    together."""
     T, hq, d = q.shape
     nb, bs, hkv, _ = key_cache.shape
     R = seq_lens.shape[0]
@@ -306,7 +310,8 @@ def pa_attention(q, key_cache, value_cache, block_table, query_start_loc, seq_le
         _dev(query_start_loc, "query_start_loc", torch.int32),
         _dev(seq_lens, "seq_lens", torch.int32), R, T, int(max_query_len), int(max_seq_len),
         hq, hkv, d, bs, nb, float(scale), dt, cdt, _scale_ptr(k_scale, "k_scale"),
-        _scale_ptr(v_scale, "v_scale"), _dev(out, "out"), ws_ptr, ws_bytes, _stream(stream))
+        _scale_ptr(v_scale, "v_scale"), PA_ATTN_SHARED_BLOCKS if shared_blocks else 0,
+        _dev(out, "out"), ws_ptr, ws_bytes, _stream(stream))
     _check(rc, "pa_attention")
 
 

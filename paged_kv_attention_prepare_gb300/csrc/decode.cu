@@ -50,6 +50,8 @@ constexpr int kPage = 16;         // tokens per cache block
 constexpr int kCandidates = 8;    // partition lengths p_min << k
 constexpr int kSingle = INT_MAX / 2;
 constexpr int kQueue = 8;         // item queue entries (producer -> consumer warps)
+constexpr int kGroupRows = 32;    // rows of a shared-partition group item (8 per consumer warp)
+constexpr int kGroupShift = 48;   // queue entry = item index | members << kGroupShift
 
 struct Params {
     CUtensorMap tmK;
@@ -336,7 +338,9 @@ template <> struct QConv<__nv_bfloat16, __half> {
 // the TMA swizzle, for each element size and head_dim.
 __device__ __forceinline__ int perm16(int k) { return ((0x27146350u >> (4 * (k & 7))) & 0xf) | (k & 8); }
 
-template <typename TQ, typename TC, int D, int RPI>
+// kGroups: shared-partition group items (callers whose block tables may
+// share physical blocks); the kernel without them has no code for them.
+template <typename TQ, typename TC, int D, int RPI, bool kGroups>
 __global__ void __launch_bounds__(kThreads, RPI == 8 ? 2 : kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ Params p) {
     using L = Lay<TC, D>;
@@ -359,12 +363,14 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     long long *qitem = reinterpret_cast<long long *>(qempty + kQueue);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // arrivals that release a stage: group items need all four warps
+    constexpr uint32_t kRelease = kGroups ? kConsumerWarps : 1;
 
     if (tid < kCandidates) cand[tid] = 0;
     if (tid == 0) {
         for (int s = 0; s < kSt; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kRelease);   // every warp of a group item, or the owner for all
         }
         mbar_init(cbar, kConsumerWarps);
         for (int e = 0; e < kQueue; ++e) {
@@ -435,6 +441,36 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     // consumer warps; without one, CTA b takes items b, b + grid, ...  Either
     // way a CTA's indices rise, as the walker needs.
 
+    // ---- shared-partition groups.  Requests of one query token whose block
+    // tables hold the same physical blocks over a whole partition that their
+    // query sees completely (a prefix shared after a fork or by prefix
+    // caching) read the same K/V there.  Runs of such requests, cut at
+    // multiples of kGroupRows / G in batch order, form one group item: the
+    // first request's item reads the pages once for every member's rows and
+    // the others' items for that partition are skipped.  Only with an item
+    // queue (the producer publishes the member count) and a partial slot for
+    // every partition.
+    const int gcap = (kGroups && p.item_counter && p.part_o && p.G <= 8 && kGroupRows % p.G == 0)
+                         ? kGroupRows / p.G : 0;   // members per group (0: no groups)
+    // partition s of the window's request at lane rl, fully visible to its
+    // single query token and part of a single row chunk
+    auto groupable = [&](int rl, int s) {
+        const int n = __shfl_sync(0xffffffffu, walk.n, rl);
+        const int L = __shfl_sync(0xffffffffu, walk.L, rl);
+        const int nc = __shfl_sync(0xffffffffu, walk.nchunks, rl);
+        return n == 1 && nc == 1 && (long long)(s + 1) * part <= L - 1;
+    };
+    // the same blocks for partition s in requests ra and rb (warp-wide)
+    auto same_blocks = [&](int ra, int rb, int s) {
+        const int P = part / kPage;
+        const int32_t *a = p.bt + (long long)ra * p.MB + (long long)s * P;
+        const int32_t *b = p.bt + (long long)rb * p.MB + (long long)s * P;
+        bool same = true;
+        for (int c0 = 0; same && c0 < P; c0 += 32)
+            same = __ballot_sync(0xffffffffu, c0 + lane < P && a[c0 + lane] != b[c0 + lane]) == 0;
+        return same;
+    };
+
     if (warp == kConsumerWarps) {
         // =================== producer warp ===================
         // Issue order: K unit 0, V unit 0, K unit 1, V unit 1, ... of each
@@ -446,20 +482,54 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         // pairs handed to each consumer warp so far, mod 256: one byte per warp
         uint32_t handed = 0;
         auto handed_to = [&](int w) { return (handed >> (8 * w)) & 0xffu; };
+        int blk0 = 0;            // the item's first 32 block ids, when already loaded
+        bool have_blk0 = false;
         bool ok = true;
-        for (long long k = 0; ok; ++k) {
+        for (long long k = 0; ok; ++k) {   // k: items published
             if (p.item_counter) {
                 unsigned int cand = 0;
-                if (lane == 0) cand = atomicAdd(p.item_counter, 1u);
-                cand = __shfl_sync(0xffffffffu, cand, 0);
-                const bool valid = walk.find((long long)cand, lane, it);
+                bool valid;
+                long long members = 0;
+                for (;;) {   // the next item that is not a group member's
+                    if (lane == 0) cand = atomicAdd(p.item_counter, 1u);
+                    cand = __shfl_sync(0xffffffffu, cand, 0);
+                    valid = walk.find((long long)cand, lane, it);
+                    have_blk0 = false;
+                    if (!valid || gcap == 0) break;
+                    const int rl = it.r - walk.rb;
+                    if (!groupable(rl, it.split)) break;
+                    // The item's first 32 block ids (its copies need them) and, in
+                    // the same round trip, the partition's first block id in the
+                    // neighbouring requests: only a match there calls for a full
+                    // comparison.
+                    const long long pg = (long long)it.split * (part / kPage);
+                    const bool prev_ok = it.r % gcap != 0 && groupable(rl - 1, it.split);
+                    const bool next_ok = (it.r + 1) % gcap != 0 && it.r + 1 < p.R &&
+                                         groupable(rl + 1, it.split);
+                    blk0 = p.bt[(long long)it.r * p.MB + pg + lane];   // a full partition: >= 32 pages
+                    int nb = -1;
+                    if (lane == 0 && prev_ok) nb = p.bt[(long long)(it.r - 1) * p.MB + pg];
+                    if (lane == 1 && next_ok) nb = p.bt[(long long)(it.r + 1) * p.MB + pg];
+                    have_blk0 = true;
+                    const int first = __shfl_sync(0xffffffffu, blk0, 0);
+                    const int prev = __shfl_sync(0xffffffffu, nb, 0), next = __shfl_sync(0xffffffffu, nb, 1);
+                    if (prev_ok && prev == first && same_blocks(it.r, it.r - 1, it.split))
+                        continue;   // a member: its group's first request covers it
+                    int m = 1;
+                    if (next_ok && next == first)
+                        while (m < gcap && (it.r + m) % gcap != 0 && it.r + m < p.R &&
+                               groupable(rl + m, it.split) && same_blocks(it.r + m, it.r, it.split))
+                            ++m;
+                    if (m > 1) members = m;
+                    break;
+                }
                 const int e = (int)(k % kQueue);
                 if (lane == 0) {
                     if (!mbar_wait(&qempty[e], (uint32_t)(((k / kQueue) & 1) ^ 1))) {
                         flag(p.status, PA_CHECK_TIMEOUT);
                         ok = false;
                     } else {
-                        qitem[e] = valid ? (long long)cand : -1;
+                        qitem[e] = valid ? ((long long)cand | (members << kGroupShift)) : -1;
                         mbar_arrive(&qfull[e]);
                     }
                 }
@@ -475,7 +545,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             for (int g0 = 0; ok && g0 < npages; g0 += 32) {
                 int blk = 0;
                 if (g0 + lane < npages) {
-                    blk = row[g0 + lane];
+                    blk = (g0 == 0 && have_blk0) ? blk0 : row[g0 + lane];
                     if (blk < 0 || blk >= p.NB) {
                         flag(p.status, PA_CHECK_BLOCK_ID);
                         blk = 0;
@@ -564,11 +634,9 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     static_assert(L::SR == 128 || NCH == 1, "one chunk per lane on 64-byte rows");
     const int koff_a = L::chunk_off(key_a, tq), koff_b = L::chunk_off(key_b, tq);
     auto koff = [&](int base, int jj) { return (base ^ (64 * (jj & 1))) + (jj >> 1) * L::kSubBytes; };
-    int vkey[4];                     // page rows of keys 2tq, 2tq + 1, 2tq + 8, 2tq + 9
-    vkey[0] = perm16(2 * tq);
-    vkey[1] = perm16(2 * tq + 1);
-    vkey[2] = perm16(2 * tq + 8);
-    vkey[3] = perm16(2 * tq + 9);
+    // page rows of keys 2tq, 2tq + 1, 2tq + 8, 2tq + 9 (recomputed where
+    // needed, which is only on partial pages: no registers held for them)
+    auto vkey = [&](int e) { return perm16(2 * tq + (e & 1) + 8 * (e >> 1)); };
     int voff[L::E == 2 ? 1 : 4];
     if constexpr (L::E == 2) {
         const int mi = lane >> 3;
@@ -576,14 +644,18 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     } else {
         const int byte = gq * (D / 8);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) voff[e] = L::chunk_off(vkey[e], byte / 16) + byte % 16;
+        for (int e = 0; e < 4; ++e) voff[e] = L::chunk_off(vkey(e), byte / 16) + byte % 16;
     }
     float *cw = comb + warp * C::kComb;
-    uint32_t taken = 0;              // unit pairs this warp has consumed
+    // Unit pairs handed to each warp's stages so far, mod 256: one byte per
+    // warp, kept exactly as the producer keeps it (with group items, whose
+    // units every warp reads); without them a warp counts only its own.
+    uint32_t handed = 0, taken = 0;
     uint32_t cpar = 0;
     bool ok = true;
     for (long long k = 0; ok; ++k) {
         long long i = blockIdx.x + k * gridDim.x;
+        int members = 0;             // > 1: a shared-partition group item
         if (p.item_counter) {
             const int e = (int)(k % kQueue);
             if (!mbar_wait_warp(&qfull[e], (uint32_t)((k / kQueue) & 1))) {
@@ -591,12 +663,15 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 ok = false;
                 break;
             }
-            i = qitem[e];
+            const long long v = qitem[e];
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty[e]);
-            if (i < 0) break;
+            if (v < 0) break;
+            i = v & ((1LL << kGroupShift) - 1);
+            if constexpr (kGroups) members = (int)(v >> kGroupShift);
         }
         if (!walk.find(i, lane, it)) break;
+        const bool grp = kGroups && members > 1;
         int k0, k1;
         item_keys<RPI>(p, it, part, k0, k1);
         const int npages = (k1 - k0 + kPage - 1) / kPage;
@@ -604,24 +679,41 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         const int nrows = it.n * p.G;
         const int pos0 = it.L - it.n;  // position of the request's first query token
         // last key each of this lane's two rows (2tq, 2tq + 1) may see; -1 for
-        // rows past the item
+        // rows past the item.  A group item's rows are 8 per warp (row 8 warp +
+        // x is member (8 warp + x) / G's head (8 warp + x) % G) and see the
+        // whole partition.
         int lim0 = -1, lim1 = -1;
-        {
+        if (grp) {
+            if (8 * warp + 2 * tq < members * p.G) lim0 = k1 - 1;
+            if (8 * warp + 2 * tq + 1 < members * p.G) lim1 = k1 - 1;
+        } else {
             const int r0 = it.chunk * RPI + 2 * tq, r1 = r0 + 1;
             if (2 * tq < RPI && r0 < nrows) lim0 = min(pos0 + r0 / p.G, k1 - 1);
             if (2 * tq + 1 < RPI && r1 < nrows) lim1 = min(pos0 + r1 / p.G, k1 - 1);
         }
         // Pages whose last key every row of the item sees need no mask (rows
         // past the item then pick up scores, but they are never written out).
-        const int lim_all = min(pos0 + (it.chunk * RPI) / p.G, k1 - 1);
+        const int lim_all = grp ? k1 - 1 : min(pos0 + (it.chunk * RPI) / p.G, k1 - 1);
 
-        // Q^T fragments (B operand): row gq of the item, this lane's dims.
+        // Q^T fragments (B operand): row gq of the item (of the warp's rows
+        // for a group), this lane's dims.
         uint32_t qf[KS][2];
         {
-            const int rr = it.chunk * RPI + gq;
-            const bool have = gq < RPI && rr < nrows;
-            const TQ *qrow = q + ((long long)(qstart + (have ? rr / p.G : 0)) * p.Hq + it.g * p.G +
-                                  (have ? rr % p.G : 0)) * D;
+            bool have;
+            long long tok;
+            int head;
+            if (grp) {
+                const int gr = 8 * warp + gq;
+                have = gr < members * p.G;
+                tok = qstart + (have ? gr / p.G : 0);   // members hold one token each, in order
+                head = have ? gr % p.G : 0;
+            } else {
+                const int rr = it.chunk * RPI + gq;
+                have = gq < RPI && rr < nrows;
+                tok = qstart + (have ? rr / p.G : 0);
+                head = have ? rr % p.G : 0;
+            }
+            const TQ *qrow = q + (tok * p.Hq + it.g * p.G + head) * D;
 #pragma unroll
             for (int jj = 0; jj < NCH; ++jj) {
                 const int d0 = (tq + 4 * jj) * (16 / L::E);   // first dim of the lane's chunk
@@ -646,13 +738,14 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
         constexpr int kSP = C::kSP;
         const int nunits = (npages + kSP - 1) / kSP;
-        for (int pu = warp; pu < nunits; pu += kConsumerWarps, ++taken) {
-            const uint32_t stK = pair_stage<C::kPairsPerWarp>(warp, taken), stV = stK + 1;
-            const uint32_t phK = (taken / C::kPairsPerWarp) & 1u, phV = phK;
+        // One unit pair (K, V): QK of its pages, one softmax update, PV, then
+        // the release (count: every warp of a group item arrives; an ordinary
+        // item's owner arrives for all).
+        auto run_unit = [&](int pu, uint32_t stK, uint32_t phK, uint32_t release) -> bool {
+            const uint32_t stV = stK + 1, phV = phK;
             if (!mbar_wait_warp(&full[stK], phK) || !mbar_wait_warp(&full[stV], phV)) {
                 flag(p.status, PA_CHECK_TIMEOUT);
-                ok = false;
-                break;
+                return false;
             }
             // The unit's pages: QK of each (independent MMA chains), one
             // softmax update over all their keys, then PV of each.
@@ -705,7 +798,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             if (!unit_visible) {
 #pragma unroll
                 for (int sp = 0; sp < kSP; ++sp) {
-                    const int pa = keyb[sp] + key_a, pb = keyb[sp] + key_b;
+                    const int pa = keyb[sp] + perm16(gq), pb = keyb[sp] + perm16(gq + 8);
                     sv[sp][0] = pa <= lim0 ? sv[sp][0] : -INFINITY;
                     sv[sp][1] = pa <= lim1 ? sv[sp][1] : -INFINITY;
                     sv[sp][2] = pb <= lim0 ? sv[sp][2] : -INFINITY;
@@ -775,8 +868,8 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 if constexpr (L::E == 2) {
                     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // keys (2tq, 2tq+1), (+8, +9)
                     if constexpr (!kFull) {
-                        mlo = (vkey[0] < nvalid ? 0x0000ffffu : 0u) | (vkey[1] < nvalid ? 0xffff0000u : 0u);
-                        mhi = (vkey[2] < nvalid ? 0x0000ffffu : 0u) | (vkey[3] < nvalid ? 0xffff0000u : 0u);
+                        mlo = (vkey(0) < nvalid ? 0x0000ffffu : 0u) | (vkey(1) < nvalid ? 0xffff0000u : 0u);
+                        mhi = (vkey(2) < nvalid ? 0x0000ffffu : 0u) | (vkey(3) < nvalid ? 0xffff0000u : 0u);
                     }
                     const uint32_t vbase = smem_u32(vpage);
 #pragma unroll
@@ -812,7 +905,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                             w[e][1] = v2.y;
                         }
                         if constexpr (!kFull) {
-                            const uint32_t keep = vkey[e] < nvalid ? 0xffffffffu : 0u;
+                            const uint32_t keep = vkey(e) < nvalid ? 0xffffffffu : 0u;
 #pragma unroll
                             for (int tp = 0; tp < NW; ++tp) w[e][tp] &= keep;
                         }
@@ -834,11 +927,84 @@ paged_decode_kernel(const __grid_constant__ Params p) {
           }
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&empty[stK]);
-                mbar_arrive(&empty[stV]);
+                mbar_arrive_n(&empty[stK], release);
+                mbar_arrive_n(&empty[stV], release);
+            }
+            return true;
+        };
+        // Unit j sits in the next stage pair of warp j mod 4.  A warp takes
+        // its own units of an ordinary item, every unit of a group item.
+        if (!grp) {
+            uint32_t c = kGroups ? (handed >> (8 * warp)) & 0xffu : taken;
+            for (int pu = warp; ok && pu < nunits; pu += kConsumerWarps, ++c)
+                ok = run_unit(pu, pair_stage<C::kPairsPerWarp>(warp, c), (c / C::kPairsPerWarp) & 1u,
+                              kRelease);
+            if constexpr (!kGroups) taken = c;
+        } else {
+            for (int pu = 0; ok && pu < nunits; ++pu) {
+                const int ow = pu % kConsumerWarps;
+                const uint32_t c = ((handed >> (8 * ow)) & 0xffu) + (uint32_t)(pu / kConsumerWarps);
+                ok = run_unit(pu, pair_stage<C::kPairsPerWarp>(ow, c), (c / C::kPairsPerWarp) & 1u, 1u);
             }
         }
         if (!ok) break;
+        if constexpr (kGroups) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const uint32_t units = nunits > w ? (uint32_t)((nunits - w + kConsumerWarps - 1) / kConsumerWarps) : 0u;
+                const uint32_t c = (((handed >> (8 * w)) & 0xffu) + units) & 0xffu;
+                handed = (handed & ~(0xffu << (8 * w))) | (c << (8 * w));
+            }
+        }
+
+        if (grp) {
+            // ---- each warp's rows are complete: write them to their members'
+            //      partial slots (the merge pass combines the partitions)
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+            }
+            // partial slot of the member holding row 8 warp + x, from the
+            // walker's window (a group never crosses a 32-request window)
+            auto slot_of = [&](int x) -> long long {
+                const int gr = 8 * warp + x;
+                const int rl = it.r - walk.rb + min(gr / p.G, members - 1);
+                const int items = __shfl_sync(0xffffffffu, walk.items, rl);
+                const int pincl = __shfl_sync(0xffffffffu, walk.pincl, rl);
+                const int nsp = __shfl_sync(0xffffffffu, walk.nsplit, rl);
+                return walk.pslot_base + (pincl - items) + (long long)it.g * nsp + it.split;
+            };
+            const long long ps0 = slot_of(2 * tq), ps1 = slot_of(2 * tq + 1);
+            const int h0 = (8 * warp + 2 * tq) % p.G, h1 = (8 * warp + 2 * tq + 1) % p.G;
+            const bool v0 = lim0 >= 0, v1 = lim1 >= 0;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                int dlo, dhi;
+                if constexpr (L::E == 2) {
+                    dlo = 16 * mt + gq;
+                    dhi = dlo + 8;
+                } else {
+                    dlo = gq * (D / 8) + 4 * (mt >> 1) + 2 * (mt & 1);
+                    dhi = dlo + 1;
+                }
+                if (v0) {
+                    float *po = p.part_o + (ps0 * RPI + h0) * D;
+                    po[dlo] = o[mt][0] * vs;
+                    po[dhi] = o[mt][2] * vs;
+                }
+                if (v1) {
+                    float *po = p.part_o + (ps1 * RPI + h1) * D;
+                    po[dlo] = o[mt][1] * vs;
+                    po[dhi] = o[mt][3] * vs;
+                }
+            }
+            if (gq == 0) {
+                if (v0) *reinterpret_cast<float2 *>(p.part_ml + (ps0 * RPI + h0) * 2) = make_float2(m0, l0);
+                if (v1) *reinterpret_cast<float2 *>(p.part_ml + (ps1 * RPI + h1) * 2) = make_float2(m1, l1);
+            }
+            continue;
+        }
 
         // ---- combine the four warps' states and write the item out
 #pragma unroll
@@ -926,7 +1092,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     // every queue entry and the item barrier once, so the others' bounded
     // waits and the producer's drain can finish.
     if (!ok && lane == 0) {
-        for (int s = 0; s < kSt; ++s) mbar_arrive(&empty[s]);
+        for (int s = 0; s < kSt; ++s) mbar_arrive_n(&empty[s], kRelease);
         for (int e = 0; e < kQueue; ++e) mbar_arrive(&qempty[e]);
         mbar_arrive(cbar);
     }
@@ -1098,18 +1264,18 @@ static pa_status launch_merge(const Params &prm, cudaStream_t stream) {
     return PA_OK;
 }
 
-template <typename TQ, typename TC, int D, int RPI>
-pa_status launch_typed(Params &prm, long long max_items, long long merge_splits, cudaStream_t stream) {
+template <typename TQ, typename TC, int D, int RPI, bool kGroups>
+pa_status launch_split_k(Params &prm, long long max_items, cudaStream_t stream) {
     using S = Cfg<TC, D, RPI>;
     static int resident[64] = {};  // CTAs per SM, per device
     int dev = 0;
     PA_TRY_CUDA(cudaGetDevice(&dev));
     int per_sm = dev < 64 ? resident[dev] : 0;
     if (per_sm == 0) {
-        PA_TRY_CUDA(cudaFuncSetAttribute(paged_decode_kernel<TQ, TC, D, RPI>,
+        PA_TRY_CUDA(cudaFuncSetAttribute(paged_decode_kernel<TQ, TC, D, RPI, kGroups>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes));
         PA_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, paged_decode_kernel<TQ, TC, D, RPI>, kThreads, S::kBytes));
+            &per_sm, paged_decode_kernel<TQ, TC, D, RPI, kGroups>, kThreads, S::kBytes));
         if (per_sm < 1) return PA_ERR_UNSUPPORTED;
         if (dev < 64) resident[dev] = per_sm;
     }
@@ -1117,9 +1283,18 @@ pa_status launch_typed(Params &prm, long long max_items, long long merge_splits,
     long long grid = (long long)per_sm * num_sms();
     if (max_items < grid) grid = max_items;
     if (grid < 1) grid = 1;
-    paged_decode_kernel<TQ, TC, D, RPI><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
+    paged_decode_kernel<TQ, TC, D, RPI, kGroups><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
+    return PA_OK;
+}
+
+template <typename TQ, typename TC, int D, int RPI>
+pa_status launch_typed(Params &prm, long long max_items, long long merge_splits, bool groups,
+                       cudaStream_t stream) {
+    const pa_status st = groups ? launch_split_k<TQ, TC, D, RPI, true>(prm, max_items, stream)
+                                : launch_split_k<TQ, TC, D, RPI, false>(prm, max_items, stream);
+    if (st != PA_OK) return st;
     if (merge_splits > 0 && prm.R > 0) {
         switch (merge_warps_per_head(merge_splits, prm.R, prm.Hq)) {
             case 1: return launch_merge<TQ, D, RPI, 1>(prm, stream);
@@ -1132,23 +1307,24 @@ pa_status launch_typed(Params &prm, long long max_items, long long merge_splits,
 }
 
 template <typename TQ, typename TC, int D>
-pa_status dispatch_rpi(int rpi, Params &prm, long long grid, long long merge, cudaStream_t stream) {
+pa_status dispatch_rpi(int rpi, Params &prm, long long grid, long long merge, bool groups,
+                       cudaStream_t stream) {
     switch (rpi) {
-        case 1: return launch_typed<TQ, TC, D, 1>(prm, grid, merge, stream);
-        case 2: return launch_typed<TQ, TC, D, 2>(prm, grid, merge, stream);
-        case 4: return launch_typed<TQ, TC, D, 4>(prm, grid, merge, stream);
-        default: return launch_typed<TQ, TC, D, 8>(prm, grid, merge, stream);
+        case 1: return launch_typed<TQ, TC, D, 1>(prm, grid, merge, groups, stream);
+        case 2: return launch_typed<TQ, TC, D, 2>(prm, grid, merge, groups, stream);
+        case 4: return launch_typed<TQ, TC, D, 4>(prm, grid, merge, groups, stream);
+        default: return launch_typed<TQ, TC, D, 8>(prm, grid, merge, groups, stream);
     }
 }
 
 template <typename TQ>
 pa_status dispatch_cache(bool fp8, int D, int rpi, Params &prm, long long grid, long long merge,
-                         cudaStream_t stream) {
+                         bool groups, cudaStream_t stream) {
     if (fp8)
-        return D == 128 ? dispatch_rpi<TQ, Fp8E4M3, 128>(rpi, prm, grid, merge, stream)
-                        : dispatch_rpi<TQ, Fp8E4M3, 64>(rpi, prm, grid, merge, stream);
-    return D == 128 ? dispatch_rpi<TQ, TQ, 128>(rpi, prm, grid, merge, stream)
-                    : dispatch_rpi<TQ, TQ, 64>(rpi, prm, grid, merge, stream);
+        return D == 128 ? dispatch_rpi<TQ, Fp8E4M3, 128>(rpi, prm, grid, merge, groups, stream)
+                        : dispatch_rpi<TQ, Fp8E4M3, 64>(rpi, prm, grid, merge, groups, stream);
+    return D == 128 ? dispatch_rpi<TQ, TQ, 128>(rpi, prm, grid, merge, groups, stream)
+                    : dispatch_rpi<TQ, TQ, 64>(rpi, prm, grid, merge, groups, stream);
 }
 
 // Rows per item: all heads of a kv group (at most 8, the register budget).
@@ -1165,6 +1341,9 @@ inline int rows_per_item(int G, int max_q) {
 }
 
 constexpr int kPreferredPartition = 512;
+// A whole partition holds at least 32 pages: the split-K kernel's group check
+// reads a partition's first 32 block ids at once.
+static_assert(kPreferredPartition % (32 * kPage) == 0, "partitions of whole 32-page groups");
 constexpr size_t kAlign = 256;
 
 inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -1250,9 +1429,11 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
 
     // the merge pass (when partitions exist) sizes itself by the most partitions a request can have
     const long long merge_splits = merge ? splits : 0;
+    // group items need the partial slots (a merge pass) and the item queue
+    const bool groups = (a.flags & PA_ATTN_SHARED_BLOCKS) && merge && a.ctrl;
     return a.dtype == PA_BF16
-               ? dispatch_cache<__nv_bfloat16>(fp8, a.D, rpi, prm, grid, merge_splits, stream)
-               : dispatch_cache<__half>(fp8, a.D, rpi, prm, grid, merge_splits, stream);
+               ? dispatch_cache<__nv_bfloat16>(fp8, a.D, rpi, prm, grid, merge_splits, groups, stream)
+               : dispatch_cache<__half>(fp8, a.D, rpi, prm, grid, merge_splits, groups, stream);
 }
 
 }  // namespace pa

@@ -318,7 +318,7 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
     return pa_attention_ex(q, key_cache, value_cache, block_table, max_blocks_per_req,
                            query_start_loc, seq_lens, num_reqs, num_tokens, max_query_len,
                            max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                           num_blocks, scale, dtype, dtype, nullptr, nullptr, out, workspace,
+                           num_blocks, scale, dtype, dtype, nullptr, nullptr, 0u, out, workspace,
                            workspace_bytes, stream);
 }
 
@@ -329,8 +329,9 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
                           int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                           int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
                           pa_dtype dtype, pa_dtype cache_dtype, const float *k_scale,
-                          const float *v_scale, void *out, void *workspace,
+                          const float *v_scale, uint32_t flags, void *out, void *workspace,
                           size_t workspace_bytes, pa_stream_t stream) {
+    if (flags & ~PA_ATTN_SHARED_BLOCKS) return PA_ERR_INVALID;
     if (num_reqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0 ||
         num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks < 0 || max_blocks_per_req < 0 || (dtype != PA_BF16 && dtype != PA_FP16))
@@ -371,6 +372,7 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
     a.k_scale = cache_dtype == PA_FP8_E4M3 ? k_scale : nullptr;
     a.v_scale = cache_dtype == PA_FP8_E4M3 ? v_scale : nullptr;
     a.out = out;
+    a.flags = flags;
     // The workspace starts with a small control block (the kernels' item
     // counters); the split-K partials take the rest.
     a.ctrl = nullptr;

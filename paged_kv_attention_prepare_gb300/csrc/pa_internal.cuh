@@ -76,6 +76,7 @@ struct AttnArgs {
     void *ws;              // decode partials (after the control block)
     size_t ws_bytes;
     unsigned int *ctrl;    // control block at the workspace's start (NULL: none)
+    uint32_t flags;        // PA_ATTN_* bits
 };
 
 // Bytes at the start of a caller's workspace kept for per-call counters.
@@ -131,6 +132,11 @@ __device__ __forceinline__ void fence_mbar_init() {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {

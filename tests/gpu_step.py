@@ -13,12 +13,17 @@ def to_dev(a, dev="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
-def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda"):
+def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda",
+             shared_blocks=None):
     """prep -> cache write -> attention on the GPU, on copies of the pools.
 
     ``vals`` holds the generator's tensors (any device).  Returns a dict with
     host numpy index arrays, the written pools (torch, on the GPU), the
-    attention output (torch, on the GPU) and the status word."""
+    attention output (torch, on the GPU) and the status word.
+    ``shared_blocks`` (the PA_ATTN_SHARED_BLOCKS flag) defaults to whether
+    the workload's tables share blocks."""
+    if shared_blocks is None:
+        shared_blocks = w.shares_blocks
     i32 = torch.int32
     R, T = w.num_reqs, w.num_tokens
     cap = R + 1 if qsl_capacity is None else qsl_capacity
@@ -49,7 +54,8 @@ def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda"):
     ws = torch.empty(max(int(workspace_bytes), 1), dtype=torch.uint8, device=dev)
     pa.pa_attention(q, kc, vc, bt, out["query_start_loc"][: R + 1], out["seq_lens"],
                     w.max_query_len, w.max_seq_len, w.scale, o,
-                    ws if workspace_bytes else None, k_scale=ks, v_scale=vs)
+                    ws if workspace_bytes else None, k_scale=ks, v_scale=vs,
+                    shared_blocks=shared_blocks)
     status, detail = pa.pa_get_status()
     res = {k: v.cpu().numpy() for k, v in out.items()}
     res.update(key_cache=kc, value_cache=vc, out=o, status=status, detail=detail)

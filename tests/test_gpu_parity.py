@@ -112,6 +112,63 @@ def test_many_partitions_merge(longest, hq, hkv):
     _check_attention(res, ref)
 
 
+def _shared_runs_case(seed, group, hkv, dtype, nreq=14):
+    """Decode requests whose block tables share 80 blocks (1280 tokens: two
+    whole 512-key partitions and a quarter of a third), each with its own
+    tail; request 5 diverges inside the second partition, request 7 is a
+    3-token chunk, and the last two requests share nothing."""
+    rng = np.random.default_rng(seed)
+    bs, shared_n = 16, 80
+    tails = rng.integers(2, 40, size=nreq)          # private blocks after the prefix
+    need = shared_n + int(tails.sum()) + 1 + 2 * 120
+    nb = int(need * 1.1) + 8
+    perm = [int(b) for b in rng.permutation(nb)]
+    shared, k = perm[:shared_n], shared_n
+    rows, nst, nct = [], [], []
+    for r in range(nreq):
+        if r >= nreq - 2:                            # unrelated requests
+            own = perm[k:k + 120]
+            k += 120
+            rows.append(own)
+            ctx = 120 * bs - int(rng.integers(0, 15))
+        else:
+            own = perm[k:k + int(tails[r])]
+            k += int(tails[r])
+            row = list(shared) + own
+            if r == 5:                               # one block of the second partition differs
+                row[40] = perm[k]
+                k += 1
+            rows.append(row)
+            ctx = len(row) * bs - int(rng.integers(0, 15))
+        n = 3 if r == 7 else 1
+        nst.append(n)
+        nct.append(ctx - n)
+    bt = workloads._tables(rows)
+    uniq = np.unique(bt[bt >= 0]).size
+    return workloads.Workload(f"shared-runs-{seed}", np.array(nst, np.int32),
+                              np.array(nct, np.int32), bt, nb, bs, hkv * group, hkv, 128, dtype,
+                              uniq)
+
+
+@pytest.mark.parametrize("group,hkv,dtype,fp8", [(4, 2, "bf16", False), (1, 2, "fp16", False),
+                                                 (8, 1, "bf16", False), (2, 3, "bf16", False),
+                                                 (3, 2, "fp16", False), (4, 2, "bf16", True)])
+def test_shared_partition_groups(group, hkv, dtype, fp8):
+    # Requests reading the same blocks over whole partitions are computed as
+    # one group item (up to 32 rows); the rest as usual.  Same results as
+    # the oracle, which reads every request's blocks on its own.
+    w = _shared_runs_case(group * 10 + hkv, group, hkv, dtype)
+    if fp8:
+        w = workloads.fp8(w, k_scale=0.3, v_scale=0.2)
+    assert w.shares_blocks
+    vals = workloads.make_values(w, 5)
+    _, _, _, ref = _oracle_step(w, vals)
+    for shared in (True, False):   # with and without the group kernel
+        res = run_step(w, vals, shared_blocks=shared)
+        assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+        _check_attention(res, ref)
+
+
 @pytest.mark.parametrize("group,ws", [(4, None), (8, None), (1, 0)])
 def test_prompt_chunk_longer_than_a_partition(group, ws):
     # A 600-token chunk at 300 computed spans two 512-key partitions: its first

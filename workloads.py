@@ -100,6 +100,14 @@ class Workload:
         elt = 1 if self.kv_cache_dtype == "fp8_e4m3" else 2
         return int(self.context_lens.sum()) * 2 * self.num_kv_heads * self.head_dim * elt
 
+    @property
+    def shares_blocks(self) -> bool:
+        """Some physical block is referenced by more than one request's
+        context (copy-on-write or prefix sharing)."""
+        nblk = -(-self.context_lens // self.block_size)
+        ids = self.block_table[np.arange(self.block_table.shape[1])[None, :] < nblk[:, None]]
+        return np.unique(ids).size < ids.size
+
     def kv_unique_bytes(self) -> int:
         """Bytes of K and V in the distinct blocks the tables reference."""
         elt = 1 if self.kv_cache_dtype == "fp8_e4m3" else 2
