@@ -130,7 +130,7 @@ def sub_batch(w, mask, q, bt_dev, qsl_host, sl_host, dev):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("decode.cu", "pa_internal.cuh"):
+    for name in ("decode.cu", "decode_fp16.cu", "pa_internal.cuh"):
         with open(os.path.join(ROOT, "paged_kv_attention_prepare_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

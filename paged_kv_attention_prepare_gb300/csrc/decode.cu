@@ -1327,6 +1327,18 @@ pa_status dispatch_cache(bool fp8, int D, int rpi, Params &prm, long long grid, 
                     : dispatch_rpi<TQ, TQ, 64>(rpi, prm, grid, merge, groups, stream);
 }
 
+// The fp16 instantiations compile in a translation unit of their own
+// (decode_fp16.cu includes this file with PA_DECODE_FP16_UNIT defined), in
+// parallel with the bf16 ones here.
+pa_status dispatch_fp16(bool fp8, int D, int rpi, Params &prm, long long grid, long long merge,
+                        bool groups, cudaStream_t stream);
+#ifdef PA_DECODE_FP16_UNIT
+pa_status dispatch_fp16(bool fp8, int D, int rpi, Params &prm, long long grid, long long merge,
+                        bool groups, cudaStream_t stream) {
+    return dispatch_cache<__half>(fp8, D, rpi, prm, grid, merge, groups, stream);
+}
+#endif
+
 // Rows per item: all heads of a kv group (at most 8, the register budget).
 // With 4+ heads per group a single-token decode already fills the item, so
 // short multi-token requests are split into more items rather than making
@@ -1350,6 +1362,7 @@ inline size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 }  // namespace decode
 
+#ifndef PA_DECODE_FP16_UNIT
 size_t decode_workspace_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq, int32_t Hq,
                              int32_t Hkv, int32_t D) {
     using namespace decode;
@@ -1433,7 +1446,8 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     const bool groups = (a.flags & PA_ATTN_SHARED_BLOCKS) && merge && a.ctrl;
     return a.dtype == PA_BF16
                ? dispatch_cache<__nv_bfloat16>(fp8, a.D, rpi, prm, grid, merge_splits, groups, stream)
-               : dispatch_cache<__half>(fp8, a.D, rpi, prm, grid, merge_splits, groups, stream);
+               : dispatch_fp16(fp8, a.D, rpi, prm, grid, merge_splits, groups, stream);
 }
+#endif  // PA_DECODE_FP16_UNIT
 
 }  // namespace pa

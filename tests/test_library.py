@@ -68,6 +68,16 @@ def test_attention_rejects_bad_arguments(case):
     assert rc == expect
 
 
+@pytest.mark.parametrize("flags", [2, 0x80000000, 3])
+def test_attention_ex_rejects_unknown_flags(flags):
+    # PA_ATTN_SHARED_BLOCKS is the only flag; any other bit is refused before
+    # anything is launched
+    L = pa.lib()
+    rc = L.pa_attention_ex(FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 2, 1, 16, 4, 2, 64, 16, 8,
+                           0.1, pa.PA_BF16, pa.PA_BF16, None, None, flags, FAKE, None, 0, None)
+    assert rc == pa.PA_ERR_INVALID
+
+
 def test_prepare_rejects_small_qsl_capacity_and_huge_pool():
     L = pa.lib()
     assert L.pa_prepare_inputs(FAKE, FAKE, FAKE, 3, 2, 16, 5, 8, FAKE, FAKE, FAKE, FAKE, 3,
