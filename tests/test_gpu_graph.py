@@ -158,12 +158,14 @@ def test_attention_is_deterministic(name):
                                             w.max_seq_len, w.num_q_heads, w.num_kv_heads,
                                             w.head_dim)
     ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    shared = w.shares_blocks    # the shared-prefix step runs its group items
     outs = []
     for _ in range(3):
         out = torch.full_like(vals["q"], float("nan"))
         pa.pa_attention(vals["q"], vals["key_cache"], vals["value_cache"], bt, qsl, sl,
                         w.max_query_len, w.max_seq_len, w.scale, out, ws,
-                        k_scale=vals.get("k_scale"), v_scale=vals.get("v_scale"))
+                        k_scale=vals.get("k_scale"), v_scale=vals.get("v_scale"),
+                        shared_blocks=shared)
         outs.append(out)
     torch.cuda.synchronize()
     assert pa.pa_get_status() == (pa.PA_OK, 0)

@@ -169,6 +169,22 @@ def test_shared_partition_groups(group, hkv, dtype, fp8):
         _check_attention(res, ref)
 
 
+@pytest.mark.parametrize("shrink", [2, 4, 16])
+def test_shared_partition_groups_with_longer_partitions(shrink):
+    # A smaller workspace makes the kernel pick longer partitions (1024+
+    # keys: 64+ pages compared per group check); groups then cover fewer,
+    # longer partitions and the last partial one stays per request.
+    w = _shared_runs_case(99 + shrink, 4, 2, "bf16", nreq=20)
+    vals = workloads.make_values(w, 7)
+    full = pa.pa_attention_workspace_size(w.num_reqs, w.num_tokens, w.max_query_len,
+                                          w.max_seq_len, w.num_q_heads, w.num_kv_heads,
+                                          w.head_dim)
+    _, _, _, ref = _oracle_step(w, vals)
+    res = run_step(w, vals, workspace_bytes=max(full // shrink, 4096), shared_blocks=True)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_attention(res, ref)
+
+
 @pytest.mark.parametrize("group,ws", [(4, None), (8, None), (1, 0)])
 def test_prompt_chunk_longer_than_a_partition(group, ws):
     # A 600-token chunk at 300 computed spans two 512-key partitions: its first
