@@ -738,9 +738,10 @@ paged_decode_kernel(const __grid_constant__ Params p) {
 
         constexpr int kSP = C::kSP;
         const int nunits = (npages + kSP - 1) / kSP;
-        // One unit pair (K, V): QK of its pages, one softmax update, PV, then
-        // the release (count: every warp of a group item arrives; an ordinary
-        // item's owner arrives for all).
+        // One unit pair (K, V): QK of its pages and the release of K's stage,
+        // one softmax update, PV and the release of V's stage (count: every
+        // warp of a group item arrives; an ordinary item's owner arrives for
+        // all).
         auto run_unit = [&](int pu, uint32_t stK, uint32_t phK, uint32_t release) -> bool {
             const uint32_t stV = stK + 1, phV = phK;
             if (!mbar_wait_warp(&full[stK], phK) || !mbar_wait_warp(&full[stV], phV)) {
@@ -790,6 +791,10 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 for (int e = 0; e < 4; ++e) sv[sp][e] = have[sp] ? (sa[e] + sb[e]) * qs : -INFINITY;
             }
             const bool unit_visible = keyb[kSP - 1] + kPage - 1 <= lim_all && have[kSP - 1];
+            // K is in registers now: its stage goes back to the producer half a
+            // unit before V's.
+            __syncwarp();
+            if (lane == 0) mbar_arrive_n(&empty[stK], release);
 
             // ---- online softmax with a lazily moved reference max: P stays
             //      below 2^8, so the 16-bit P and the f32 sums are exact enough,
@@ -926,10 +931,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             else pv_page(std::false_type{});
           }
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_n(&empty[stK], release);
-                mbar_arrive_n(&empty[stV], release);
-            }
+            if (lane == 0) mbar_arrive_n(&empty[stV], release);
             return true;
         };
         // Unit j sits in the next stage pair of warp j mod 4.  A warp takes
