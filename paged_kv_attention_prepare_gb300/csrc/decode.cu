@@ -20,10 +20,11 @@
 //     launch is needed.
 //   * One producer warp issues swizzled 3-D TMA copies of 16-token pages of
 //     one kv head into a 16-stage shared-memory ring, driven by the block
-//     table: K unit, V unit, ... where a unit is one page (two for FP8
-//     pools).  Unit j of an item goes to consumer warp j mod 4.  mbarriers:
-//     full (TMA bytes) and empty (one arrive by the owning warp); every wait
-//     is bounded.
+//     table: K unit, V unit, ... where a unit is the consecutive pages that
+//     fill 4 KiB (one 16-bit page at head_dim 128, up to four FP8 pages at
+//     head_dim 64).  Unit j of an item goes to consumer warp j mod 4.
+//     mbarriers: full (TMA bytes) and empty (the consumers' release); every
+//     wait is bounded.
 //   * Consumers run on the tensor cores with mma.sync (m16n8k16, f32
 //     accumulate): S^T = K Q^T and O^T += V^T P^T per page, the item's rows
 //     as the MMA's N, an online softmax per warp, the four warps' states
@@ -112,9 +113,12 @@ template <typename TQ> struct MmaIn<TQ, Fp8E4M3> { using type = __half; };
 template <typename TC, int D, int RPI>
 struct Cfg {
     using L = Lay<TC, D>;
-    // Pages per ring stage: an FP8 page is half the bytes of a 16-bit one, so
-    // two consecutive pages of a request share a stage and one handoff.
-    static constexpr int kSP = L::E == 1 ? 2 : 1;
+    // Pages per ring stage: consecutive pages of a request share a stage and
+    // one handoff up to 4 KiB (one 16-bit page at head_dim 128; two at
+    // head_dim 64 or FP8; four FP8 pages at head_dim 64), so every layout
+    // keeps the same bytes in flight.  With 2 KiB stages head_dim 64 streamed
+    // at 4.6 TB/s, with 4 KiB at 5.5-6.0.
+    static constexpr int kSP = L::kPageBytes >= 4096 ? 1 : 4096 / L::kPageBytes;
     static constexpr int kUnitBytes = kSP * L::kPageBytes;
     // 64 KB of pages in flight per CTA at head_dim 128
     static constexpr int kStages = 16;
