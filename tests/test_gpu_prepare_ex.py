@@ -162,6 +162,16 @@ def test_random_batches_vs_oracle(seed, r, drafted):
     _compare(_run_ex(nst, nct, bt, bs, t, nb, **kw), _oracle_ex(nst, nct, bt, bs, t, nb, **kw))
 
 
+@pytest.mark.parametrize("r", [12_289, 50_000])
+def test_many_requests(r):
+    # The request starts of every CTA sit in shared memory (up to 200 KB);
+    # 50,000 requests is the documented maximum.
+    nst, nct, bt, bs, t, nb = _random_batch(r, r, 4, 120)
+    kw = dict(totals=workloads.make_request_totals(
+        workloads.Workload("many", nst, nct, bt, nb, bs, 8, 8, 64, "bf16"), 3))
+    _compare(_run_ex(nst, nct, bt, bs, t, nb, **kw), _oracle_ex(nst, nct, bt, bs, t, nb, **kw))
+
+
 def test_extended_call_matches_the_plain_call():
     nst, nct, bt, bs, t, nb = _random_batch(9, 700, 30, 2000)
     res = _run_ex(nst, nct, bt, bs, t, nb, with_cu=False)
