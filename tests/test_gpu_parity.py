@@ -169,6 +169,64 @@ def test_shared_partition_groups(group, hkv, dtype, fp8):
         _check_attention(res, ref)
 
 
+def _random_sharing_case(seed):
+    """Random requests over a pool where runs of requests share a prefix of
+    random length (0-3 partitions and a bit), some diverging at a random
+    block, some holding several query tokens; random head shapes."""
+    rng = np.random.default_rng(1000 + seed)
+    bs = 16
+    group = int(rng.choice([1, 2, 3, 4, 8]))
+    hkv = int(rng.choice([1, 2, 4]))
+    d = int(rng.choice([64, 128]))
+    dtype = str(rng.choice(["bf16", "fp16"]))
+    nreq = int(rng.integers(2, 40))
+    rows, nst, nct, k = [], [], [], 0
+    nb = 60_000
+    perm = [int(b) for b in rng.permutation(nb)]
+    r = 0
+    while r < nreq:
+        run = int(rng.integers(1, 12))
+        shared = perm[k:k + int(rng.integers(0, 110))]
+        k += len(shared)
+        for _ in range(min(run, nreq - r)):
+            row = list(shared)
+            if row and rng.random() < 0.2:            # diverge at a random block
+                row[int(rng.integers(0, len(row)))] = perm[k]
+                k += 1
+            tail = int(rng.integers(1, 30))
+            row += perm[k:k + tail]
+            k += tail
+            n = 1 if rng.random() < 0.85 else int(rng.integers(2, 6))
+            ctx = len(row) * bs - int(rng.integers(0, bs - n + 1))
+            rows.append(row)
+            nst.append(n)
+            nct.append(ctx - n)
+            r += 1
+    bt = workloads._tables(rows)
+    used = np.unique(bt[bt >= 0])
+    # compact the pool to the blocks in use (ids remapped), plus a few spares
+    remap = {int(b): i for i, b in enumerate(used)}
+    bt = np.vectorize(lambda b: remap.get(int(b), -1))(bt).astype(np.int32)
+    w = workloads.Workload(f"rand-share-{seed}", np.array(nst, np.int32), np.array(nct, np.int32),
+                           bt, len(used) + 4, bs, hkv * group, hkv, d, dtype, len(used))
+    if rng.random() < 0.25:
+        w = workloads.fp8(w, k_scale=0.3, v_scale=0.2)
+    return w, float(rng.choice([1, 1, 2, 8]))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_sharing_patterns(seed):
+    w, shrink = _random_sharing_case(seed)
+    vals = workloads.make_values(w, seed)
+    full = pa.pa_attention_workspace_size(w.num_reqs, w.num_tokens, w.max_query_len,
+                                          w.max_seq_len, w.num_q_heads, w.num_kv_heads,
+                                          w.head_dim)
+    _, _, _, ref = _oracle_step(w, vals)
+    res = run_step(w, vals, workspace_bytes=max(int(full / shrink), 4096), shared_blocks=True)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_attention(res, ref)
+
+
 @pytest.mark.parametrize("shrink", [2, 4, 16])
 def test_shared_partition_groups_with_longer_partitions(shrink):
     # A smaller workspace makes the kernel pick longer partitions (1024+
