@@ -82,8 +82,9 @@ enum {
     PA_CHECK_BLOCK_ID = 1u << 2,       /* block_table entry outside [0, num_blocks) */
     PA_CHECK_LOGICAL_BLOCK = 1u << 3,  /* position / block_size >= max_blocks_per_req */
     PA_CHECK_SLOT = 1u << 4,           /* slot_mapping entry >= num_blocks * block_size */
-    PA_CHECK_SEQ_LEN = 1u << 5,        /* seq_lens[r] < query length, qsl decreasing, or
-                                          a context wider than the table */
+    PA_CHECK_SEQ_LEN = 1u << 5,        /* seq_lens[r] < query length, qsl decreasing, a
+                                          context wider than the table, or (attention)
+                                          seq_lens[r] > max_seq_len */
     PA_CHECK_TIMEOUT = 1u << 6,        /* a bounded wait inside a kernel ran out */
     PA_CHECK_TOKEN_INDEX = 1u << 7,    /* a token's position >= max_model_len (its id
                                           would come from another request's row) */
@@ -330,7 +331,9 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens,
  *                 this step's K/V (pa_cache_write first, same stream)
  *   block_table   device int32 [num_reqs][max_blocks_per_req]
  *   query_start_loc device int32 [num_reqs + 1]; seq_lens device int32 [num_reqs]
- *   max_query_len, max_seq_len  host upper bounds of q length / seq_lens
+ *   max_query_len, max_seq_len  host upper bounds of q length / seq_lens (a
+ *                 request with seq_lens[r] > max_seq_len is flagged
+ *                 PA_CHECK_SEQ_LEN and left out)
  *   head_dim      64 or 128; block_size 16; num_q_heads % num_kv_heads == 0
  *   scale         softmax scale (usually 1/sqrt(head_dim))
  *   out           device [num_tokens][num_q_heads][head_dim]

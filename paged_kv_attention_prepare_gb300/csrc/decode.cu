@@ -70,7 +70,9 @@ struct Params {
                                  // free up (NULL: fixed stride over the items)
     int R, T, MB, NB, Hq, Hkv, G;
     int tau;              // requests with more query tokens are not handled here
+    int max_seq;          // the caller's bound on seq_lens (longer requests are flagged)
     int p_min;            // preferred partition length in keys (multiple of 256)
+    int part_fixed;       // the workspace holds every partial at p_min: no choice to make
     float qscale;         // softmax scale * log2(e)
     const float *k_scale; // FP8 pools: cached value = element * scale (device scalars)
     const float *v_scale;
@@ -171,7 +173,7 @@ struct Walker {
             const int a = p->qsl[r], b = p->qsl[r + 1];
             n = b - a;
             L = p->seq_lens[r];
-            const bool sane = a >= 0 && b <= p->T && n >= 0 && L >= n &&
+            const bool sane = a >= 0 && b <= p->T && n >= 0 && L >= n && L <= p->max_seq &&
                               (L + kPage - 1) / kPage <= p->MB;
             if (!sane) flag(p->status, PA_CHECK_SEQ_LEN);
             if (sane && n >= 1 && n <= p->tau) {
@@ -395,12 +397,12 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         unsigned long long local[kCandidates];
 #pragma unroll
         for (int k = 0; k < kCandidates; ++k) local[k] = 0;
-        if (p.p_min < kSingle) {
+        if (p.p_min < kSingle && !p.part_fixed) {
             for (int r = tid; r < p.R; r += kThreads) {
                 const int a = p.qsl[r], b = p.qsl[r + 1];
                 const int n = b - a;
                 const int L = p.seq_lens[r];
-                if (a < 0 || b > p.T || n < 1 || n > p.tau || L < n ||
+                if (a < 0 || b > p.T || n < 1 || n > p.tau || L < n || L > p.max_seq ||
                     (L + kPage - 1) / kPage > p.MB)
                     continue;
                 const long long per = (long long)p.Hkv * ((n * p.G + RPI - 1) / RPI);
@@ -418,7 +420,9 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     }
     __syncthreads();
     int part = kSingle;
-    if (p.p_min < kSingle) {
+    if (p.part_fixed) {
+        part = p.p_min;
+    } else if (p.p_min < kSingle) {
         for (int k = kCandidates - 1; k >= 0; --k)
             if (cand[k] <= (unsigned long long)p.pslot_cap) part = p.p_min << k;
     }
@@ -440,10 +444,11 @@ paged_decode_kernel(const __grid_constant__ Params p) {
     Walker<RPI> walk;
     walk.begin(&p, part, lane);
     typename Walker<RPI>::Item it;
-    // With an item counter the producer takes each next index from it and
-    // publishes it in queue entry k % kQueue (-1: no more items) for the
-    // consumer warps; without one, CTA b takes items b, b + grid, ...  Either
-    // way a CTA's indices rise, as the walker needs.
+    // With an item counter the producer takes its CTA's own index first, then
+    // grid + each next value of the counter, and publishes the index in queue
+    // entry k % kQueue (-1: no more items) for the consumer warps; without
+    // one, CTA b takes items b, b + grid, ...  Either way a CTA's indices
+    // rise, as the walker needs.
 
     // ---- shared-partition groups.  Requests of one query token whose block
     // tables hold the same physical blocks over a whole partition that their
@@ -488,6 +493,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
         auto handed_to = [&](int w) { return (handed >> (8 * w)) & 0xffu; };
         int blk0 = 0;            // the item's first 32 block ids, when already loaded
         bool have_blk0 = false;
+        bool first_fetch = true; // a CTA's first item is its own index: no atomic storm at launch
         bool ok = true;
         for (long long k = 0; ok; ++k) {   // k: items published
             if (p.item_counter) {
@@ -495,8 +501,13 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 bool valid;
                 long long members = 0;
                 for (;;) {   // the next item that is not a group member's
-                    if (lane == 0) cand = atomicAdd(p.item_counter, 1u);
-                    cand = __shfl_sync(0xffffffffu, cand, 0);
+                    if (first_fetch) {
+                        cand = blockIdx.x;
+                        first_fetch = false;
+                    } else {
+                        if (lane == 0) cand = gridDim.x + atomicAdd(p.item_counter, 1u);
+                        cand = __shfl_sync(0xffffffffu, cand, 0);
+                    }
                     valid = walk.find((long long)cand, lane, it);
                     have_blk0 = false;
                     if (!valid || gcap == 0) break;
@@ -1412,6 +1423,7 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     prm.Hkv = a.Hkv;
     prm.G = a.Hq / a.Hkv;
     prm.tau = tau;
+    prm.max_seq = a.max_seq;
     prm.qscale = a.scale * 1.4426950408889634f;
     prm.status = status_word();
     if (!prm.status) return PA_ERR_CUDA;
@@ -1438,6 +1450,14 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
             prm.pslot_cap = cap;
             prm.p_min = kPreferredPartition;
             merge = true;
+            // Every request is at most max_seq long (longer ones are flagged
+            // and skipped), so when the workspace holds the partials of this
+            // bound at p_min the kernel needs no pass over the requests to
+            // choose a partition length.
+            const long long bound = (long long)a.Hkv *
+                                    ((long long)a.R + ((long long)a.T * prm.G + rpi - 1) / rpi) *
+                                    ((a.max_seq + kPreferredPartition - 1) / kPreferredPartition);
+            prm.part_fixed = cap >= bound ? 1 : 0;
         }
     }
 

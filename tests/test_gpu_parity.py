@@ -462,6 +462,31 @@ def test_attention_flags_bad_block_and_bad_lengths():
     assert st == pa.PA_ERR_DEVICE_CHECK and "seq_len" in pa.check_bits(detail)
 
 
+def test_seq_len_above_max_seq_len_is_flagged_and_skipped():
+    # max_seq_len is the caller's bound on seq_lens: a longer request is
+    # flagged and left out; every other request is computed as usual.
+    rng = np.random.default_rng(8)
+    w = workloads._make("bound", [1, 1, 1, 3], [2900, 1200, 700, 2000], rng, 8, 2, 128, "bf16")
+    vals = workloads.make_values(w, 8)
+    res = run_step(w, vals)
+    assert res["status"] == pa.PA_OK
+    _, _, _, ref = _oracle_step(w, vals)
+    q = vals["q"].cuda()
+    qsl = torch.from_numpy(res["query_start_loc"]).cuda()
+    sl = torch.from_numpy(res["seq_lens"]).cuda()
+    bound = 2500                                       # request 0 (2901 keys) is past it
+    nbytes = pa.pa_attention_workspace_size(w.num_reqs, w.num_tokens, w.max_query_len, bound,
+                                            w.num_q_heads, w.num_kv_heads, w.head_dim)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    o = torch.full_like(q, float("nan"))
+    pa.pa_attention(q, res["key_cache"], res["value_cache"], to_dev(w.block_table), qsl, sl,
+                    w.max_query_len, bound, w.scale, o, ws)
+    st, detail = pa.pa_get_status()
+    assert st == pa.PA_ERR_DEVICE_CHECK and pa.check_bits(detail) == {"seq_len"}
+    got = o.float().cpu().numpy().astype(np.float64)
+    assert np.abs(got[1:] - ref[1:]).max() <= ATOL
+
+
 def test_host_side_rejections():
     q = torch.zeros(2, 4, 96, dtype=torch.bfloat16, device="cuda")
     pool = torch.zeros(4, 16, 2, 96, dtype=torch.bfloat16, device="cuda")
