@@ -1146,7 +1146,8 @@ template <> __device__ __forceinline__ void fma_vec<float2>(float *o, float w, c
     o[1] = fmaf(w, v.y, o[1]);
 }
 
-template <typename T, int D, int RPI, int WPH>
+// B: partial rows in flight per warp (fewer registers for short contexts)
+template <typename T, int D, int RPI, int WPH, int B>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_constant__ Params p) {
     constexpr int DPL = D / 32;
     constexpr int kHeads = kMergeWarps / WPH;   // heads per CTA
@@ -1184,9 +1185,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
         float M = -INFINITY, Lsum = 0.f;
         if (active && cnt_w > 0) {
             // the first batch of partial rows, and (m, l) of partitions lane, lane + 32, ...
-            V v[kMergeBatch];
+            V v[B];
 #pragma unroll
-            for (int k = 0; k < kMergeBatch; ++k)
+            for (int k = 0; k < B; ++k)
                 if (k < cnt_w) v[k] = *row(k);
             const float2 ml0 = lane < cnt_w ? ml[split(lane) * RPI + j] : make_float2(-INFINITY, 0.f);
             M = ml0.x;
@@ -1200,14 +1201,14 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
                 const float w = mv.x == -INFINITY ? 0.f : fast_exp2(mv.x - M);
                 Lsum += w * mv.y;
                 const int cnt = min(32, cnt_w - i0);
-                for (int k0 = 0; k0 < cnt; k0 += kMergeBatch) {
+                for (int k0 = 0; k0 < cnt; k0 += B) {
                     if (i0 + k0 > 0) {   // later batches (the first was issued above)
 #pragma unroll
-                        for (int k = 0; k < kMergeBatch; ++k)
+                        for (int k = 0; k < B; ++k)
                             if (k0 + k < cnt) v[k] = *row(i0 + k0 + k);
                     }
 #pragma unroll
-                    for (int k = 0; k < kMergeBatch; ++k) {
+                    for (int k = 0; k < B; ++k) {
                         const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
                         if (k0 + k < cnt) fma_vec(o, wk, v[k]);
                     }
@@ -1263,7 +1264,7 @@ static int merge_warps_per_head(long long max_splits, long long R, long long Hq)
     return wph;
 }
 
-template <typename T, int D, int RPI, int WPH>
+template <typename T, int D, int RPI, int WPH, int B = kMergeBatch>
 static pa_status launch_merge(const Params &prm, cudaStream_t stream) {
     constexpr int kHeads = kMergeWarps / WPH;
     const long long groups = (prm.Hq + kHeads - 1) / kHeads;
@@ -1276,7 +1277,7 @@ static pa_status launch_merge(const Params &prm, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, merge_kernel<T, D, RPI, WPH>, prm));
+    PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, merge_kernel<T, D, RPI, WPH, B>, prm));
     note_launch();
     return PA_OK;
 }
@@ -1314,7 +1315,9 @@ pa_status launch_typed(Params &prm, long long max_items, long long merge_splits,
     if (st != PA_OK) return st;
     if (merge_splits > 0 && prm.R > 0) {
         switch (merge_warps_per_head(merge_splits, prm.R, prm.Hq)) {
-            case 1: return launch_merge<TQ, D, RPI, 1>(prm, stream);
+            case 1:   // at most 8 partitions: a batch of 8 rows, more warps resident
+                return merge_splits <= 8 ? launch_merge<TQ, D, RPI, 1, 8>(prm, stream)
+                                         : launch_merge<TQ, D, RPI, 1>(prm, stream);
             case 2: return launch_merge<TQ, D, RPI, 2>(prm, stream);
             case 4: return launch_merge<TQ, D, RPI, 4>(prm, stream);
             default: return launch_merge<TQ, D, RPI, 8>(prm, stream);
