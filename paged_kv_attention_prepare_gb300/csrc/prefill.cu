@@ -698,75 +698,165 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 tc_fence_after();
                 const int key0 = j * kBN;
                 const bool full_tile = key0 + kBN - 1 <= pos;
-                // Pass 1: row max of the raw scores (scale > 0 keeps the
-                // argmax), 64 columns per TMEM round trip, four chains.
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[64];
-                    tmem_ld32(colS + hh * 64, *reinterpret_cast<uint32_t (*)[32]>(r));
-                    tmem_ld32(colS + hh * 64 + 32, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
-                    tmem_wait_ld();
-                    if (!full_tile) {
-#pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            if (key0 + hh * 64 + k > pos) r[k] = 0xff800000u;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 64; k += 2)
-                        m4[(k >> 1) & 3] = fmaxf(m4[(k >> 1) & 3],
-                                                 fmaxf(__uint_as_float(r[k]), __uint_as_float(r[k + 1])));
-                }
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2.x;
-                const bool need = mx > m_ref + kRescaleThreshold;
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    // O holds PV of tiles < j, all complete: S_j's commit (waited
-                    // above) covers every MMA issued before it.  Rescale.
-                    const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
-#pragma unroll
-                    for (int cc = 0; cc < D; cc += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(colO + cc, o);
+                if constexpr (!F8) {
+                    // One TMEM pass, 64 columns at a time: the half's row max (scale
+                    // > 0 keeps the argmax), then P = exp2(s*c - m_ref) in packed
+                    // pairs written over the scores already read (64 keys ->
+                    // columns 32hh..32hh+31).  The reference max moves lazily:
+                    // only when a half's max passes it by more than 2^8, so P stays
+                    // below 256.  Sums and O accumulated against an older reference
+                    // are scaled down when it moves: the tile's first half in
+                    // TMEM (rare: only when the second half moves it again), the
+                    // tile's partial sum, and O and l of earlier tiles once per
+                    // tile.  A row with no visible key is never written out, so
+                    // any NaN stays in its own row.
+                    const float m_prev = m_ref;
+                    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    #pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[64];
+                        tmem_ld32(colS + hh * 64, *reinterpret_cast<uint32_t (*)[32]>(r));
+                        tmem_ld32(colS + hh * 64 + 32, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
                         tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(colO + cc, o);
+                        if (!full_tile) {
+    #pragma unroll
+                            for (int k = 0; k < 64; ++k)
+                                if (key0 + hh * 64 + k > pos) r[k] = 0xff800000u;
+                        }
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    #pragma unroll
+                        for (int k = 0; k < 64; k += 2)
+                            m4[(k >> 1) & 3] = fmaxf(m4[(k >> 1) & 3],
+                                                     fmaxf(__uint_as_float(r[k]), __uint_as_float(r[k + 1])));
+                        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2.x;
+                        const bool need = mx > m_ref + kRescaleThreshold;
+                        if (need) {
+                            const float alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - mx);
+                            acc[0].x *= alpha;
+                            acc[0].y *= alpha;
+                            acc[1].x *= alpha;
+                            acc[1].y *= alpha;
+                        }
+                        if (hh == 1 && __any_sync(0xffffffffu, need)) {
+                            // the first half's P was written against the old reference
+                            const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
+                            uint32_t w[32];
+                            tmem_ld32(colS, w);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                float a, b;
+                                Elt<TM>::unpack2(w[e], a, b);
+                                w[e] = Elt<TM>::pack2(a * alpha, b * alpha);
+                            }
+                            tmem_st32(colS, w);
+                        }
+                        if (need) m_ref = mx;
+                        const float2 mneg = make_float2(-m_ref, -m_ref);
+                        uint32_t w[32];
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]),
+                                                              __uint_as_float(r[2 * e + 1])), c2, mneg);
+                            y.x = fast_exp2(y.x);
+                            y.y = fast_exp2(y.y);
+                            acc[e & 1] = __fadd2_rn(acc[e & 1], y);
+                            w[e] = Elt<TM>::pack2(y.x, y.y);
+                        }
+                        tmem_st32(colS + hh * 32, w);
+                    }
+                    if (j > 0 && __any_sync(0xffffffffu, m_ref != m_prev)) {
+                        // O holds PV of tiles < j, all complete: S_j's commit (waited
+                        // above) covers every MMA issued before it.  Rescale.
+                        const float alpha = m_ref != m_prev ? fast_exp2(m_prev - m_ref) : 1.f;
+    #pragma unroll
+                        for (int cc = 0; cc < D; cc += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(colO + cc, o);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(colO + cc, o);
+                        }
+                        l *= alpha;
                     }
                     tmem_wait_st();
-                    if (need) l *= alpha;
-                }
-                if (need) m_ref = mx;
-                // Pass 2: P = exp2(s*c - m_ref) in packed pairs, written over
-                // the scores already read (64 keys -> columns 32hh..32hh+31).
-                // A row with no visible key is never written out, so any NaN
-                // stays in its own row.
-                const float2 mneg = make_float2(-m_ref, -m_ref);
-                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[64];
-                    tmem_ld32(colS + hh * 64, *reinterpret_cast<uint32_t (*)[32]>(r));
-                    tmem_ld32(colS + hh * 64 + 32, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
-                    tmem_wait_ld();
-                    if (!full_tile) {
-#pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            if (key0 + hh * 64 + k > pos) r[k] = 0xff800000u;
+                    l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                } else {
+                    // FP8 pools: two passes over the scores (row max, then P).
+                    // The one-pass form above measured slower here when scores
+                    // spread widely (427 against 378 us on the mixed step's
+                    // chunk over unscaled pools).
+                    // Pass 1: row max of the raw scores (scale > 0 keeps the
+                    // argmax), 64 columns per TMEM round trip, four chains.
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    #pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[64];
+                        tmem_ld32(colS + hh * 64, *reinterpret_cast<uint32_t (*)[32]>(r));
+                        tmem_ld32(colS + hh * 64 + 32, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
+                        tmem_wait_ld();
+                        if (!full_tile) {
+    #pragma unroll
+                            for (int k = 0; k < 64; ++k)
+                                if (key0 + hh * 64 + k > pos) r[k] = 0xff800000u;
+                        }
+    #pragma unroll
+                        for (int k = 0; k < 64; k += 2)
+                            m4[(k >> 1) & 3] = fmaxf(m4[(k >> 1) & 3],
+                                                     fmaxf(__uint_as_float(r[k]), __uint_as_float(r[k + 1])));
                     }
-                    uint32_t w[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]),
-                                                          __uint_as_float(r[2 * e + 1])), c2, mneg);
-                        y.x = fast_exp2(y.x);
-                        y.y = fast_exp2(y.y);
-                        acc[e & 1] = __fadd2_rn(acc[e & 1], y);
-                        w[e] = Elt<TM>::pack2(y.x, y.y);
+                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2.x;
+                    const bool need = mx > m_ref + kRescaleThreshold;
+                    if (j > 0 && __any_sync(0xffffffffu, need)) {
+                        // O holds PV of tiles < j, all complete: S_j's commit (waited
+                        // above) covers every MMA issued before it.  Rescale.
+                        const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
+    #pragma unroll
+                        for (int cc = 0; cc < D; cc += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(colO + cc, o);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(colO + cc, o);
+                        }
+                        tmem_wait_st();
+                        if (need) l *= alpha;
                     }
-                    tmem_st32(colS + hh * 32, w);
+                    if (need) m_ref = mx;
+                    // Pass 2: P = exp2(s*c - m_ref) in packed pairs, written over
+                    // the scores already read (64 keys -> columns 32hh..32hh+31).
+                    // A row with no visible key is never written out, so any NaN
+                    // stays in its own row.
+                    const float2 mneg = make_float2(-m_ref, -m_ref);
+                    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    #pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[64];
+                        tmem_ld32(colS + hh * 64, *reinterpret_cast<uint32_t (*)[32]>(r));
+                        tmem_ld32(colS + hh * 64 + 32, *reinterpret_cast<uint32_t (*)[32]>(r + 32));
+                        tmem_wait_ld();
+                        if (!full_tile) {
+    #pragma unroll
+                            for (int k = 0; k < 64; ++k)
+                                if (key0 + hh * 64 + k > pos) r[k] = 0xff800000u;
+                        }
+                        uint32_t w[32];
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            float2 y = __ffma2_rn(make_float2(__uint_as_float(r[2 * e]),
+                                                              __uint_as_float(r[2 * e + 1])), c2, mneg);
+                            y.x = fast_exp2(y.x);
+                            y.y = fast_exp2(y.y);
+                            acc[e & 1] = __fadd2_rn(acc[e & 1], y);
+                            w[e] = Elt<TM>::pack2(y.x, y.y);
+                        }
+                        tmem_st32(colS + hh * 32, w);
+                    }
+                    tmem_wait_st();
+                    l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
                 }
-                tmem_wait_st();
-                l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
                 if (j == ntS - 1 && ntS == nt && it.L < key0 + kBN) {
                     // Keys past the context in the item's last tile: their V
                     // rows hold stale data (or nothing was loaded); make them
