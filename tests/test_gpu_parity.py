@@ -275,6 +275,42 @@ def test_tensor_core_prefill_chunks(d, dtype, group, hkv):
     _check_attention(res, ref)
 
 
+@pytest.mark.parametrize("dtype,fp8", [("bf16", False), ("fp16", False), ("bf16", True)])
+def test_prefill_score_jumps_inside_and_across_tiles(dtype, fp8):
+    # Keys whose K rows are scaled up make some scores far larger than the
+    # rest: inside a 128-key tile the second half's maximum passes the
+    # first's by far more than 2^8 (the first half's P, already written, is
+    # scaled down), and later tiles move the reference again (O and the row
+    # sum are scaled down).  Same results as the oracle.
+    # (V is halved: the near one-hot rows then stay within the bf16 output's
+    # rounding budget of the 1e-2 bound.)
+    rng = np.random.default_rng(17)
+    w = workloads._make("jumps", [300, 1], [500, 900], rng, 8, 2, 128, dtype)
+    if fp8:
+        w = workloads.fp8(w, k_scale=0.25, v_scale=0.125)
+    vals = workloads.make_values(w, 4)
+    vals["value"] = (vals["value"].float() * 0.5).to(vals["value"].dtype)
+    if fp8:   # the same E4M3 bytes read at half the scale
+        w = workloads.fp8(w, k_scale=0.25, v_scale=0.0625)
+        vals["v_scale"] = vals["v_scale"] * 0.5
+    else:
+        vals["value_cache"] = (vals["value_cache"].float() * 0.5).to(vals["value_cache"].dtype)
+    kc = vals["key_cache"]
+    bt = w.block_table[0]
+    for lo, hi, f in ((64, 128, 6.0), (600, 640, 9.0), (700, 720, 12.0)):
+        for pos in range(lo, hi):
+            blk, off = int(bt[pos // 16]), pos % 16
+            if fp8:   # E4M3 bytes: scale the decoded value, re-encode
+                row = kc[blk, off].view(torch.float8_e4m3fn).float() * f
+                kc[blk, off] = row.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+            else:
+                kc[blk, off] = (kc[blk, off].float() * f).to(kc.dtype)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_attention(res, ref)
+
+
 def test_head_ratio_without_tensor_path():
     # 128 is not a multiple of 3 q heads per kv head: every request, long or
     # short, runs on the split-K kernel.
