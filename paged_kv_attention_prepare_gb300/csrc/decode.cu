@@ -11,10 +11,10 @@
 //     for all Hq/Hkv heads that share it and for all query tokens of a short
 //     chunk.  Rows per item (RPI) is a template parameter.
 //   * Persistent CTAs (3 per SM; 2 for 8-row items, which need more
-//     registers).  The producer warp takes each next item index from a
-//     counter in the workspace as its CTA frees up (a fixed stride when there
-//     is no workspace) and passes it to the consumer warps through a small
-//     shared-memory queue.  Every warp walks the request list itself (a
+//     registers).  The producer warp takes its CTA's own index first, then
+//     each next item index from a counter in the workspace as its CTA frees
+//     up (a fixed stride when there is no workspace), and passes it to the
+//     consumer warps through a small shared-memory queue.  Every warp walks the request list itself (a
 //     warp-wide scan over 32 requests at a time) to map an item index to
 //     (r, g, chunk, partition), so no work list is stored and no planning
 //     launch is needed.
@@ -32,6 +32,10 @@
 //   * A request whose context fits one partition writes its output directly;
 //     otherwise (m, l, unnormalised o) go to the workspace and the merge
 //     kernel combines them.
+//   * With kGroups (callers whose block tables share blocks), single-token
+//     requests holding the same blocks over a whole partition form group
+//     items: the pages are read once and each consumer warp computes 8 of up
+//     to 32 rows over every page.
 #include <climits>
 #include <cstring>
 #include <type_traits>
