@@ -129,10 +129,15 @@ def sub_batch(w, mask, q, bt_dev, qsl_host, sl_host, dev):
 
 
 def kernel_source_hash() -> str:
+    """Hash of the split-K kernel's sources with comments and blank space
+    removed: a comment edit does not change the kernel the profile measured."""
     h = hashlib.sha256()
     for name in ("decode.cu", "decode_fp16.cu", "pa_internal.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_attention_prepare_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_attention_prepare_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
