@@ -515,6 +515,16 @@ def run_ours(args):
     }
     del tok_dev, tok_host
 
+    # ---- the cache write alone: the step's new K/V rows into their slots
+    # (read and write, plus the slot indices)
+    write_elt = 1 if w.kv_cache_dtype == "fp8_e4m3" else 2
+    write_bytes = T * 2 * w.num_kv_heads * w.head_dim * (2 + write_elt) + 4 * T
+    write_us = time_calls(lambda: pa.pa_cache_write(vals["key"], vals["value"], kc, vc, slot,
+                                                    k_scale=ks, v_scale=vs), args.steps)
+    cache_write = {"us": write_us, "bytes": int(write_bytes),
+                   "GBps": write_bytes / (write_us * 1e-6) / 1e9,
+                   "note": "launch-bound below ~10 MB of rows"}
+
     # ---- end to end: inputs from pinned host memory, output back to host.
     # Every step copies its inputs host -> device and reads its output back,
     # through the same public calls.  When the step's KV bytes exceed the L2
@@ -726,6 +736,7 @@ def run_ours(args):
             "clocks": clocks.summary(),
             "attn_us_per_step": float(np.mean(attn_ms)) * 1e3,
             "prep_us": prep_us,
+            "cache_write": cache_write,
             "block_ops": block_ops,
             "launch": ("cuda_graph: the three calls captured once, one replay per step"
                        if graph_ms is not None else f"eager (graph capture failed: {graph_error})"),
