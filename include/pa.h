@@ -299,9 +299,9 @@ pa_status pa_zero_blocks(void *key_cache, void *value_cache, const int32_t *bloc
  * split every request's context into its preferred number of partitions.
  * Any smaller workspace (including 0) is still correct: the kernel then uses
  * longer partitions so the partial results fit (less parallelism for long
- * contexts), and without the first 256 bytes the tensor-core kernel takes its
- * work items in a fixed order instead of as its CTAs free up.  Arguments are
- * host-known bounds of the step.
+ * contexts), and without the first 256 bytes (the item counters) both
+ * kernels take their work items in a fixed order instead of as their CTAs
+ * free up.  Arguments are host-known bounds of the step.
  */
 size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens,
                                    int32_t max_query_len, int32_t max_seq_len,
