@@ -6,11 +6,14 @@
 // path (cu_seqlens_q, seqused_k, block_table).  Same maths as the split-K
 // kernel: out = softmax(scale * q K^T, causal) V per request and kv head.
 //
-// Work item = (request, kv head g, 256-row pair of tiles).  A row is one
-// (query token, q head of group g) pair, so a K/V tile serves all Hq/Hkv
-// heads of the group and both 128-row tiles ("slots" A and B) of the pair;
-// each Q tile is one 3-D TMA box {64 dims, G heads, 128/G tokens} per 64-dim
-// half.  Items run on persistent CTAs (one per SM), heaviest first.
+// Work item = (request, kv head g, pair of row tiles).  A row is one
+// (query token, q head of group g) pair, so a K/V tile serves all G = Hq/Hkv
+// heads of the group and both 128-row tiles ("slots" A and B) of the pair.
+// A tile holds TT = floor(128/G) whole tokens (TT*G rows, token-major); each
+// Q tile is one 3-D TMA box {64 dims, G heads, TT tokens} per 64-dim half.
+// When G does not divide 128 the last 128 - TT*G rows of every Q buffer are
+// zeroed once and never loaded or written out.  Items run on persistent
+// CTAs (one per SM), heaviest first.
 //
 // Per 128-key KV tile j (8 pages of 16 tokens, each page one TMA box per
 // 64-dim half, 128-byte swizzle, addressed through the block table), for
@@ -69,6 +72,7 @@ struct Params {
     const int32_t *qsl;
     const int32_t *seq_lens;
     int R, T, MB, NB, Hq, Hkv, G;
+    int TT;         // query tokens per 128-row tile: floor(128 / G)
     int tau;        // requests with more than tau query tokens are handled here
     float qscale;   // softmax scale * log2(e)
     const float *k_scale, *v_scale;   // FP8 pools (device scalars; NULL = 1)
@@ -203,7 +207,7 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
-// Work items: per request with more than tau tokens, Hkv x ceil(n*G/256)
+// Work items: per request with more than tau tokens, Hkv x ceil(n/(2 TT))
 // tile pairs, ordered last pair first (the tile with the most keys), kv heads
 // interleaved.  Every warp walks the request list itself.
 // ---------------------------------------------------------------------------
@@ -231,7 +235,7 @@ struct Walker {
             L = p->seq_lens[r];
             const bool sane = a >= 0 && b <= p->T && n >= 0 && L >= n &&
                               (L + kPage - 1) / kPage <= p->MB;
-            if (sane && n > p->tau) items = p->Hkv * ((n * p->G + 2 * kBM - 1) / (2 * kBM));
+            if (sane && n > p->tau) items = p->Hkv * ((n + 2 * p->TT - 1) / (2 * p->TT));
         }
         incl = items;
 #pragma unroll
@@ -262,9 +266,9 @@ struct Walker {
         it.qstart = __shfl_sync(0xffffffffu, a, src);
         it.r = rb + src;
         const int local = li - excl;
-        const int nm = (it.n * p->G + 2 * kBM - 1) / (2 * kBM);
+        const int nm = (it.n + 2 * p->TT - 1) / (2 * p->TT);
         it.g = local % p->Hkv;
-        it.mt = nm - 1 - local / p->Hkv;  // index of the 256-row pair
+        it.mt = nm - 1 - local / p->Hkv;  // index of the tile pair
         return true;
     }
 };
@@ -280,11 +284,10 @@ __device__ __forceinline__ long long snake_item(int k) {
 // KV tiles slot `slot` of an item needs: keys 0 .. (last position any of its
 // rows sees); 0 when the slot has no rows.
 __device__ __forceinline__ int slot_tiles(const Params &p, const Item &it, int slot) {
-    const int first_row = it.mt * 2 * kBM + slot * kBM;
-    const int nrows = it.n * p.G;
-    if (first_row >= nrows) return 0;
-    const int last_row = min(first_row + kBM, nrows) - 1;
-    const int max_pos = it.L - it.n + last_row / p.G;
+    const int first_tok = (it.mt * 2 + slot) * p.TT;
+    if (first_tok >= it.n) return 0;
+    const int last_tok = min(first_tok + p.TT, it.n) - 1;
+    const int max_pos = it.L - it.n + last_tok;
     return (max_pos + kBN) / kBN;
 }
 
@@ -381,6 +384,16 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         prefetch_tensor_map(&p.tmK);
         prefetch_tensor_map(&p.tmV);
     }
+    {
+        // Rows TT*G .. 127 of both Q tiles (G does not divide 128): no box
+        // lands there, so zero them once and their scores stay finite.  With
+        // the 128-byte swizzle a row keeps its own 128 bytes of each half.
+        const int pad0 = p.TT * p.G, per = (kBM - pad0) * 8;   // 16-byte chunks per half
+        for (int i = tid; i < 2 * C::kHalves * per; i += blockDim.x)
+            *reinterpret_cast<uint4 *>(sQ + (i / per) * (kBM * 128) + (pad0 + (i % per) / 8) * 128 +
+                                       (i % 8) * 16) = make_uint4(0, 0, 0, 0);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -454,9 +467,10 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 else {
                     const int nslots = ntB > 0 ? 2 : 1;
                     uint64_t *qb = &bar[F8 ? B_QLAND : B_QFULL];
-                    mbar_arrive_expect_tx(qb, nslots * C::kQBytes);
+                    // a box counts in full, zero-filled rows past T included
+                    mbar_arrive_expect_tx(qb, nslots * p.TT * p.G * (D * 2));
                     for (int sl = 0; sl < nslots; ++sl) {
-                        const int tok0 = it.qstart + (it.mt * 2 + sl) * (kBM / p.G);
+                        const int tok0 = it.qstart + (it.mt * 2 + sl) * p.TT;
 #pragma unroll
                         for (int h = 0; h < C::kHalves; ++h)
                             tma_load_3d(sQ + sl * C::kQBytes + h * (kBM * 128), &p.tmQ, qb, h * 64,
@@ -685,9 +699,8 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 t0 += nt;
                 continue;
             }
-            const int rr = (it.mt * 2 + slot) * kBM + row;
-            const bool valid = rr < it.n * p.G;
-            const int tl = rr / p.G;
+            const int tl = (it.mt * 2 + slot) * p.TT + row / p.G;   // token in the request
+            const bool valid = row < p.TT * p.G && tl < it.n;
             const int pos = valid ? it.L - it.n + tl : -1;  // last key this row sees
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < ntS; ++j, ++cnt) {
@@ -897,7 +910,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
             tc_fence_after();
             const float inv = l > 0.f ? vs / l : 0.f;
             T *dst = reinterpret_cast<T *>(p.out) +
-                     ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + rr % p.G) * D;
+                     ((long long)(it.qstart + tl) * p.Hq + it.g * p.G + row % p.G) * D;
 #pragma unroll
             for (int cc = 0; cc < D; cc += 32) {
                 uint32_t r[32];
@@ -932,7 +945,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
 }
 
 // 3-D TMA map, 128-byte swizzle, 64-element inner box: q as [T][Hq][D] with a
-// {64, G, 128/G} box, or a pool as [NB*bs][Hkv][D] with a {64, 1, 16} box.
+// {64, G, floor(128/G)} box, or a pool as [NB*bs][Hkv][D] with a {64, 1, 16} box.
 bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
                   uint32_t b1, uint32_t b2, int elt = 2) {
     static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
@@ -980,7 +993,7 @@ pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) 
 int prefill_tau(const AttnArgs &a) {
     const int G = a.Hq / a.Hkv;
     // The tensor-core kernel takes the row max of unscaled scores: scale > 0.
-    if ((a.D != 64 && a.D != 128) || G < 1 || 128 % G != 0 || !(a.scale > 0.f)) return INT_MAX;
+    if ((a.D != 64 && a.D != 128) || G < 1 || G > prefill::kBM || !(a.scale > 0.f)) return INT_MAX;
     // FP8 pools: the tensor-core kernel widens E4M3 tiles at head_dim 128;
     // at 64 every request stays on the split-K kernel.
     if (a.cache_dtype != a.dtype && a.D != 128) return INT_MAX;
@@ -996,7 +1009,8 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     const uint64_t slots = (uint64_t)a.NB * a.bs;
     const bool f8 = a.cache_dtype == PA_FP8_E4M3;
     const int elt = f8 ? 1 : 2;
-    if (!encode_sw128(&prm.tmQ, a.q, a.D, a.Hq, a.T, G, kBM / G) ||
+    const int TT = kBM / G;
+    if (!encode_sw128(&prm.tmQ, a.q, a.D, a.Hq, a.T, G, TT) ||
         !encode_sw128(&prm.tmK, a.kc, a.D, a.Hkv, slots, 1, kPage, elt) ||
         !encode_sw128(&prm.tmV, a.vc, a.D, a.Hkv, slots, 1, kPage, elt))
         return PA_ERR_CUDA;
@@ -1015,12 +1029,13 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     prm.Hq = a.Hq;
     prm.Hkv = a.Hkv;
     prm.G = G;
+    prm.TT = TT;
     prm.tau = tau;
     prm.qscale = a.scale * 1.4426950408889634f;
     prm.status = status_word();
     if (!prm.status) return PA_ERR_CUDA;
     // upper bound on the row tiles
-    const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T * G + 2 * kBM - 1) / (2 * kBM));
+    const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T + 2 * TT - 1) / (2 * TT));
     const bool bf16 = a.dtype == PA_BF16;
     if (f8)   // head_dim 128 (prefill_tau keeps other FP8 shapes on the split-K kernel)
         return bf16 ? launch_typed<__nv_bfloat16, 128, true>(prm, items, stream)

@@ -311,11 +311,37 @@ def test_prefill_score_jumps_inside_and_across_tiles(dtype, fp8):
     _check_attention(res, ref)
 
 
-def test_head_ratio_without_tensor_path():
-    # 128 is not a multiple of 3 q heads per kv head: every request, long or
-    # short, runs on the split-K kernel.
-    rng = np.random.default_rng(3)
-    w = workloads._make("g3", [90, 1, 20], [10, 300, 0], rng, 6, 2, 128, "bf16")
+@pytest.mark.parametrize("d,dtype,group,hkv,fp8", [
+    (128, "bf16", 3, 2, False), (64, "fp16", 5, 2, False), (128, "bf16", 7, 4, False),
+    (128, "fp16", 6, 1, False), (64, "bf16", 48, 1, False), (64, "fp16", 65, 1, False),
+    (128, "bf16", 7, 4, True)])
+def test_tensor_core_prefill_head_ratios_not_dividing_128(d, dtype, group, hkv, fp8):
+    # A 128-row tile holds floor(128/G) whole tokens; the rows left over are
+    # zero and never written.  Several tile pairs, a last pair with only its
+    # first tile, a tile with a single token (G = 65), next to short requests
+    # on the split-K kernel.
+    rng = np.random.default_rng(group + d)
+    nst = [300, 1, 17, 5, 129]
+    nct = [0, 400, 250, 33, 700]
+    w = workloads._make("ratio", nst, nct, rng, hkv * group, hkv, d, dtype)
+    if fp8:
+        w = workloads.fp8(w, k_scale=0.5, v_scale=0.25)
+    vals = workloads.make_values(w, group)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_attention(res, ref)
+
+
+def test_head_ratio_above_128_stays_on_split_k():
+    # More than 128 q heads per kv head: a token no longer fits a tile, so
+    # long requests run on the split-K kernel too.  fp16: in bf16 the rows
+    # that see only a few keys (the third request starts from nothing) land
+    # at 0.01006 for |o| near 2.3, which is exactly the bf16 rounding of P
+    # before the PV product plus that of the output (reproduced on the CPU
+    # from these inputs), just past the 1e-2 bound with 9,760 rows.
+    rng = np.random.default_rng(160)
+    w = workloads._make("g160", [40, 1, 20], [10, 300, 0], rng, 160, 1, 64, "fp16")
     vals = workloads.make_values(w, 3)
     res = run_step(w, vals)
     _, _, _, ref = _oracle_step(w, vals)
