@@ -424,7 +424,7 @@ def _sample_tokens(w, k, seed):
     return np.array(sorted(picks), np.int32)
 
 
-@pytest.mark.parametrize("name", ["decode", "mixed", "mha", "shared_prefix"])
+@pytest.mark.parametrize("name", ["decode", "mixed", "mha", "shared_prefix", "mixed_gqa28_4"])
 def test_full_size_workloads(name):
     w = workloads.named(name)
     vals = workloads.make_values(w, 1, device="cuda")

@@ -170,15 +170,15 @@ def decode_batch(seed: int = 1) -> Workload:
                  rng, 32, 8, 128, "bf16")
 
 
-def mixed_step(seed: int = 2) -> Workload:
+def mixed_step(seed: int = 2, hq: int = 32, hkv: int = 8) -> Workload:
     """One 5000-token prompt chunk at 2048 computed, then 200 single-token decodes
-    with context ~ U[256, 8192]; 32 q / 8 kv heads, D 128."""
+    with context ~ U[256, 8192]; 32 q / 8 kv heads (or hq / hkv), D 128."""
     rng = np.random.default_rng(seed)
     ctx = rng.integers(256, 8192, size=200, endpoint=True)
     nst = np.concatenate([[5000], np.ones(200, np.int64)])
     nct = np.concatenate([[2048], ctx - 1])
-    return _make("mixed-5000@2048+200x[256,8192]-gqa32/8-d128", nst, nct, rng,
-                 32, 8, 128, "bf16")
+    return _make(f"mixed-5000@2048+200x[256,8192]-gqa{hq}/{hkv}-d128", nst, nct, rng,
+                 hq, hkv, 128, "bf16")
 
 
 def mha_decode(seed: int = 3) -> Workload:
@@ -231,6 +231,9 @@ NAMED = {
     "shared_prefix": shared_prefix,
     "decode_fp8": lambda seed=1: fp8(decode_batch(seed)),
     "mixed_fp8": lambda seed=2: fp8(mixed_step(seed)),
+    # 7 q heads per kv head (28 / 4): the tensor-core kernel's tiles hold 18
+    # tokens (126 of 128 rows)
+    "mixed_gqa28_4": lambda seed=2: mixed_step(seed, 28, 4),
 }
 
 
