@@ -139,7 +139,12 @@ struct Cfg {
     static_assert(kPairsPerWarp * 2 * kConsumerWarps == kStages, "stages must split evenly among warps");
     static_assert((kPairsPerWarp & (kPairsPerWarp - 1)) == 0, "per-warp counters wrap at a power of two");
     static constexpr int kStageBytes = kStages * kUnitBytes;
-    static constexpr int kComb = RPI * (D + 2);       // per warp: acc[row][D], m[row], l[row]
+    // The four warps' states are combined through shared memory in kCombPasses
+    // passes of kDC dims each: at 8 rows and head_dim 128 two passes keep the
+    // buffer at the 4-row size, so three CTAs still fit an SM.
+    static constexpr int kCombPasses = (RPI == 8 && D == 128) ? 2 : 1;
+    static constexpr int kDC = D / kCombPasses;
+    static constexpr int kComb = RPI * (kDC + 2);     // per warp: acc[row][kDC], m[row], l[row]
     static constexpr int kBytes = kStageBytes + kConsumerWarps * kComb * 4 +
                                   (2 * kStages + 2) * 8 + kCandidates * 8 + kQueue * 3 * 8 +
                                   1024;
@@ -351,7 +356,7 @@ __device__ __forceinline__ int perm16(int k) { return ((0x27146350u >> (4 * (k &
 // kGroups: shared-partition group items (callers whose block tables may
 // share physical blocks); the kernel without them has no code for them.
 template <typename TQ, typename TC, int D, int RPI, bool kGroups>
-__global__ void __launch_bounds__(kThreads, RPI == 8 ? 2 : kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 paged_decode_kernel(const __grid_constant__ Params p) {
     using L = Lay<TC, D>;
     using TM = typename MmaIn<TQ, TC>::type;
@@ -1033,81 +1038,91 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, x);
             l1 += __shfl_xor_sync(0xffffffffu, l1, x);
         }
-        // O^T element (dim row, item row): rows 2tq, 2tq+1 of this lane
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            int dlo, dhi;   // dims of the m-tile's rows gq and gq + 8
-            if constexpr (L::E == 2) {
-                dlo = 16 * mt + gq;
-                dhi = dlo + 8;
-            } else {
-                dlo = gq * (D / 8) + 4 * (mt >> 1) + 2 * (mt & 1);
-                dhi = dlo + 1;
-            }
+        constexpr int DC = C::kDC;
+        if (gq == 0) {   // (m, l) once: the passes leave them in place
             if (2 * tq < RPI) {
-                cw[(2 * tq) * D + dlo] = o[mt][0];
-                cw[(2 * tq) * D + dhi] = o[mt][2];
+                cw[RPI * DC + 2 * tq] = m0;
+                cw[RPI * DC + RPI + 2 * tq] = l0;
             }
             if (2 * tq + 1 < RPI) {
-                cw[(2 * tq + 1) * D + dlo] = o[mt][1];
-                cw[(2 * tq + 1) * D + dhi] = o[mt][3];
+                cw[RPI * DC + 2 * tq + 1] = m1;
+                cw[RPI * DC + RPI + 2 * tq + 1] = l1;
             }
         }
-        if (gq == 0) {
-            if (2 * tq < RPI) {
-                cw[RPI * D + 2 * tq] = m0;
-                cw[RPI * D + RPI + 2 * tq] = l0;
-            }
-            if (2 * tq + 1 < RPI) {
-                cw[RPI * D + 2 * tq + 1] = m1;
-                cw[RPI * D + RPI + 2 * tq + 1] = l1;
-            }
-        }
-        if (!consumer_sync(cbar, cpar, lane)) {
-            flag(p.status, PA_CHECK_TIMEOUT);
-            ok = false;
-            break;
-        }
-        for (int o2 = tid; o2 < RPI * D / 2; o2 += kConsumers) {
-            const int r = o2 / (D / 2);
-            const int d = (o2 % (D / 2)) * 2;
-            const int rr = it.chunk * RPI + r;
-            if (rr >= nrows) continue;
-            float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb[w * C::kComb + RPI * D + r]);
-            float Ls = 0.f, s0 = 0.f, s1 = 0.f;
+        for (int hp = 0; hp < C::kCombPasses; ++hp) {
+            // O^T element (dim row, item row): rows 2tq, 2tq+1 of this lane;
+            // an m-tile's two dims of a lane lie in the same pass
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float *c = comb + w * C::kComb;
-                const float mw = c[RPI * D + r];
-                const float sw = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-                Ls += sw * c[RPI * D + RPI + r];
-                const float2 a = *reinterpret_cast<const float2 *>(c + r * D + d);
-                s0 += sw * a.x;
-                s1 += sw * a.y;
+            for (int mt = 0; mt < KS; ++mt) {
+                int dlo, dhi;   // dims of the m-tile's rows gq and gq + 8
+                if constexpr (L::E == 2) {
+                    dlo = 16 * mt + gq;
+                    dhi = dlo + 8;
+                } else {
+                    dlo = gq * (D / 8) + 4 * (mt >> 1) + 2 * (mt & 1);
+                    dhi = dlo + 1;
+                }
+                const bool mine = L::E == 2 ? (16 * mt) / DC == hp : dlo / DC == hp;
+                if (!mine) continue;
+                dlo -= hp * DC;
+                dhi -= hp * DC;
+                if (2 * tq < RPI) {
+                    cw[(2 * tq) * DC + dlo] = o[mt][0];
+                    cw[(2 * tq) * DC + dhi] = o[mt][2];
+                }
+                if (2 * tq + 1 < RPI) {
+                    cw[(2 * tq + 1) * DC + dlo] = o[mt][1];
+                    cw[(2 * tq + 1) * DC + dhi] = o[mt][3];
+                }
             }
-            s0 *= vs;   // an FP8 pool's V scale; 1 otherwise
-            s1 *= vs;
-            if (it.pslot < 0) {
-                const float inv = 1.f / Ls;
-                const int h = it.g * p.G + rr % p.G;
-                TQ *dst = reinterpret_cast<TQ *>(p.out) +
-                          ((long long)(qstart + rr / p.G) * p.Hq + h) * D + d;
-                *reinterpret_cast<uint32_t *>(dst) = Elt<TQ>::pack2(s0 * inv, s1 * inv);
-            } else {
-                float *po = p.part_o + (it.pslot * RPI + r) * D + d;
-                *reinterpret_cast<float2 *>(po) = make_float2(s0, s1);
-                if (d == 0)
-                    *reinterpret_cast<float2 *>(p.part_ml + (it.pslot * RPI + r) * 2) =
-                        make_float2(M, Ls);
+            if (!consumer_sync(cbar, cpar, lane)) {
+                flag(p.status, PA_CHECK_TIMEOUT);
+                ok = false;
+                break;
+            }
+            for (int o2 = tid; o2 < RPI * DC / 2; o2 += kConsumers) {
+                const int r = o2 / (DC / 2);
+                const int dl = (o2 % (DC / 2)) * 2, d = hp * DC + dl;
+                const int rr = it.chunk * RPI + r;
+                if (rr >= nrows) continue;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb[w * C::kComb + RPI * DC + r]);
+                float Ls = 0.f, s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float *c = comb + w * C::kComb;
+                    const float mw = c[RPI * DC + r];
+                    const float sw = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                    Ls += sw * c[RPI * DC + RPI + r];
+                    const float2 a = *reinterpret_cast<const float2 *>(c + r * DC + dl);
+                    s0 += sw * a.x;
+                    s1 += sw * a.y;
+                }
+                s0 *= vs;   // an FP8 pool's V scale; 1 otherwise
+                s1 *= vs;
+                if (it.pslot < 0) {
+                    const float inv = 1.f / Ls;
+                    const int h = it.g * p.G + rr % p.G;
+                    TQ *dst = reinterpret_cast<TQ *>(p.out) +
+                              ((long long)(qstart + rr / p.G) * p.Hq + h) * D + d;
+                    *reinterpret_cast<uint32_t *>(dst) = Elt<TQ>::pack2(s0 * inv, s1 * inv);
+                } else {
+                    float *po = p.part_o + (it.pslot * RPI + r) * D + d;
+                    *reinterpret_cast<float2 *>(po) = make_float2(s0, s1);
+                    if (d == 0)
+                        *reinterpret_cast<float2 *>(p.part_ml + (it.pslot * RPI + r) * 2) =
+                            make_float2(M, Ls);
+                }
+            }
+            if (!consumer_sync(cbar, cpar, lane)) {  // the combine buffer is free again
+                flag(p.status, PA_CHECK_TIMEOUT);
+                ok = false;
+                break;
             }
         }
-        if (!consumer_sync(cbar, cpar, lane)) {  // the combine buffer is free again
-            flag(p.status, PA_CHECK_TIMEOUT);
-            ok = false;
-            break;
-        }
+        if (!ok) break;
     }
     // A consumer that stops early (a timed-out wait) releases every stage,
     // every queue entry and the item barrier once, so the others' bounded
