@@ -333,6 +333,43 @@ def test_tensor_core_prefill_head_ratios_not_dividing_128(d, dtype, group, hkv, 
     _check_attention(res, ref)
 
 
+# (q heads per kv head, kv heads, head_dim, dtype, FP8 pools): ratios that do
+# and do not divide 128, up to a single token per tensor-core tile, on both
+# kernels (8-row split-K items combine their warps in two passes at D 128)
+RATIO_SWEEP = [
+    (1, 2, 64, "bf16", False), (2, 2, 128, "fp16", False), (3, 1, 64, "fp16", False),
+    (5, 1, 128, "bf16", False), (6, 2, 64, "bf16", False), (9, 1, 128, "fp16", False),
+    (10, 1, 64, "fp16", False), (11, 2, 128, "bf16", False), (12, 1, 128, "bf16", False),
+    (13, 1, 64, "bf16", False), (14, 1, 128, "fp16", False), (15, 2, 64, "fp16", False),
+    (20, 1, 128, "bf16", False), (24, 1, 64, "bf16", False), (32, 1, 128, "fp16", False),
+    (40, 1, 128, "bf16", False), (64, 1, 64, "fp16", False), (96, 1, 128, "bf16", False),
+    (127, 1, 64, "bf16", False), (128, 1, 128, "fp16", False),
+    (3, 2, 128, "bf16", True), (5, 1, 128, "fp16", True), (6, 1, 128, "bf16", True),
+    (12, 1, 128, "bf16", True), (16, 1, 64, "bf16", True), (24, 1, 128, "fp16", True),
+]
+
+
+@pytest.mark.parametrize("group,hkv,d,dtype,fp8", RATIO_SWEEP)
+def test_head_ratio_sweep(group, hkv, d, dtype, fp8):
+    # Random decodes, short chunks (split-K) and chunks of 17..150 tokens
+    # (tensor-core kernel), contexts up to ~850 keys (two partitions and the
+    # merge pass).  Every request starts from at least 32 computed tokens: a
+    # row that sees 2-4 keys can pass 1e-2 in bf16 by rounding alone.
+    rng = np.random.default_rng(1000 * group + d + (7 if fp8 else 0))
+    r = int(rng.integers(2, 6, endpoint=True))
+    nst = np.where(rng.random(r) < 0.5, 1, rng.integers(2, 25, size=r))
+    nst[0] = int(rng.integers(17, 151))
+    nct = rng.integers(32, 701, size=r)
+    w = workloads._make("ratio-sweep", nst, nct, rng, hkv * group, hkv, d, dtype)
+    if fp8:
+        w = workloads.fp8(w, k_scale=0.25, v_scale=0.125)
+    vals = workloads.make_values(w, group)
+    res = run_step(w, vals)
+    _, _, _, ref = _oracle_step(w, vals)
+    assert res["status"] == pa.PA_OK, pa.check_bits(res["detail"])
+    _check_attention(res, ref)
+
+
 def test_head_ratio_above_128_stays_on_split_k():
     # More than 128 q heads per kv head: a token no longer fits a tile, so
     # long requests run on the split-K kernel too.  fp16: in bf16 the rows
