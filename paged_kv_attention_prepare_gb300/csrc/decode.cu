@@ -10,8 +10,9 @@
 //     (query token, q head of group g) pair, so each K/V page is read once
 //     for all Hq/Hkv heads that share it and for all query tokens of a short
 //     chunk.  Rows per item (RPI) is a template parameter.
-//   * Persistent CTAs (3 per SM; 2 for 8-row items, which need more
-//     registers).  The producer warp takes its CTA's own index first, then
+//   * Persistent CTAs, 3 per SM (128 registers; at 8 rows and head_dim 128
+//     the warps' states are combined in two passes of 64 dims, so the
+//     combine buffer fits).  The producer warp takes its CTA's own index first, then
 //     each next item index from a counter in the workspace as its CTA frees
 //     up (a fixed stride when there is no workspace), and passes it to the
 //     consumer warps through a small shared-memory queue.  Every warp walks the request list itself (a
