@@ -326,8 +326,8 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens,
  * to the element type.
  *
  * Requests with more than 16 query tokens run on the tensor-core (tcgen05)
- * kernel when num_q_heads / num_kv_heads <= 128 and scale > 0 (FP8 pools:
- * head_dim 128 only); every other request runs on the split-K kernel.  Both
+ * kernel when num_q_heads / num_kv_heads <= 128 and scale > 0; every other
+ * request runs on the split-K kernel.  Both
  * compute the definition above in the same precision.
  *
  * Arguments:

@@ -33,12 +33,14 @@
 // softmax and epilogue, 6..9 = slot B; warp w reads TMEM lanes 32*(w%4)..+31.
 // Every mbarrier wait is bounded.
 //
-// FP8 (E4M3) pools, head_dim 128: the MMAs run in f16 (E4M3 widens to f16
-// exactly; a bf16 q is rounded to f16).  Each FP8 page lands (one 128-byte
-// row per slot, swizzled) in the upper half of its f16 tile buffer, where
-// an FP8 row takes exactly the bytes of its own upper-half f16 row; two more
-// warps (10, 11) widen the tile in place, row by row, and only then signal
-// the tile full.  K's scale joins the softmax scale, V's scales the output.
+// FP8 (E4M3) pools: the MMAs run in f16 (E4M3 widens to f16 exactly; a bf16
+// q is rounded to f16).  At head_dim 128 each FP8 page lands (one 128-byte
+// row per slot, swizzled) in the upper half of its f16 tile buffer, where an
+// FP8 row takes exactly the bytes of its own upper-half f16 row; at head_dim
+// 64 it lands (64-byte rows, unswizzled) in a staging area of its own.  Two
+// more warps (10, 11) widen the tile into the f16 layout, row by row, and
+// only then signal the tile full.  K's scale joins the softmax scale, V's
+// scales the output.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -89,6 +91,11 @@ struct Cfg {
     static constexpr int kHalfBytes = kBN * 128;         // one 64-dim half of a K/V tile
     static constexpr int kPageHalfBytes = kPage * 128;
     static constexpr int kSmem = 2 * kQBytes + 4 * kTileBytes + 512 + 1024;
+    // FP8 pools at head_dim 64: 64-byte rows of K and V, two stages each,
+    // staged after the barriers (1024-byte aligned) before widening
+    static constexpr int kLandBytes = kBN * 64;
+    static constexpr int kLandOffset = 2 * kQBytes + 4 * kTileBytes + 1024;
+    static constexpr int kSmemF8Land = kLandOffset + 4 * kLandBytes + 1024;
     // TMEM columns: S_A 0, O_A 128, S_B 256, O_B 384
     __device__ static constexpr uint32_t col_s(int slot) { return (uint32_t)slot * 256; }
     __device__ static constexpr uint32_t col_o(int slot) { return (uint32_t)slot * 256 + 128; }
@@ -344,11 +351,44 @@ __device__ __forceinline__ void bf16_tile_to_f16(unsigned char *tile, int bytes,
     }
 }
 
+// Widen the E4M3 rows [r0, r1) of a 64-dim tile: row r's 64 bytes sit
+// unswizzled at land + 64 r; its 64 f16 values become row r of the f16 tile
+// (128 bytes, 128-byte swizzle).  Lane: row r0 + 8u + lane/4, 16 dims
+// 16 (lane%4) .. +15 (two f16 chunks).  r1 - r0 is a multiple of 32.
+__device__ __forceinline__ void widen_e4m3_rows64(const unsigned char *land, unsigned char *tile,
+                                                  int r0, int r1, int lane) {
+    const int c = lane & 3;
+    for (int rb = r0; rb < r1; rb += 32) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = rb + 8 * u + (lane >> 2);
+            v[u] = *reinterpret_cast<const uint4 *>(land + r * 64 + (c << 4));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = rb + 8 * u + (lane >> 2), x = r & 7;
+            uint32_t h[8];
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                asm("{\n.reg .b16 l, hh;\nmov.b32 {l, hh}, %2;\n"
+                    "cvt.rn.f16x2.e4m3x2 %0, l;\ncvt.rn.f16x2.e4m3x2 %1, hh;\n}"
+                    : "=r"(h[2 * e]), "=r"(h[2 * e + 1])
+                    : "r"(w[e]));
+            }
+            unsigned char *dst_row = tile + r * 128;
+            *reinterpret_cast<uint4 *>(dst_row + (((2 * c) ^ x) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(dst_row + (((2 * c + 1) ^ x) << 4)) =
+                make_uint4(h[4], h[5], h[6], h[7]);
+        }
+    }
+}
+
 template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const __grid_constant__ Params p) {
     using C = Cfg<D>;
     using TM = typename std::conditional<F8, __half, T>::type;   // the MMAs' input type
-    static_assert(!F8 || D == 128, "FP8 pools: head_dim 128");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -356,6 +396,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
     unsigned char *sK = sQ + 2 * C::kQBytes;        // 2 stages
     unsigned char *sV = sK + 2 * C::kTileBytes;     // 2 stages
     uint64_t *bar = reinterpret_cast<uint64_t *>(sV + 2 * C::kTileBytes);
+    unsigned char *sL = base + C::kLandOffset;      // FP8 at head_dim 64: [K st0, K st1, V st0, V st1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *q_items = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [kQueue]
@@ -492,8 +533,9 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 }
                 const int st = (int)(t & 1);
                 const uint32_t ph = (uint32_t)((t >> 1) & 1);
-                // FP8: one 128-byte row per slot, into the tile's upper half
-                const uint32_t bytes = F8 ? (uint32_t)npg * kPage * 128
+                // FP8: one D-byte row per slot (head_dim 128: into the tile's
+                // upper half; 64: into the staging area)
+                const uint32_t bytes = F8 ? (uint32_t)npg * kPage * D
                                           : (uint32_t)npg * C::kHalves * C::kPageHalfBytes;
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv) {
@@ -508,8 +550,10 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                     if (!ok) break;
                     if (lane < npg) {
                         if constexpr (F8) {
-                            tma_load_3d(dst + C::kHalfBytes + lane * kPage * 128, kv ? &p.tmV : &p.tmK,
-                                        fullb, 0, it.g, blk * kPage);
+                            unsigned char *fdst =
+                                D == 128 ? dst + C::kHalfBytes + lane * kPage * 128
+                                         : sL + (kv * 2 + st) * C::kLandBytes + lane * kPage * 64;
+                            tma_load_3d(fdst, kv ? &p.tmV : &p.tmK, fullb, 0, it.g, blk * kPage);
                         } else {
 #pragma unroll
                             for (int h = 0; h < C::kHalves; ++h)
@@ -664,8 +708,13 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                             ok = false;
                             break;
                         }
-                        widen_e4m3_tile((kv ? sV : sK) + st * C::kTileBytes, C::kHalfBytes, cw * 64,
-                                        cw * 64 + 64, lane);
+                        if constexpr (D == 128)
+                            widen_e4m3_tile((kv ? sV : sK) + st * C::kTileBytes, C::kHalfBytes, cw * 64,
+                                            cw * 64 + 64, lane);
+                        else
+                            widen_e4m3_rows64(sL + (kv * 2 + st) * C::kLandBytes,
+                                              (kv ? sV : sK) + st * C::kTileBytes, cw * 64, cw * 64 + 64,
+                                              lane);
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bar[(kv ? B_VFULL : B_KFULL) + st]);
@@ -944,10 +993,12 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
-// 3-D TMA map, 128-byte swizzle, 64-element inner box: q as [T][Hq][D] with a
-// {64, G, floor(128/G)} box, or a pool as [NB*bs][Hkv][D] with a {64, 1, 16} box.
+// 3-D TMA map, 128-byte swizzle, 128-byte inner box: q as [T][Hq][D] with a
+// {64, G, floor(128/G)} box, or a pool as [NB*bs][Hkv][D] with a {64, 1, 16}
+// box (16-bit) or {128, 1, 16} (FP8, head_dim 128).  plain_rows: an FP8 pool
+// at head_dim 64, whole 64-byte rows in a {64, 1, 16} box, no swizzle.
 bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
-                  uint32_t b1, uint32_t b2, int elt = 2) {
+                  uint32_t b1, uint32_t b2, int elt = 2, bool plain_rows = false) {
     static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     if (!enc) {
         void *fn = nullptr;
@@ -960,29 +1011,31 @@ bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, u
     }
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {d0 * elt, d0 * d1 * elt};
-    const cuuint32_t box[3] = {128u / (cuuint32_t)elt, b1, b2};   // 128 bytes per box row
+    const cuuint32_t box[3] = {plain_rows ? (cuuint32_t)d0 : 128u / (cuuint32_t)elt, b1, b2};
     const cuuint32_t es[3] = {1u, 1u, 1u};
     return enc(map, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                const_cast<void *>(ptr), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               plain_rows ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename T, int D, bool F8>
 pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) {
     using C = Cfg<D>;
+    constexpr int kSmem = (F8 && D == 64) ? C::kSmemF8Land : C::kSmem;
     static bool configured[64] = {};
     int dev = 0;
     PA_TRY_CUDA(cudaGetDevice(&dev));
     if (dev >= 64 || !configured[dev]) {
         PA_TRY_CUDA(cudaFuncSetAttribute(paged_prefill_kernel<T, D, F8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem));
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
         if (dev < 64) configured[dev] = true;
     }
     long long grid = num_sms();
     if (items < grid) grid = items;
     if (grid < 1) return PA_OK;
-    paged_prefill_kernel<T, D, F8><<<(int)grid, threads_for(F8), C::kSmem, stream>>>(prm);
+    paged_prefill_kernel<T, D, F8><<<(int)grid, threads_for(F8), kSmem, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
     return PA_OK;
@@ -994,9 +1047,6 @@ int prefill_tau(const AttnArgs &a) {
     const int G = a.Hq / a.Hkv;
     // The tensor-core kernel takes the row max of unscaled scores: scale > 0.
     if ((a.D != 64 && a.D != 128) || G < 1 || G > prefill::kBM || !(a.scale > 0.f)) return INT_MAX;
-    // FP8 pools: the tensor-core kernel widens E4M3 tiles at head_dim 128;
-    // at 64 every request stays on the split-K kernel.
-    if (a.cache_dtype != a.dtype && a.D != 128) return INT_MAX;
     return prefill::kTauDefault;
 }
 
@@ -1011,8 +1061,8 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     const int elt = f8 ? 1 : 2;
     const int TT = kBM / G;
     if (!encode_sw128(&prm.tmQ, a.q, a.D, a.Hq, a.T, G, TT) ||
-        !encode_sw128(&prm.tmK, a.kc, a.D, a.Hkv, slots, 1, kPage, elt) ||
-        !encode_sw128(&prm.tmV, a.vc, a.D, a.Hkv, slots, 1, kPage, elt))
+        !encode_sw128(&prm.tmK, a.kc, a.D, a.Hkv, slots, 1, kPage, elt, f8 && a.D == 64) ||
+        !encode_sw128(&prm.tmV, a.vc, a.D, a.Hkv, slots, 1, kPage, elt, f8 && a.D == 64))
         return PA_ERR_CUDA;
     prm.k_scale = a.k_scale;
     prm.v_scale = a.v_scale;
@@ -1037,9 +1087,12 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     // upper bound on the row tiles
     const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T + 2 * TT - 1) / (2 * TT));
     const bool bf16 = a.dtype == PA_BF16;
-    if (f8)   // head_dim 128 (prefill_tau keeps other FP8 shapes on the split-K kernel)
+    if (f8 && a.D == 128)
         return bf16 ? launch_typed<__nv_bfloat16, 128, true>(prm, items, stream)
                     : launch_typed<__half, 128, true>(prm, items, stream);
+    if (f8)
+        return bf16 ? launch_typed<__nv_bfloat16, 64, true>(prm, items, stream)
+                    : launch_typed<__half, 64, true>(prm, items, stream);
     if (a.D == 128)
         return bf16 ? launch_typed<__nv_bfloat16, 128, false>(prm, items, stream)
                     : launch_typed<__half, 128, false>(prm, items, stream);

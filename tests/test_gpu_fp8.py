@@ -109,12 +109,26 @@ def test_fp8_head_shapes(d, dtype, group):
     _check_step(w, workloads.make_values(w, 2))
 
 
-def test_fp8_long_chunk_runs_on_the_split_k_kernel():
-    # a prompt chunk longer than the split-K kernel's usual share: FP8 pools
-    # keep every request on it
-    w = _fp8_case(77, max_reqs=3, max_new=8, max_computed=300, long_prefill=200, head_dim=128,
-                  group=4, num_kv_heads=2)
+@pytest.mark.parametrize("d,dtype,group,hkv", [(128, "bf16", 4, 2), (64, "bf16", 4, 2),
+                                               (64, "fp16", 1, 3), (64, "bf16", 7, 1),
+                                               (64, "fp16", 16, 1)])
+def test_fp8_long_chunk(d, dtype, group, hkv):
+    # A 200-token prompt chunk over FP8 pools runs on the tensor-core kernel,
+    # which widens each landed E4M3 tile to f16 in shared memory (head_dim
+    # 128: in place; 64: from a staging area).  Short requests beside it stay
+    # on the split-K kernel.
+    w = _fp8_case(77 + d + group, max_reqs=3, max_new=8, max_computed=300, long_prefill=200,
+                  head_dim=d, dtype=dtype, group=group, num_kv_heads=hkv)
     _check_step(w, workloads.make_values(w, 5))
+
+
+def test_fp8_head_dim_64_prompt_tiles():
+    # Head_dim 64 over FP8 pools, a 600-token chunk at 500 computed: many
+    # 128-key tiles and both staging stages of K and V, a ragged last tile.
+    rng = np.random.default_rng(64)
+    w = workloads._make("fp8-d64", [600, 1, 3], [500, 900, 40], rng, 8, 2, 64, "bf16")
+    w = workloads.fp8(w, k_scale=0.25, v_scale=0.125)
+    _check_step(w, workloads.make_values(w, 9))
 
 
 @pytest.mark.parametrize("name", ["decode_fp8", "mixed_fp8"])

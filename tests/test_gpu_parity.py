@@ -275,8 +275,9 @@ def test_tensor_core_prefill_chunks(d, dtype, group, hkv):
     _check_attention(res, ref)
 
 
-@pytest.mark.parametrize("dtype,fp8", [("bf16", False), ("fp16", False), ("bf16", True)])
-def test_prefill_score_jumps_inside_and_across_tiles(dtype, fp8):
+@pytest.mark.parametrize("dtype,fp8,d", [("bf16", False, 128), ("fp16", False, 128),
+                                        ("bf16", True, 128), ("fp16", False, 64), ("bf16", True, 64)])
+def test_prefill_score_jumps_inside_and_across_tiles(dtype, fp8, d):
     # Keys whose K rows are scaled up make some scores far larger than the
     # rest: inside a 128-key tile the second half's maximum passes the
     # first's by far more than 2^8 (the first half's P, already written, is
@@ -285,7 +286,7 @@ def test_prefill_score_jumps_inside_and_across_tiles(dtype, fp8):
     # (V is halved: the near one-hot rows then stay within the bf16 output's
     # rounding budget of the 1e-2 bound.)
     rng = np.random.default_rng(17)
-    w = workloads._make("jumps", [300, 1], [500, 900], rng, 8, 2, 128, dtype)
+    w = workloads._make("jumps", [300, 1], [500, 900], rng, 8, 2, d, dtype)
     if fp8:
         w = workloads.fp8(w, k_scale=0.25, v_scale=0.125)
     vals = workloads.make_values(w, 4)
