@@ -131,7 +131,7 @@ def test_fp8_head_dim_64_prompt_tiles():
     _check_step(w, workloads.make_values(w, 9))
 
 
-@pytest.mark.parametrize("name", ["decode_fp8", "mixed_fp8"])
+@pytest.mark.parametrize("name", ["decode_fp8", "mixed_fp8", "chunk_fp8_d64"])
 def test_fp8_full_size_sampled(name):
     from test_gpu_parity import _sample_tokens
     w = workloads.named(name)

@@ -181,6 +181,13 @@ def mixed_step(seed: int = 2, hq: int = 32, hkv: int = 8) -> Workload:
                  hq, hkv, 128, "bf16")
 
 
+def chunk_fp8_d64(seed: int = 5) -> Workload:
+    """One 5000-token prompt chunk at 2048 computed over FP8 (E4M3) pools at
+    head_dim 64; 32 q / 8 kv heads, bf16 q."""
+    rng = np.random.default_rng(seed)
+    return fp8(_make("chunk-5000@2048-gqa32/8-d64", [5000], [2048], rng, 32, 8, 64, "bf16"))
+
+
 def mha_decode(seed: int = 3) -> Workload:
     """30 single-token decodes at context 2048; 40 q = 40 kv heads, D 128, fp16."""
     rng = np.random.default_rng(seed)
@@ -234,6 +241,7 @@ NAMED = {
     # 7 q heads per kv head (28 / 4): the tensor-core kernel's tiles hold 18
     # tokens (126 of 128 rows)
     "mixed_gqa28_4": lambda seed=2: mixed_step(seed, 28, 4),
+    "chunk_fp8_d64": lambda seed=5: chunk_fp8_d64(seed),
 }
 
 
