@@ -11,6 +11,7 @@
  *                      token_indices), the discard mask and the sampled rows
  *                      of speculative decoding;
  *   pa_cache_write     each new token's K and V copied to its cache slot;
+ *   pa_prepare_and_write  pa_prepare_inputs and pa_cache_write in one launch;
  *   pa_copy_blocks / pa_zero_blocks  whole-block copy-on-write copies and
  *                      the zeroing of newly allocated blocks;
  *   pa_attention       causal grouped-query attention of every token over
@@ -136,6 +137,44 @@ pa_status pa_prepare_inputs(const int32_t *num_scheduled_tokens,
                             int32_t *slot_mapping, int32_t *query_start_loc,
                             int32_t qsl_capacity, int32_t *seq_lens,
                             int32_t *logits_indices, pa_stream_t stream);
+
+/*
+ * pa_prepare_and_write -- pa_prepare_inputs and pa_cache_write_ex in one
+ * launch.
+ *
+ * "How vLLM Works Internally", section "Fused Kernels" (one launch instead
+ * of two, and no round trip of slot_mapping through global memory between
+ * them), applied to "Building the Batch", section "How they are computed"
+ * (the index tensors) and "Inside vLLM: Following One Request", the write op
+ * (token t's K and V rows to slot_mapping[t]).  The outputs are bit for bit
+ * those of pa_prepare_inputs followed, on the same stream, by
+ * pa_cache_write_ex with the slot_mapping it produced: every index tensor,
+ * and every pool row written (16-bit pools: a copy; PA_FP8_E4M3 pools:
+ * E4M3(x / scale)).  A token whose slot fails a check (slot_mapping -1) is
+ * not written, as a negative slot is skipped by pa_cache_write.
+ *
+ * Arguments: those of pa_prepare_inputs, then key, value [num_tokens] rows
+ * of num_kv_heads * head_dim elements kv_token_stride elements apart (16-byte
+ * aligned rows), the pools (layout as pa_cache_write; 16-byte aligned rows,
+ * 8-byte for FP8 pools), num_kv_heads, head_dim, dtype (of key/value),
+ * cache_dtype (dtype or PA_FP8_E4M3) and the FP8 scales (device scalars,
+ * NULL = 1.0; ignored for 16-bit pools).  The pools hold
+ * num_blocks * block_size slots.
+ * Errors: those of pa_prepare_inputs and pa_cache_write_ex; PA_ERR_UNSUPPORTED
+ * also when a row or base address is not aligned as above (the two separate
+ * calls take any alignment).  Data checks as pa_prepare_inputs.
+ */
+pa_status pa_prepare_and_write(const int32_t *num_scheduled_tokens,
+                               const int32_t *num_computed_tokens, const int32_t *block_table,
+                               int32_t num_reqs, int32_t max_blocks_per_req, int32_t block_size,
+                               int32_t num_tokens, int32_t num_blocks, int32_t *req_indices,
+                               int32_t *positions, int32_t *slot_mapping,
+                               int32_t *query_start_loc, int32_t qsl_capacity, int32_t *seq_lens,
+                               int32_t *logits_indices, const void *key, const void *value,
+                               int64_t kv_token_stride, void *key_cache, void *value_cache,
+                               int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                               pa_dtype cache_dtype, const float *k_scale, const float *v_scale,
+                               pa_stream_t stream);
 
 /*
  * pa_prepare_inputs_ex -- pa_prepare_inputs plus the rest of the step's
@@ -322,8 +361,10 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens,
  * g = h / (num_q_heads / num_kv_heads):
  *     out[t][h] = sum_{j <= p} softmax_j(scale * q[t][h] . K_r[j][g]) V_r[j][g]
  * where K_r[j] is the cache entry at block_table[r][j / block_size],
- * offset j % block_size.  Accumulation is fp32; the output is rounded once
- * to the element type.
+ * offset j % block_size.  Accumulation is fp32; the softmax weights enter
+ * the weighted sum of V as f16, or for bf16 as two bf16 terms (the weight
+ * rounded, then the remainder rounded: 16 significant bits); the output is
+ * rounded once to the element type.
  *
  * Requests with more than 16 query tokens run on the tensor-core (tcgen05)
  * kernel when num_q_heads / num_kv_heads <= 128 and scale > 0; every other
@@ -367,9 +408,11 @@ pa_status pa_attention(const void *q, const void *key_cache, const void *value_c
  * Internally", section "FP8 KV Cache": cache_dtype == dtype is exactly
  * pa_attention; cache_dtype == PA_FP8_E4M3 reads one-byte E4M3 pools whose
  * cached key is element * *k_scale and cached value element * *v_scale
- * (device scalars; NULL = 1.0).  Every request runs on the split-K kernel
- * with its tensor-core MMAs in f16 (E4M3 widens to f16 exactly; bf16 q is
- * rounded to f16, exact inside f16's range); the output is dtype.  Errors as
+ * (device scalars; NULL = 1.0).  Requests go to the same two kernels as in
+ * pa_attention (more than 16 query tokens: the tcgen05 kernel; the rest: the
+ * split-K kernel); over FP8 pools both run their MMAs in f16 (E4M3 widens to
+ * f16 exactly; bf16 q is rounded to f16, exact inside f16's range; the
+ * softmax weights are f16).  The output is dtype.  Errors as
  * pa_attention, plus PA_ERR_INVALID for a cache_dtype that is neither dtype
  * nor PA_FP8_E4M3.
  *
@@ -416,7 +459,11 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
  *     longer KV partitions.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept per device and per
+ *     CUDA context (a context of one's own on the same device has its own
+ *     copy of the array and is looked up on its first call).  A device reset
+ *     (cudaDeviceReset) destroys the array with its context: the library
+ *     does not support calls on a device after it was reset.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents; nothing needs clearing (each call writes what it
  *     reads), but calls that overlap on the GPU (different streams, or

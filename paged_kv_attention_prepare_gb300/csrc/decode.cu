@@ -293,6 +293,15 @@ template <> struct Mma<__nv_bfloat16> {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
     }
+    // P enters the PV product as two bf16 terms, hi = bf16(p) and
+    // lo = bf16(p - hi): 16 significant bits instead of 8, so the weights
+    // add about 2^-17 of |v| to the error instead of 2^-9 (a near one-hot row
+    // with |v| near 4 would otherwise be off by 0.008 before the output's own
+    // rounding).
+    static constexpr bool kSplitP = true;
+    __device__ __forceinline__ static uint32_t residual(float lo, float hi, uint32_t packed) {
+        return pack(lo - __uint_as_float(packed << 16), hi - __uint_as_float(packed & 0xffff0000u));
+    }
 };
 template <> struct Mma<__half> {
     __device__ __forceinline__ static void run(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -307,6 +316,10 @@ template <> struct Mma<__half> {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
     }
+    // f16 P carries 11 significant bits (P <= 256 stays far from f16's
+    // limits): one term is enough.
+    static constexpr bool kSplitP = false;
+    __device__ __forceinline__ static uint32_t residual(float, float, uint32_t) { return 0u; }
 };
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
@@ -822,7 +835,8 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             if (lane == 0) mbar_arrive_n(&empty[stK], release);
 
             // ---- online softmax with a lazily moved reference max: P stays
-            //      below 2^8, so the 16-bit P and the f32 sums are exact enough,
+            //      below 2^8 (inside the 16-bit types' range; bf16 P enters
+            //      the PV product as a hi + lo pair), the sums stay in f32,
             //      and O is rescaled only when a row's max grows by more than 8
             //      (in log2 units).
             if (!unit_visible) {
@@ -862,7 +876,8 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 l0 *= al0;
                 l1 *= al1;
             }
-            uint32_t pb[kSP][2];
+            constexpr bool kSplit = Mma<TM>::kSplitP;
+            uint32_t pb[kSP][2], pl[kSP][2];
 #pragma unroll
             for (int sp = 0; sp < kSP; ++sp) {
                 float pv[4];
@@ -879,8 +894,13 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                 }
                 l0 += pv[0] + pv[2];
                 l1 += pv[1] + pv[3];
-                pb[sp][0] = movmatrix_trans(Mma<TM>::pack(pv[0], pv[1]));
-                pb[sp][1] = movmatrix_trans(Mma<TM>::pack(pv[2], pv[3]));
+                const uint32_t h0 = Mma<TM>::pack(pv[0], pv[1]), h1 = Mma<TM>::pack(pv[2], pv[3]);
+                pb[sp][0] = movmatrix_trans(h0);
+                pb[sp][1] = movmatrix_trans(h1);
+                if constexpr (kSplit) {
+                    pl[sp][0] = movmatrix_trans(Mma<TM>::residual(pv[0], pv[1], h0));
+                    pl[sp][1] = movmatrix_trans(Mma<TM>::residual(pv[2], pv[3], h1));
+                }
             }
 
             // ---- O^T += V^T P^T, page by page
@@ -889,6 +909,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
             if (!have[sp]) break;
             const int key0 = keyb[sp];
             const uint32_t pb0 = pb[sp][0], pb1 = pb[sp][1];
+            const uint32_t pl0 = kSplit ? pl[sp][0] : 0u, pl1 = kSplit ? pl[sp][1] : 0u;
             const unsigned char *vpage = stages + stV * C::kUnitBytes + sp * L::kPageBytes;
             // Slots past the context hold stale data (maybe NaN): on a partial
             // page their V is zeroed in registers (their P is already 0).
@@ -915,6 +936,7 @@ paged_decode_kernel(const __grid_constant__ Params p) {
                             a[3] &= mhi;
                         }
                         Mma<TM>::run(o[mt], a[0], a[1], a[2], a[3], pb0, pb1);
+                        if constexpr (kSplit) Mma<TM>::run(o[mt], a[0], a[1], a[2], a[3], pl0, pl1);
                     }
                 } else {
                     // D/32 words per key: dims gq*D/8 + 4 tp .. + 3; byte-interleave

@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,6 +45,13 @@ struct PrepArgs {
 };
 
 pa_status launch_prepare(const PrepArgs &a, cudaStream_t stream);
+// The index build (no optional groups) and the cache write in one launch;
+// PA_ERR_UNSUPPORTED when the rows are not 16-byte aligned (8-byte FP8 pool
+// rows).
+pa_status launch_prepare_write(const PrepArgs &a, const void *key, const void *value,
+                               int64_t stride_elems, void *kc, void *vc, int32_t row_elems,
+                               pa_dtype dtype, pa_dtype cache_dtype, const float *k_scale,
+                               const float *v_scale, cudaStream_t stream);
 
 pa_status launch_copy_blocks(void *kc, void *vc, int64_t block_bytes, int32_t num_blocks,
                              const int32_t *src, const int32_t *dst, int32_t n,
@@ -107,6 +115,37 @@ bool encode_pool_map_swizzled(CUtensorMap *map, const void *pool, int64_t num_sl
 
 __device__ __forceinline__ void flag(unsigned int *status, unsigned int bit) {
     atomicOr(status, bit);
+}
+
+// Block-wide exclusive scan of one value per thread.  Returns the thread's
+// exclusive prefix and sets `total` to the block's sum.  `sh` is 33 shared
+// ints (one per warp plus the total); it is free again on return.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *sh, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w0 = lane < nwarps ? sh[lane] : 0;
+        int w = w0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        if (lane < nwarps) sh[lane] = w - w0;
+        if (lane == 31) sh[32] = w;
+    }
+    __syncthreads();
+    const int r = sh[warp] + incl - v;
+    total = sh[32];
+    __syncthreads();
+    return r;
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -240,6 +279,25 @@ template <> struct Elt<__half> {
         return *reinterpret_cast<uint32_t *>(&h);
     }
 };
+
+// Eight 16-bit elements (one 16-byte load, element 0 in the low half of the
+// first word) to E4M3 codes (element 0 in the low byte): each divided by
+// `scale` in IEEE single precision (correctly rounded), then rounded to the
+// nearest E4M3 value, ties to even, saturating at +-448 (NaN stays NaN).
+template <typename T>
+__device__ __forceinline__ uint2 quantize8_e4m3(const uint4 src, float scale) {
+    const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float x0, x1;
+        Elt<T>::unpack2(w[e], x0, x1);
+        const uint32_t q = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale)), __NV_SATFINITE, __NV_E4M3);
+        out[e >> 1] |= (q & 0xffffu) << (16 * (e & 1));
+    }
+    return make_uint2(out[0], out[1]);
+}
 
 }  // namespace pa
 

@@ -57,10 +57,22 @@ constexpr int kBN = 128;          // keys per KV tile
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kBN / kPage;
 constexpr int kSoftmaxWarps = 8;   // four per slot
-constexpr int kConvWarps = 2;      // FP8 pools: widening E4M3 -> f16 in shared memory
-__host__ __device__ constexpr int threads_for(bool f8) {
-    return (2 + kSoftmaxWarps + (f8 ? kConvWarps : 0)) * 32;
+constexpr int kConvWarps = 2;      // FP8 pools: E4M3 -> f16; bf16 pools: V tiles bf16 -> f16
+__host__ __device__ constexpr int threads_for(bool conv) {
+    return (2 + kSoftmaxWarps + (conv ? kConvWarps : 0)) * 32;
 }
+// Which tiles the two converter warps rewrite in shared memory before the
+// tensor core reads them.  FP8 pools: Q (bf16 -> f16), K and V (E4M3 -> f16).
+// bf16 pools: V only, so that P enters PV as f16 (11 significant bits; a
+// bf16 P would add up to 2^-9 of |v| to the error).  fp16 pools: none.
+template <typename T, bool F8>
+struct Conv {
+    static constexpr bool kV = !F8 && std::is_same<T, __nv_bfloat16>::value;
+    static constexpr bool kAny = F8 || kV;
+};
+// Largest magnitude (bits without the sign) of a bf16 value that f16
+// represents: 65280; the next bf16 value, 65536, is past f16's 65504.
+constexpr uint32_t kBf16F16Max = 0x477Fu;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 constexpr int kTauDefault = 16;           // longer query chunks take this kernel
@@ -90,7 +102,8 @@ struct Cfg {
     static constexpr int kTileBytes = kBN * D * 2;
     static constexpr int kHalfBytes = kBN * 128;         // one 64-dim half of a K/V tile
     static constexpr int kPageHalfBytes = kPage * 128;
-    static constexpr int kSmem = 2 * kQBytes + 4 * kTileBytes + 512 + 1024;
+    // Q (2 tiles), K (2 stages), V (vst stages), barriers and slack to align
+    static constexpr int smem(int vst) { return 2 * kQBytes + (2 + vst) * kTileBytes + 512 + 1024; }
     // FP8 pools at head_dim 64: 64-byte rows of K and V, two stages each,
     // staged after the barriers (1024-byte aligned) before widening
     static constexpr int kLandBytes = kBN * 64;
@@ -103,16 +116,18 @@ struct Cfg {
 
 // Barrier slots (uint64) in shared memory.
 enum {
-    B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
-    B_VEMPTY, B_VEMPTY1,
-    B_SFULL,      // [2] per slot: S_X ready
+    B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1,
+    B_VFULL,                 // [3] per V stage (two or three in use)
+    B_VEMPTY = B_VFULL + 3,  // [3]
+    B_SFULL = B_VEMPTY + 3,  // [2] per slot: S_X ready
     B_PFULL = B_SFULL + 2,   // [2] per slot: P_X written (one arrive per softmax warp)
     B_ODONE = B_PFULL + 2,   // [2] per slot: the item's last PV_X done
     B_OFREE = B_ODONE + 2,   // [2] per slot: O_X read out by the epilogue
     B_DRAIN = B_OFREE + 2,
     B_QLAND,      // FP8 pools: TMA bytes landed, before widening
-    B_KLAND, B_KLAND1, B_VLAND, B_VLAND1,
-    B_IFULL,                      // [kQueue] item queue entry written by the producer
+    B_KLAND, B_KLAND1,
+    B_VLAND,                      // [3]
+    B_IFULL = B_VLAND + 3,        // [kQueue] item queue entry written by the producer
     B_IEMPTY = B_IFULL + 4,       // [kQueue] entry read by every other warp
     B_COUNT = B_IEMPTY + 4
 };
@@ -184,6 +199,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
+        : "r"(taddr));
+}
+
+// 32 lanes x 16 columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 
@@ -385,21 +411,106 @@ __device__ __forceinline__ void widen_e4m3_rows64(const unsigned char *land, uns
     }
 }
 
+// One 64-key half of a bf16 V tile (keys 64 h .. 64 h + 63: 8 KiB of
+// 128-byte rows in each 64-dim half of the tile, at v0 + dh * half_bytes)
+// to f16 in place, when f16 holds every value of its first `valid` keys
+// (the keys inside the context; the rest is zeroed before the tensor core
+// reads the tile).  Elementwise, so the swizzle does not matter.  Values
+// below f16's normal range round to its subnormals (an absolute error of
+// 2^-25 at most).  Returns 0 when converted; 1 when some value is past
+// 65280 in magnitude, infinite or NaN: the half stays bf16 (its P is then
+// written as a bf16 pair).
+template <int kHalves>
+__device__ __forceinline__ int v_half_to_f16(unsigned char *v0, int half_bytes, int valid, int lane) {
+    uint32_t mx = 0;
+#pragma unroll
+    for (int dh = 0; dh < kHalves; ++dh)
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const int c = lane + 32 * i;   // 16-byte chunk; row c / 8
+            if (c / 8 < valid) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(v0 + dh * half_bytes + c * 16);
+                mx = __vmaxu2(mx, x.x & 0x7fff7fffu);
+                mx = __vmaxu2(mx, x.y & 0x7fff7fffu);
+                mx = __vmaxu2(mx, x.z & 0x7fff7fffu);
+                mx = __vmaxu2(mx, x.w & 0x7fff7fffu);
+            }
+        }
+    mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
+    if (mx > kBf16F16Max) return 1;
+#pragma unroll
+    for (int dh = 0; dh < kHalves; ++dh)
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(v0 + dh * half_bytes + (lane + 32 * i) * 16);
+            uint4 x = *ptr;
+            uint32_t *w = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __half2 h = __floats2half2_rn(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xffff0000u));
+                w[e] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            *ptr = x;
+        }
+    return 0;
+}
+
+// Rewrite the f16 P of the key halves set in `halves` (bit h: keys 64h ..
+// 64h+63, columns 64h .. 64h+31 of this warp's TMEM lanes) as bf16 pairs:
+// hi = bf16(p) in the same columns, lo = bf16(p - hi) in 64h+32 .. 64h+63.
+// Both are exact: an f16 value's 11 significant bits are hi's 8 and lo's 3.
+__device__ __noinline__ void split_p_halves(uint32_t colS, int halves) {
+    for (int h = 0; h < 2; ++h) {
+        if (!((halves >> h) & 1)) continue;
+        for (int c0 = 0; c0 < 32; c0 += 16) {
+            uint32_t w[16], wl[16];
+            tmem_ld16(colS + 64 * h + c0, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                float a, b, ha, hb;
+                Elt<__half>::unpack2(w[e], a, b);
+                w[e] = Elt<__nv_bfloat16>::pack2(a, b);
+                Elt<__nv_bfloat16>::unpack2(w[e], ha, hb);
+                wl[e] = Elt<__nv_bfloat16>::pack2(a - ha, b - hb);
+            }
+            tmem_st16(colS + 64 * h + c0, w);
+            tmem_st16(colS + 64 * h + 32 + c0, wl);
+        }
+    }
+    tmem_wait_st();
+}
+
 template <typename T, int D, bool F8>
-__global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(threads_for(Conv<T, F8>::kAny), 1)
+paged_prefill_kernel(const __grid_constant__ Params p) {
     using C = Cfg<D>;
-    using TM = typename std::conditional<F8, __half, T>::type;   // the MMAs' input type
+    // QK runs in q's type (f16 over FP8 pools); PV runs in f16: P as f16
+    // and V as f16 (bf16 pools: converted in shared memory first).  A bf16
+    // V half that f16 cannot hold stays bf16, and its f16 P is rewritten as
+    // two bf16 terms (split_p_halves) for two PV MMAs: the same P, exactly.
+    // P of keys 64h .. 64h+63 of a tile: f16 (or hi) in S columns 64h ..
+    // 64h+31, lo in 64h+32 .. 64h+63.
+    using TQK = typename std::conditional<F8, __half, T>::type;
+    constexpr bool kConvV = Conv<T, F8>::kV;
+    constexpr bool kConv = Conv<T, F8>::kAny;
+    // V ring stages.  bf16 pools take three: the softmax reads a V tile's
+    // format before it writes P, so V_j must have landed and been converted
+    // by S_j, one tile earlier than PV_j needs it.
+    constexpr int kVSt = kConvV ? 3 : 2;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *sQ = base;                       // 2 tiles: slot A, slot B
     unsigned char *sK = sQ + 2 * C::kQBytes;        // 2 stages
-    unsigned char *sV = sK + 2 * C::kTileBytes;     // 2 stages
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sV + 2 * C::kTileBytes);
+    unsigned char *sV = sK + 2 * C::kTileBytes;     // kVSt stages
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sV + kVSt * C::kTileBytes);
     unsigned char *sL = base + C::kLandOffset;      // FP8 at head_dim 64: [K st0, K st1, V st0, V st1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *q_items = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [kQueue]
+    // bf16 pools: per V stage and key half, 1 when the half stayed bf16
+    volatile int *v_fmt = reinterpret_cast<volatile int *>(tmem_slot + 2 + kQueue);   // [kVSt][2]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -413,11 +524,11 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i) {
             const bool per_warp = (i >= B_PFULL && i < B_PFULL + 2) || (i >= B_OFREE && i < B_OFREE + 2);
-            // FP8: Q/K/V full are signalled by the widening warps
-            const bool widened = F8 && (i == B_QFULL || (i >= B_KFULL && i <= B_KFULL1) ||
-                                        (i >= B_VFULL && i <= B_VFULL1));
+            // FP8: Q/K/V full are signalled by the widening warps; bf16: V full
+            const bool widened = (F8 && (i == B_QFULL || (i >= B_KFULL && i <= B_KFULL1))) ||
+                                 (kConv && i >= B_VFULL && i < B_VFULL + 3);
             const bool readers = i >= B_IEMPTY && i < B_IEMPTY + kQueue;   // every warp but 0
-            mbar_init(&bar[i], readers ? 1 + kSoftmaxWarps + (F8 ? kConvWarps : 0)
+            mbar_init(&bar[i], readers ? 1 + kSoftmaxWarps + (kConv ? kConvWarps : 0)
                                        : per_warp ? kSoftmaxWarps / 2 : (widened ? kConvWarps : 1));
         }
         fence_mbar_init();
@@ -531,19 +642,22 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                         blk = 0;
                     }
                 }
-                const int st = (int)(t & 1);
-                const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                // K ring: two stages; V ring: kVSt
+                const int kst = (int)(t & 1), vst = (int)(t % kVSt);
+                const uint32_t kph = (uint32_t)((t >> 1) & 1), vph = (uint32_t)((t / kVSt) & 1);
                 // FP8: one D-byte row per slot (head_dim 128: into the tile's
                 // upper half; 64: into the staging area)
                 const uint32_t bytes = F8 ? (uint32_t)npg * kPage * D
                                           : (uint32_t)npg * C::kHalves * C::kPageHalfBytes;
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv) {
-                    uint64_t *fullb = &bar[(F8 ? (kv ? B_VLAND : B_KLAND) : (kv ? B_VFULL : B_KFULL)) + st];
+                    const int st = kv ? vst : kst;
+                    uint64_t *fullb = &bar[(F8 ? (kv ? B_VLAND : B_KLAND)
+                                               : (kv ? (kConvV ? B_VLAND : B_VFULL) : B_KFULL)) + st];
                     uint64_t *emptyb = &bar[(kv ? B_VEMPTY : B_KEMPTY) + st];
                     unsigned char *dst = (kv ? sV : sK) + st * C::kTileBytes;
                     if (lane == 0) {
-                        if (!mbar_wait(emptyb, ph ^ 1)) ok = false;
+                        if (!mbar_wait(emptyb, (kv ? vph : kph) ^ 1)) ok = false;
                         else mbar_arrive_expect_tx(fullb, bytes);
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -569,14 +683,15 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
         if (!ok) fail();
         // Drain: the last copies issued into each ring must have landed.
         if (lane == 0) {
-            const int kf = F8 ? B_KLAND : B_KFULL, vf = F8 ? B_VLAND : B_VFULL;
+            const int kf = F8 ? B_KLAND : B_KFULL, vf = kConv ? B_VLAND : B_VFULL;
             if (lastK >= 0) mbar_wait(&bar[kf + (int)(lastK & 1)], (uint32_t)((lastK >> 1) & 1));
-            if (lastV >= 0) mbar_wait(&bar[vf + (int)(lastV & 1)], (uint32_t)((lastV >> 1) & 1));
+            if (lastV >= 0) mbar_wait(&bar[vf + (int)(lastV % kVSt)], (uint32_t)((lastV / kVSt) & 1));
         }
     } else if (warp == 1) {
         // =================== MMA issuer ===================
-        const uint32_t idQK = instr_desc<TM>(kBM, kBN, 0);
-        const uint32_t idPV = instr_desc<TM>(kBM, D, 1);
+        const uint32_t idQK = instr_desc<TQK>(kBM, kBN, 0);
+        const uint32_t idPV = instr_desc<__half>(kBM, D, 1);
+        const uint32_t idPVb = instr_desc<__nv_bfloat16>(kBM, D, 1);   // bf16 V halves
         long long t0 = 0;           // KV tiles of earlier items
         long long cnt[2] = {0, 0};  // tiles processed per slot (barrier phases)
         int its[2] = {0, 0};        // items processed per slot
@@ -620,25 +735,48 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 }
                 for (int j = 0; ok && j < nt; ++j) {
                     const long long t = t0 + j;
-                    const int st = (int)(t & 1);
-                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                    const int st = (int)(t % kVSt);   // V stage of tile t
+                    const uint32_t ph = (uint32_t)((t / kVSt) & 1);
                     bool v_ready = false, k_next_ready = false;
                     const long long t1 = t + 1;
+                    // V of this tile (normally landed long before P) and, over
+                    // bf16 pools, which of its key halves stayed bf16: read
+                    // before waiting for P, off the P -> PV path
+                    int bfh = 0;
                     for (int sl = 0; ok && sl < 2; ++sl) {
                         if (j >= ns[sl]) continue;
+                        if (!v_ready) {
+                            if (!wait_or_fail(&bar[B_VFULL + st], ph)) break;
+                            v_ready = true;
+                            if constexpr (kConvV) bfh = v_fmt[2 * st] | (v_fmt[2 * st + 1] << 1);
+                        }
                         if (!wait_or_fail(&bar[B_PFULL + sl], (uint32_t)(cnt[sl] & 1))) break;
-                        if (!v_ready && !wait_or_fail(&bar[B_VFULL + st], ph)) break;
-                        v_ready = true;
                         if (j == 0 && !wait_or_fail(&bar[B_OFREE + sl], (uint32_t)((its[sl] & 1) ^ 1)))
                             break;
                         tc_fence_after();
                         const uint64_t dv0 = smem_desc_sw128(smem_u32(sV + st * C::kTileBytes),
                                                              C::kHalfBytes, 1024);
+                        if (!bfh) {
 #pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk)
-                            mma_ts(tmem + C::col_o(sl), tmem + C::col_s(sl) + 8 * kk,
-                                   dv0 + (uint64_t)(kk * 2048 >> 4), idPV,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < kBN / 16; ++kk)
+                                mma_ts(tmem + C::col_o(sl),
+                                       tmem + C::col_s(sl) + (kk >> 2) * 64 + (kk & 3) * 8,
+                                       dv0 + (uint64_t)(kk * 2048 >> 4), idPV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                        } else {
+                            // a bf16 half: P as hi and lo, two bf16 MMAs per step
+                            for (int kk = 0; kk < kBN / 16; ++kk) {
+                                const uint32_t pa = tmem + C::col_s(sl) + (kk >> 2) * 64 + (kk & 3) * 8;
+                                const uint64_t dv = dv0 + (uint64_t)(kk * 2048 >> 4);
+                                const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                                if ((bfh >> (kk >> 2)) & 1) {
+                                    mma_ts(tmem + C::col_o(sl), pa, dv, idPVb, acc);
+                                    mma_ts(tmem + C::col_o(sl), pa + 32, dv, idPVb, 1u);
+                                } else {
+                                    mma_ts(tmem + C::col_o(sl), pa, dv, idPV, acc);
+                                }
+                            }
+                        }
                         // O_X is read only by the epilogue, after the item's last
                         // PV; a rescale before that is ordered by S_FULL, whose
                         // commit covers every earlier MMA of this thread.
@@ -677,7 +815,39 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
             mbar_wait(&bar[B_DRAIN], 0);
         }
     } else if (warp >= 2 + kSoftmaxWarps) {
-        // =================== FP8: widen landed tiles to f16 (warps 10, 11) ===================
+        // =================== converters (warps 10, 11) ===================
+        if constexpr (kConvV) {
+            // bf16 pools: each landed V tile to f16, warp cw taking keys
+            // 64 cw .. 64 cw + 63; the format of each half for the softmax
+            // and MMA warps, then V full.
+            const int cw = warp - (2 + kSoftmaxWarps);
+            long long t = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const long long ik = item_at(k);
+                if (ik < 0 || !walk.find(ik, lane, it)) break;
+                const int nt = max(slot_tiles(p, it, 0), slot_tiles(p, it, 1));
+                for (int j = 0; ok && j < nt; ++j, ++t) {
+                    const int st = (int)(t % kVSt);
+                    if (!mbar_wait_warp(&bar[B_VLAND + st], (uint32_t)((t / kVSt) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    const int valid = min(kBN, it.L - j * kBN) - 64 * cw;   // keys inside the context
+                    const int f = v_half_to_f16<C::kHalves>(sV + st * C::kTileBytes + cw * 64 * 128,
+                                                            C::kHalfBytes, valid, lane);
+                    if (lane == 0) v_fmt[2 * st + cw] = f;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[B_VFULL + st]);
+                }
+                if (*abort_flag) ok = false;
+            }
+            if (!ok) fail();
+        }
+        // FP8 pools: widen landed Q, K and V tiles to f16 (K and V rings of
+        // two stages each, same index)
+        static_assert(!F8 || kVSt == 2, "FP8 pools use a two-stage V ring");
         if constexpr (F8) {
             const int cw = warp - (2 + kSoftmaxWarps);   // rows 64 cw .. 64 cw + 63 of each tile
             long long t = 0;
@@ -760,11 +930,23 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                 tc_fence_after();
                 const int key0 = j * kBN;
                 const bool full_tile = key0 + kBN - 1 <= pos;
+                // bf16 pools: which key halves of this tile's V stayed bf16
+                // (V_j has normally landed and been converted by S_j)
+                int vfmt = 0;
+                if constexpr (kConvV) {
+                    const long long tv = t0 + j;
+                    const int vst = (int)(tv % kVSt);
+                    if (!mbar_wait_warp(&bar[B_VFULL + vst], (uint32_t)((tv / kVSt) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    vfmt = v_fmt[2 * vst] | (v_fmt[2 * vst + 1] << 1);
+                }
                 if constexpr (!F8) {
                     // One TMEM pass, 64 columns at a time: the half's row max (scale
                     // > 0 keeps the argmax), then P = exp2(s*c - m_ref) in packed
-                    // pairs written over the scores already read (64 keys ->
-                    // columns 32hh..32hh+31).  The reference max moves lazily:
+                    // f16 pairs written over the scores already read (64 keys ->
+                    // columns 64hh..64hh+31).  The reference max moves lazily:
                     // only when a half's max passes it by more than 2^8, so P stays
                     // below 256.  Sums and O accumulated against an older reference
                     // are scaled down when it moves: the tile's first half in
@@ -808,8 +990,8 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
     #pragma unroll
                             for (int e = 0; e < 32; ++e) {
                                 float a, b;
-                                Elt<TM>::unpack2(w[e], a, b);
-                                w[e] = Elt<TM>::pack2(a * alpha, b * alpha);
+                                Elt<__half>::unpack2(w[e], a, b);
+                                w[e] = Elt<__half>::pack2(a * alpha, b * alpha);
                             }
                             tmem_st32(colS, w);
                         }
@@ -823,9 +1005,9 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                             y.x = fast_exp2(y.x);
                             y.y = fast_exp2(y.y);
                             acc[e & 1] = __fadd2_rn(acc[e & 1], y);
-                            w[e] = Elt<TM>::pack2(y.x, y.y);
+                            w[e] = Elt<__half>::pack2(y.x, y.y);
                         }
-                        tmem_st32(colS + hh * 32, w);
+                        tmem_st32(colS + hh * 64, w);
                     }
                     if (j > 0 && __any_sync(0xffffffffu, m_ref != m_prev)) {
                         // O holds PV of tiles < j, all complete: S_j's commit (waited
@@ -844,6 +1026,12 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                     }
                     tmem_wait_st();
                     l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                    // A key half whose V stayed bf16 (it holds a value f16
+                    // cannot): its f16 P, rewritten as two bf16 terms hi and
+                    // lo (an f16 value's 11 significant bits split exactly
+                    // into 8 + 3), hi in columns 64hh .. 64hh+31, lo in
+                    // 64hh+32 .. 64hh+63, for two bf16 PV MMAs.
+                    if (kConvV && vfmt) split_p_halves(colS, vfmt);
                 } else {
                     // FP8 pools: two passes over the scores (row max, then P).
                     // The one-pass form above measured slower here when scores
@@ -887,8 +1075,8 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                         if (need) l *= alpha;
                     }
                     if (need) m_ref = mx;
-                    // Pass 2: P = exp2(s*c - m_ref) in packed pairs, written over
-                    // the scores already read (64 keys -> columns 32hh..32hh+31).
+                    // Pass 2: P = exp2(s*c - m_ref) in packed f16 pairs, written
+                    // over the scores already read (64 keys -> columns 64hh..64hh+31).
                     // A row with no visible key is never written out, so any NaN
                     // stays in its own row.
                     const float2 mneg = make_float2(-m_ref, -m_ref);
@@ -912,9 +1100,9 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                             y.x = fast_exp2(y.x);
                             y.y = fast_exp2(y.y);
                             acc[e & 1] = __fadd2_rn(acc[e & 1], y);
-                            w[e] = Elt<TM>::pack2(y.x, y.y);
+                            w[e] = Elt<__half>::pack2(y.x, y.y);
                         }
-                        tmem_st32(colS + hh * 32, w);
+                        tmem_st32(colS + hh * 64, w);
                     }
                     tmem_wait_st();
                     l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
@@ -925,10 +1113,10 @@ __global__ void __launch_bounds__(threads_for(F8), 1) paged_prefill_kernel(const
                     // zero so 0 * V stays 0 in the tensor core.  The slot's
                     // four warps reach the barrier even if the wait timed out.
                     const long long tv = t0 + j;
-                    const bool landed = mbar_wait_warp(&bar[B_VFULL + (int)(tv & 1)],
-                                                       (uint32_t)((tv >> 1) & 1));
+                    const bool landed = mbar_wait_warp(&bar[B_VFULL + (int)(tv % kVSt)],
+                                                       (uint32_t)((tv / kVSt) & 1));
                     if (landed) {
-                        unsigned char *vt = sV + (int)(tv & 1) * C::kTileBytes;
+                        unsigned char *vt = sV + (int)(tv % kVSt) * C::kTileBytes;
                         const int first = it.L - key0;
                         const int rows = kBN - first;
                         for (int xx = row; xx < rows * C::kHalves * 8; xx += kBM) {
@@ -1023,7 +1211,8 @@ bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, u
 template <typename T, int D, bool F8>
 pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) {
     using C = Cfg<D>;
-    constexpr int kSmem = (F8 && D == 64) ? C::kSmemF8Land : C::kSmem;
+    constexpr int kSmem = (F8 && D == 64) ? C::kSmemF8Land : C::smem(Conv<T, F8>::kV ? 3 : 2);
+    static_assert(kSmem <= 232448, "shared memory per CTA");
     static bool configured[64] = {};
     int dev = 0;
     PA_TRY_CUDA(cudaGetDevice(&dev));
@@ -1035,7 +1224,7 @@ pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) 
     long long grid = num_sms();
     if (items < grid) grid = items;
     if (grid < 1) return PA_OK;
-    paged_prefill_kernel<T, D, F8><<<(int)grid, threads_for(F8), kSmem, stream>>>(prm);
+    paged_prefill_kernel<T, D, F8><<<(int)grid, threads_for(Conv<T, F8>::kAny), kSmem, stream>>>(prm);
     PA_TRY_CUDA(cudaGetLastError());
     note_launch();
     return PA_OK;

@@ -19,37 +19,6 @@ namespace pa {
 constexpr int kPrepThreads = 1024;
 constexpr int kPrepMaxReqs = 50000;
 
-// Block-wide exclusive scan of one value per thread.  Returns the thread's
-// exclusive prefix and sets `total` to the block's sum.  `sh` is 33 shared
-// ints (one per warp plus the total); it is free again on return.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *sh, int &total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-    }
-    if (lane == 31) sh[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int w0 = lane < nwarps ? sh[lane] : 0;
-        int w = w0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += u;
-        }
-        if (lane < nwarps) sh[lane] = w - w0;
-        if (lane == 31) sh[32] = w;
-    }
-    __syncthreads();
-    const int r = sh[warp] + incl - v;
-    total = sh[32];
-    __syncthreads();
-    return r;
-}
-
 __global__ void __launch_bounds__(kPrepThreads)
 prepare_inputs_kernel(const PrepArgs a, unsigned int *status) {
     extern __shared__ int32_t s_start[];  // [R + 1]: first flat token of each request

@@ -13,6 +13,49 @@ import torch
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
+ATOL = 1e-2
+
+
+def attention_tolerance(ref: np.ndarray, out_dtype: torch.dtype) -> np.ndarray:
+    """Per-element bound on |gpu - oracle| for an attention output of type
+    ``out_dtype``: 1e-2 (bf16/fp16 output, fp32 accumulation).  Where the
+    type's spacing near the exact value is so coarse that no value of the type
+    need lie within 1e-2 of it (|o| >= 4 in bf16, |o| >= 32 in fp16: half a
+    spacing is 1/64 or more), the bound is that half spacing plus the
+    arithmetic's share, which grows with the output: 2^-10 |o| + 2e-3 (the
+    softmax weights carry 11 significant bits or more)."""
+    bits = 8 if out_dtype == torch.bfloat16 else 11      # significant bits of the type
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.maximum(a, np.finfo(np.float64).tiny)))
+    coarse = np.exp2(e - bits) + a * 2.0 ** -10 + 2e-3
+    return np.where(np.exp2(e - bits) + 2e-3 > ATOL, coarse, ATOL)
+
+
+# (test, output dtype, largest error where the bound is 1e-2, largest error
+# elsewhere, elements compared) of every check_attention_close call; written
+# out at the end of a session when PA_ERROR_LOG names a file
+ERRORS: list = []
+
+
+def check_attention_close(got: np.ndarray, ref: np.ndarray, out_dtype: torch.dtype) -> float:
+    """Assert every element of ``got`` within ``attention_tolerance`` of the
+    oracle's ``ref``; returns the largest absolute error."""
+    assert np.isfinite(got).all()
+    if got.size == 0:
+        return 0.0
+    err = np.abs(got - ref)
+    tol = attention_tolerance(ref, out_dtype)
+    plain = tol <= ATOL
+    ERRORS.append((os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], str(out_dtype),
+                   float(err[plain].max()) if plain.any() else 0.0,
+                   float(err[~plain].max()) if (~plain).any() else 0.0, int(err.size)))
+    bad = np.argwhere(err > tol)
+    assert bad.size == 0, (f"{len(bad)} elements past the bound; max abs error {err.max()} "
+                           f"at {np.unravel_index(np.argmax(err), err.shape)}; first bad "
+                           f"{tuple(bad[0])}: got {got[tuple(bad[0])]}, oracle {ref[tuple(bad[0])]}")
+    return float(err.max())
+
+
 def golden(name: str) -> dict:
     with open(os.path.join(GOLDEN, name)) as f:
         return json.load(f)
