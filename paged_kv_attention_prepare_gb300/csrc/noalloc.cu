@@ -9,6 +9,8 @@
 // takes the same inputs and outputs as pa_attention and uses a fixed array
 // in the library's own device memory as the workspace instead of one the
 // caller passes.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pa_internal.cuh"
@@ -23,18 +25,40 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+// The array's address as last looked up on each device, and the CUDA context
+// that was current then.  A module -- and with it the array -- is loaded once
+// per context, so a caller that makes another context current on the same
+// device (driver-API contexts) gets the lookup again.
 void *g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch on the current device.  Host code must not
+// Device address of the scratch in the current context.  Host code must not
 // hand the array's name to a kernel: on the host it is only a stand-in.
 pa_status scratch_address(void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_ctx_current) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return PA_ERR_CUDA;
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    }
+    // No context is current before the runtime's first call on this thread
+    // that needs one; the lookup below makes the device's primary context
+    // current in that case.
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return PA_ERR_CUDA;
+    if (!ctx || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+        if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return PA_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return PA_OK;
