@@ -7,7 +7,7 @@ CUDA kernels; there is no CPU or PyTorch fallback, and using the package
 without the built library raises immediately.
 
 Functions carry the C names: ``pa_prepare_inputs``, ``pa_prepare_inputs_ex``,
-``pa_cache_write`` (over ``pa_cache_write_ex``), ``pa_copy_blocks``, ``pa_zero_blocks``,
+``pa_cache_write`` (over ``pa_cache_write_ex``), ``pa_prepare_and_write``, ``pa_copy_blocks``, ``pa_zero_blocks``,
 ``pa_attention_workspace_size``, ``pa_attention`` (over ``pa_attention_ex``),
 ``pa_attention_noalloc``,
 ``pa_get_status``, ``pa_launch_count``.
@@ -72,6 +72,10 @@ def lib():
             L.pa_prepare_inputs_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
                                                vp, vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp,
                                                vp, vp, vp]
+            L.pa_prepare_and_write.restype = ctypes.c_int
+            L.pa_prepare_and_write.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
+                                               vp, i32, vp, vp, vp, vp, i64, vp, vp, i32, i32,
+                                               ctypes.c_int, ctypes.c_int, vp, vp, vp]
             for fn in (L.pa_copy_blocks, L.pa_zero_blocks):
                 fn.restype = ctypes.c_int
             L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp]
@@ -241,6 +245,38 @@ def pa_cache_write(key, value, key_cache, value_cache, slot_mapping, num_blocks=
         hkv, d, bs, nb if num_blocks is None else int(num_blocks), dt, cdt,
         _scale_ptr(k_scale, "k_scale"), _scale_ptr(v_scale, "v_scale"), _stream(stream))
     _check(rc, "pa_cache_write")
+
+
+def pa_prepare_and_write(num_scheduled_tokens, num_computed_tokens, block_table, block_size,
+                         num_tokens, num_blocks, req_indices, positions, slot_mapping,
+                         query_start_loc, seq_lens, logits_indices, key, value, key_cache,
+                         value_cache, k_scale=None, v_scale=None, stream=None):
+    """``pa_prepare_inputs`` and ``pa_cache_write`` (same arguments) in one
+    launch: the index tensors, then each token's key/value row written to the
+    pools at its slot."""
+    i32 = torch.int32
+    R = num_scheduled_tokens.shape[0]
+    T, hkv, d = key.shape
+    if key.stride(1) != d or key.stride(2) != 1 or value.stride() != key.stride():
+        raise ValueError("key/value rows must be [Hkv, D]-contiguous with equal strides")
+    dt = _DTYPES.get(key.dtype)
+    if dt is None or value.dtype != key.dtype:
+        raise TypeError("key and value must share a bf16/fp16 dtype")
+    cdt = _cache_dtype(key.dtype, key_cache, value_cache)
+    rc = lib().pa_prepare_and_write(
+        _dev(num_scheduled_tokens, "num_scheduled_tokens", i32),
+        _dev(num_computed_tokens, "num_computed_tokens", i32),
+        _dev(block_table, "block_table", i32), R, block_table.shape[1] if R else 0,
+        int(block_size), int(num_tokens), int(num_blocks),
+        _dev(req_indices, "req_indices", i32), _dev(positions, "positions", i32),
+        _dev(slot_mapping, "slot_mapping", i32), _dev(query_start_loc, "query_start_loc", i32),
+        query_start_loc.shape[0], _dev(seq_lens, "seq_lens", i32),
+        _dev(logits_indices, "logits_indices", i32),
+        _dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
+        int(key.stride(0)) if T else hkv * d, _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), hkv, d, dt, cdt,
+        _scale_ptr(k_scale, "k_scale"), _scale_ptr(v_scale, "v_scale"), _stream(stream))
+    _check(rc, "pa_prepare_and_write")
 
 
 def _pools(key_cache, value_cache):

@@ -220,6 +220,48 @@ pa_status pa_prepare_inputs_ex(const int32_t *num_scheduled_tokens,
     return launch_prepare(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+pa_status pa_prepare_and_write(const int32_t *num_scheduled_tokens,
+                               const int32_t *num_computed_tokens, const int32_t *block_table,
+                               int32_t num_reqs, int32_t max_blocks_per_req, int32_t block_size,
+                               int32_t num_tokens, int32_t num_blocks, int32_t *req_indices,
+                               int32_t *positions, int32_t *slot_mapping,
+                               int32_t *query_start_loc, int32_t qsl_capacity, int32_t *seq_lens,
+                               int32_t *logits_indices, const void *key, const void *value,
+                               int64_t kv_token_stride, void *key_cache, void *value_cache,
+                               int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                               pa_dtype cache_dtype, const float *k_scale, const float *v_scale,
+                               pa_stream_t stream) {
+    PrepArgs a{};
+    a.nst = num_scheduled_tokens;
+    a.nct = num_computed_tokens;
+    a.bt = block_table;
+    a.R = num_reqs;
+    a.MB = max_blocks_per_req;
+    a.bs = block_size;
+    a.T = num_tokens;
+    a.NB = num_blocks;
+    a.num_logits = num_reqs;
+    a.req = req_indices;
+    a.pos = positions;
+    a.slot = slot_mapping;
+    a.qsl = query_start_loc;
+    a.qsl_cap = qsl_capacity;
+    a.seq_lens = seq_lens;
+    a.logits = logits_indices;
+    const pa_status st = check_prepare_core(a);
+    if (st != PA_OK) return st;
+    // the write's checks, as pa_cache_write_ex
+    if (num_kv_heads <= 0 || head_dim <= 0 || (dtype != PA_BF16 && dtype != PA_FP16) ||
+        (cache_dtype != dtype && cache_dtype != PA_FP8_E4M3))
+        return PA_ERR_INVALID;
+    if (kv_token_stride < (int64_t)num_kv_heads * head_dim) return PA_ERR_INVALID;
+    if (num_tokens > 0 && (!key || !value || !key_cache || !value_cache)) return PA_ERR_INVALID;
+    if ((int64_t)num_kv_heads * head_dim > INT32_MAX / 2) return PA_ERR_UNSUPPORTED;
+    return launch_prepare_write(a, key, value, kv_token_stride, key_cache, value_cache,
+                                num_kv_heads * head_dim, dtype, cache_dtype, k_scale, v_scale,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
 static pa_status check_block_op(void *kc, void *vc, const void *a, const void *b, int32_t n,
                                 int32_t bs, int32_t hkv, int32_t d, int32_t nb, pa_dtype dtype,
                                 int64_t *block_bytes) {

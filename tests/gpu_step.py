@@ -14,14 +14,15 @@ def to_dev(a, dev="cuda"):
 
 
 def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda",
-             shared_blocks=None):
+             shared_blocks=None, fused=False):
     """prep -> cache write -> attention on the GPU, on copies of the pools.
 
     ``vals`` holds the generator's tensors (any device).  Returns a dict with
     host numpy index arrays, the written pools (torch, on the GPU), the
     attention output (torch, on the GPU) and the status word.
     ``shared_blocks`` (the PA_ATTN_SHARED_BLOCKS flag) defaults to whether
-    the workload's tables share blocks."""
+    the workload's tables share blocks.  ``fused`` runs the index build and
+    the cache write as one call (pa_prepare_and_write)."""
     if shared_blocks is None:
         shared_blocks = w.shares_blocks
     i32 = torch.int32
@@ -34,9 +35,6 @@ def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda",
     out["query_start_loc"] = torch.full((cap,), -7, dtype=i32, device=dev)
     out["seq_lens"] = torch.full((R,), -7, dtype=i32, device=dev)
     out["logits_indices"] = torch.full((R,), -7, dtype=i32, device=dev)
-    pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, out["req_indices"],
-                         out["positions"], out["slot_mapping"], out["query_start_loc"],
-                         out["seq_lens"], out["logits_indices"])
     kc = vals["key_cache"].to(dev).clone()
     vc = vals["value_cache"].to(dev).clone()
     key = vals["key"].to(dev) if vals["key"].device.type != "cuda" else vals["key"]
@@ -44,7 +42,14 @@ def run_step(w, vals, *, workspace_bytes=None, qsl_capacity=None, dev="cuda",
     ks, vs = vals.get("k_scale"), vals.get("v_scale")   # FP8 pools only
     if ks is not None:
         ks, vs = ks.to(dev), vs.to(dev)
-    pa.pa_cache_write(key, value, kc, vc, out["slot_mapping"], k_scale=ks, v_scale=vs)
+    idx = (out["req_indices"], out["positions"], out["slot_mapping"], out["query_start_loc"],
+           out["seq_lens"], out["logits_indices"])
+    if fused:
+        pa.pa_prepare_and_write(nst, nct, bt, w.block_size, T, w.num_blocks, *idx, key, value,
+                                kc, vc, k_scale=ks, v_scale=vs)
+    else:
+        pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, *idx)
+        pa.pa_cache_write(key, value, kc, vc, out["slot_mapping"], k_scale=ks, v_scale=vs)
     q = vals["q"].to(dev).contiguous()
     o = torch.full_like(q, float("nan"))
     if workspace_bytes is None:

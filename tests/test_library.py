@@ -156,3 +156,25 @@ def test_binding_refuses_host_tensors():
     t = torch.zeros(4, dtype=torch.int32)
     with pytest.raises(TypeError):
         pa.pa_prepare_inputs(t, t, t.view(4, 1), 16, 4, 4, t, t, t, t, t, t)
+
+
+@pytest.mark.parametrize("case", ["short_stride", "bad_dtype", "bad_cache_dtype", "null_key",
+                                  "small_qsl"])
+def test_prepare_and_write_rejects_bad_arguments(case):
+    # host checks of the fused index build + cache write, before any launch
+    L = pa.lib()
+    a = dict(stride=128, dtype=pa.PA_BF16, cdt=pa.PA_BF16, key=FAKE, cap=4)
+    if case == "short_stride":
+        a["stride"] = 100
+    elif case == "bad_dtype":
+        a["dtype"] = 7
+    elif case == "bad_cache_dtype":
+        a["cdt"] = pa.PA_FP16
+    elif case == "null_key":
+        a["key"] = None
+    else:
+        a["cap"] = 2
+    rc = L.pa_prepare_and_write(FAKE, FAKE, FAKE, 3, 2, 16, 5, 8, FAKE, FAKE, FAKE, FAKE,
+                                a["cap"], FAKE, FAKE, a["key"], FAKE, a["stride"], FAKE, FAKE, 2,
+                                64, a["dtype"], a["cdt"], None, None, None)
+    assert rc == pa.PA_ERR_INVALID
