@@ -2,7 +2,7 @@
 paged attention) on synthetic workloads shaped like the pages' examples.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference]
+                    [--decode-workload NAME|none] [--impl ours|reference]
 
 Prints one JSON line.  A step is the whole path over one batch: the three
 C-ABI calls on inputs already resident in HBM, captured once into a CUDA
@@ -11,6 +11,13 @@ one by one).  The L2 is flushed (a 256 MB write) between timed steps,
 outside the timed events.  ``e2e`` repeats the step through the same public
 calls with the step's inputs copied from pinned host memory and the output
 copied back inside the timed region.
+
+The default workload is the mixed chunked-prefill step (one 5000-token
+chunk at 2048 computed plus 200 decodes), so one line carries both
+kernels' rooflines: ``roofline`` for the split-K kernel on the decode-class
+requests (HBM) and ``roofline_prefill`` for the tensor-core kernel on the
+chunk (bf16 tensor peak).  ``decode_workload`` adds the attention call of
+the 256-request decode batch, timed alone, with its own HBM roofline.
 
 Under torchrun every rank runs an independent replica (its own pool and
 requests, seeded by rank): the path has no exchange step.  Timing is the max
@@ -52,7 +59,11 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode", choices=sorted(workloads.NAMED))
+    ap.add_argument("--workload", default="mixed", choices=sorted(workloads.NAMED))
+    ap.add_argument("--decode-workload", default="decode",
+                    choices=sorted(workloads.NAMED) + ["none"],
+                    help="a decode-only workload whose attention call is also timed alone, "
+                         "with its HBM roofline (main arm, one GPU)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -128,11 +139,18 @@ def sub_batch(w, mask, q, bt_dev, qsl_host, sl_host, dev):
     return qs, qsl, sl, bts, int(n.max()), int(sl_host[reqs].max())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the split-K kernel's sources with comments and blank space
-    removed: a comment edit does not change the kernel the profile measured."""
+KERNEL_SOURCES = {
+    "paged_decode_kernel": ("decode.cu", "decode_fp16.cu", "pa_internal.cuh"),
+    "paged_prefill_kernel": ("prefill.cu", "pa_internal.cuh"),
+    "cache_write_kernel": ("cache_write.cu", "pa_internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str = "paged_decode_kernel") -> str:
+    """Hash of a kernel's sources with comments and blank space removed: a
+    comment edit does not change the kernel the profile measured."""
     h = hashlib.sha256()
-    for name in ("decode.cu", "decode_fp16.cu", "pa_internal.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_kv_attention_prepare_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -141,19 +159,22 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from a committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"paged_decode_kernel_{workload}.txt")
-    try:
-        text = open(path).read()
-    except OSError:
-        return None
-    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    if not m or not hm or hm.group(1) != kernel_source_hash():
-        return None
-    return float(m.group(1))
+def recorded_traffic(workload: str, kernel: str = "paged_decode_kernel"):
+    """DRAM bytes per launch of a kernel from a committed ncu summary
+    (``profiles/<kernel>_<workload>.txt`` or ``.md``), if it was taken on the
+    current kernel source."""
+    for ext in (".txt", ".md"):
+        path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}{ext}")
+        try:
+            text = open(path).read()
+        except OSError:
+            continue
+        m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+        if not m or not hm or hm.group(1) != kernel_source_hash(kernel):
+            return None
+        return float(m.group(1))
+    return None
 
 
 class ClockSampler:
@@ -270,13 +291,15 @@ class ClockSampler:
 # CPU oracle timing (cpu_baseline, and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, vals_host, seconds: float):
+def oracle_sample(w, vals_host, seconds: float, threads: int = 0):
     """Time the oracle on a bounded sample: the full index build and cache
     write, and attention for a growing random subset of tokens until about
-    ``seconds`` of CPU work.  Returns (tokens/s for the whole step, threads,
-    description)."""
+    ``seconds`` of CPU work, on ``threads`` host threads (0: every core).
+    Returns (tokens/s for the whole step, threads, description, phase times:
+    seconds for the index build, the cache write, and attention scaled to
+    the step)."""
     import oracle
-    nthreads = oracle.num_cpus()
+    nthreads = threads if threads > 0 else oracle.num_cpus()
     t0 = time.perf_counter()
     idx = oracle.prepare_inputs(w.num_scheduled_tokens, w.num_computed_tokens, w.block_table,
                                 w.block_size, w.num_tokens, w.num_blocks)
@@ -312,7 +335,20 @@ def oracle_sample(w, vals_host, seconds: float):
     step_s = (t1 - t0) + (t2 - t1) + per_token * w.num_tokens
     desc = (f"index build + cache write on all {w.num_tokens} tokens; attention on {done} "
             f"random tokens ({spent:.1f} s), scaled to the step's {w.num_tokens} tokens")
-    return w.num_tokens / step_s, nthreads, desc
+    phases = {"prep_s": t1 - t0, "write_s": t2 - t1, "attention_s": per_token * w.num_tokens,
+              "attention_tokens_sampled": int(done)}
+    return w.num_tokens / step_s, nthreads, desc, phases
+
+
+def cpu_baseline(w, vals_host, seconds: float) -> dict:
+    """The oracle on every host core (``value``) and on one thread, each on a
+    bounded sample of the step, with per-phase times."""
+    v, threads, desc, phases = oracle_sample(w, vals_host, seconds)
+    v1, _, desc1, phases1 = oracle_sample(w, vals_host, max(1.0, seconds / 4), threads=1)
+    return {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+            "phases": phases,
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1, "sample": desc1,
+                              "phases": phases1}}
 
 
 def host_values(vals):
@@ -328,9 +364,9 @@ def run_reference(args):
     budget = max(2.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(w, vals, budget / 4)
-    vals_s, threads, desc = [], 0, ""
+    vals_s, threads, desc, phases = [], 0, "", {}
     for _ in range(args.steps):
-        v, threads, desc = oracle_sample(w, vals, budget)
+        v, threads, desc, phases = oracle_sample(w, vals, budget)
         vals_s.append(v)
     value = float(np.median(vals_s))
     line = {
@@ -340,7 +376,7 @@ def run_reference(args):
         "data": "synthetic",
         "config": {"workload": w.name, "num_reqs": w.num_reqs, "num_tokens": w.num_tokens},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "phases": phases},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -349,6 +385,63 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # The CUDA path
 # ---------------------------------------------------------------------------
+
+def attention_alone(name, args, pa, dev, stream, flush, hbm_peak, peak_kind):
+    """Another workload's attention call timed alone: its index build and
+    cache write run first (untimed), then pa_attention on its whole batch is
+    timed with CUDA events, the L2 flushed before each launch.  Returns the
+    workload's name, the call's time and its HBM roofline."""
+    import torch
+    w = workloads.named(name)
+    vals = workloads.make_values(w, 1, device=dev)
+    i32 = torch.int32
+    R, T = w.num_reqs, w.num_tokens
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    nst, nct, bt = up(w.num_scheduled_tokens), up(w.num_computed_tokens), up(w.block_table)
+    req, pos, slot = (torch.empty(T, dtype=i32, device=dev) for _ in range(3))
+    qsl = torch.empty(R + 1, dtype=i32, device=dev)
+    sl, li = torch.empty(R, dtype=i32, device=dev), torch.empty(R, dtype=i32, device=dev)
+    ks, vs = vals.get("k_scale"), vals.get("v_scale")
+    kc, vc = vals["key_cache"], vals["value_cache"]
+    pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot, qsl, sl, li)
+    pa.pa_cache_write(vals["key"], vals["value"], kc, vc, slot, k_scale=ks, v_scale=vs)
+    out = torch.empty_like(vals["q"])
+    ws_bytes = pa.pa_attention_workspace_size(R, T, w.max_query_len, w.max_seq_len,
+                                              w.num_q_heads, w.num_kv_heads, w.head_dim)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    # host-side values settled before the timed launches (shares_blocks scans
+    # the block table on the host)
+    shared, max_q, max_seq, q = w.shares_blocks, w.max_query_len, w.max_seq_len, vals["q"]
+    evs = []
+    for k in range(max(args.warmup, 1) + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pa.pa_attention(q, kc, vc, bt, qsl, sl, max_q, max_seq, w.scale, out, ws, k_scale=ks,
+                        v_scale=vs, shared_blocks=shared)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    status, detail = pa.pa_get_status()
+    if status != pa.PA_OK:
+        raise RuntimeError(f"device checks failed ({name}): {pa.check_bits(detail)}")
+    times_ms = [a.elapsed_time(b) for a, b in evs[max(args.warmup, 1):]]
+    secs = float(np.mean(times_ms)) / 1e3
+    logical, unique = kv_bytes(w)
+    alg = unique if shared else logical
+    achieved = alg / secs / 1e9
+    line = {"workload": w.name, "num_reqs": R, "num_tokens": T, "attn_us": secs * 1e6,
+            "attn_us_min_max": [min(times_ms) * 1e3, max(times_ms) * 1e3],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": recorded_traffic(name),
+                         "kernel": "pa_attention (paged_decode_kernel + merge_kernel)",
+                         "algorithmic_bytes_per_launch": alg, "avg_launch_us": secs * 1e6,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                         "frac_of_8TBps": achieved / 8000.0}}
+    del vals, kc, vc, out, ws
+    torch.cuda.empty_cache()
+    return line
+
 
 def run_ours(args):
     import torch
@@ -387,10 +480,14 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(nst=nst, nct=nct, bt=bt, q=q, key=key, value=value, timed=True):
-        pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot, qsl,
-                             sl, li)
-        pa.pa_cache_write(key, value, kc, vc, slot, k_scale=ks, v_scale=vs)
+    def step(nst=nst, nct=nct, bt=bt, q=q, key=key, value=value, timed=True, fused=False):
+        if fused:   # the index build and the cache write as one launch
+            pa.pa_prepare_and_write(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot,
+                                    qsl, sl, li, key, value, kc, vc, k_scale=ks, v_scale=vs)
+        else:
+            pa.pa_prepare_inputs(nst, nct, bt, w.block_size, T, w.num_blocks, req, pos, slot,
+                                 qsl, sl, li)
+            pa.pa_cache_write(key, value, kc, vc, slot, k_scale=ks, v_scale=vs)
         if timed:
             a0.record(stream)
         pa.pa_attention(q, kc, vc, bt, qsl, sl, w.max_query_len, w.max_seq_len, w.scale, out, ws,
@@ -462,6 +559,36 @@ def run_ours(args):
             torch.cuda.synchronize()
             if dist is not None:
                 dist.barrier()
+    # ---- the same step with the index build and the cache write fused into
+    # one launch (pa_prepare_and_write), captured and replayed the same way
+    fused_line = None
+    try:
+        fgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fgraph, stream=gstream):
+            step(timed=False, fused=True)
+        torch.cuda.synchronize()
+        for _ in range(max(args.warmup, 1)):
+            flush.zero_()
+            fgraph.replay()
+        f_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush.zero_()
+            f_ev[k][0].record(stream)
+            fgraph.replay()
+            f_ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        f_ms = reduce_over_ranks(float(np.sum([x.elapsed_time(y) for x, y in f_ev])), "max", dist,
+                                 dev) / args.steps
+        fused_line = {"ms_per_step": f_ms, "value": reduce_over_ranks(T, "sum", dist, dev) / (f_ms / 1e3),
+                      "unit": UNIT,
+                      "what": "pa_prepare_and_write + pa_attention captured as one graph"}
+        del fgraph
+    except (RuntimeError, pa.PAError) as exc:
+        fused_line = {"error": str(exc).splitlines()[0]}
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     attn_ms = [e[2].elapsed_time(e[3]) for e in ev]
     eager_ms = reduce_over_ranks(float(np.sum(step_ms)), "max", dist, dev) / args.steps
@@ -674,7 +801,8 @@ def run_ours(args):
         flops = causal_flops(w, long_mask)
         achieved = flops / pre_s / 1e12
         roofline_prefill = {"bound": "tensor", "achieved": achieved, "peak": tf_peak,
-                            "unit": "TFLOP/s", "frac": achieved / tf_peak, "traffic": None,
+                            "unit": "TFLOP/s", "frac": achieved / tf_peak,
+                            "traffic": recorded_traffic(args.workload, "paged_prefill_kernel"),
                             "kernel": "paged_prefill_kernel (tcgen05), prefill-class requests "
                                       "alone", "flops_per_launch": flops,
                             "avg_launch_us": pre_s * 1e6,
@@ -709,10 +837,13 @@ def run_ours(args):
         if status != pa.PA_OK:
             raise RuntimeError(f"device checks failed in block ops: {pa.check_bits(detail)}")
 
+    decode_line = None
+    if world == 1 and args.decode_workload not in ("none", args.workload):
+        decode_line = attention_alone(args.decode_workload, args, pa, dev, stream, flush,
+                                      hbm_peak, peak_kind)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, threads, desc = oracle_sample(w, host_values(vals), args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline(w, host_values(vals), args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -728,6 +859,7 @@ def run_ours(args):
                        "shared_blocks_flag": bool(shared)},
             "roofline": roofline,
             "roofline_prefill": roofline_prefill,
+            "decode_workload": decode_line,
             "cpu_baseline": cpu,
             "e2e": {"value": all_tokens / (e2e_ms / args.steps / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -740,6 +872,7 @@ def run_ours(args):
             "block_ops": block_ops,
             "launch": ("cuda_graph: the three calls captured once, one replay per step"
                        if graph_ms is not None else f"eager (graph capture failed: {graph_error})"),
+            "fused_write": fused_line,
             "eager": {"ms_per_step": eager_ms, "value": all_tokens / (eager_ms / 1e3),
                       "unit": UNIT, "gpu_launches": int(eager_launches),
                       "what": "the three C-ABI calls launched one by one per step"},
