@@ -129,7 +129,9 @@ enum {
     B_VLAND,                      // [3]
     B_IFULL = B_VLAND + 3,        // [kQueue] item queue entry written by the producer
     B_IEMPTY = B_IFULL + 4,       // [kQueue] entry read by every other warp
-    B_COUNT = B_IEMPTY + 4
+    B_SPLITREQ = B_IEMPTY + 4,    // [2] per slot: the MMA warp asks for P as bf16 pairs
+    B_SPLITDONE = B_SPLITREQ + 2, // [2] per slot: P rewritten (one arrive per softmax warp)
+    B_COUNT = B_SPLITDONE + 2
 };
 constexpr int kQueue = 4;         // items the producer may run ahead
 
@@ -238,6 +240,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Whether the phase with the given parity has completed (never blocks).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
 // ---------------------------------------------------------------------------
 // Work items: per request with more than tau tokens, Hkv x ceil(n/(2 TT))
@@ -481,6 +498,34 @@ __device__ __noinline__ void split_p_halves(uint32_t colS, int halves) {
     tmem_wait_st();
 }
 
+// The MMA warp's PV of one tile when some key half of its V stayed bf16
+// (bits of `bfh`): ask the slot's softmax warps to rewrite those halves' f16
+// P as bf16 pairs and wait for them, then issue PV with one f16 MMA per 16
+// keys of an f16 half and two bf16 MMAs (hi, lo) per 16 keys of a bf16 half.
+// False when the wait ran out.
+__device__ __noinline__ bool pv_with_bf16_halves(uint64_t *req, uint64_t *done, volatile int *fmt,
+                                                 int bfh, uint32_t *nsplit, uint32_t col_o,
+                                                 uint32_t col_s, uint64_t dv0, uint32_t idPV,
+                                                 uint32_t idPVb, bool accumulate) {
+    *fmt = bfh;
+    mbar_arrive(req);
+    if (!mbar_wait(done, *nsplit & 1u)) return false;
+    ++*nsplit;
+    tc_fence_after();
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint32_t pa = col_s + (kk >> 2) * 64 + (kk & 3) * 8;
+        const uint64_t dv = dv0 + (uint64_t)(kk * 2048 >> 4);
+        const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+        if ((bfh >> (kk >> 2)) & 1) {
+            mma_ts(col_o, pa, dv, idPVb, acc);
+            mma_ts(col_o, pa + 32, dv, idPVb, 1u);
+        } else {
+            mma_ts(col_o, pa, dv, idPV, acc);
+        }
+    }
+    return true;
+}
+
 template <typename T, int D, bool F8>
 __global__ void __launch_bounds__(threads_for(Conv<T, F8>::kAny), 1)
 paged_prefill_kernel(const __grid_constant__ Params p) {
@@ -511,6 +556,7 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
     volatile int *q_items = reinterpret_cast<volatile int *>(tmem_slot + 2);   // [kQueue]
     // bf16 pools: per V stage and key half, 1 when the half stayed bf16
     volatile int *v_fmt = reinterpret_cast<volatile int *>(tmem_slot + 2 + kQueue);   // [kVSt][2]
+    volatile int *split_fmt = v_fmt + 2 * 3;   // [2]: halves of the requested P rewrite
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -523,7 +569,8 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
     if (tid == 0) {
         *abort_flag = 0;
         for (int i = 0; i < B_COUNT; ++i) {
-            const bool per_warp = (i >= B_PFULL && i < B_PFULL + 2) || (i >= B_OFREE && i < B_OFREE + 2);
+            const bool per_warp = (i >= B_PFULL && i < B_PFULL + 2) || (i >= B_OFREE && i < B_OFREE + 2) ||
+                                  (i >= B_SPLITDONE && i < B_SPLITDONE + 2);
             // FP8: Q/K/V full are signalled by the widening warps; bf16: V full
             const bool widened = (F8 && (i == B_QFULL || (i >= B_KFULL && i <= B_KFULL1))) ||
                                  (kConv && i >= B_VFULL && i < B_VFULL + 3);
@@ -695,6 +742,7 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
         long long t0 = 0;           // KV tiles of earlier items
         long long cnt[2] = {0, 0};  // tiles processed per slot (barrier phases)
         int its[2] = {0, 0};        // items processed per slot
+        uint32_t nsplit[2] = {0, 0};   // P rewrites requested per slot
         int items = 0;
         bool ok = true;
         for (int k = 0; ok; ++k, ++items) {
@@ -739,43 +787,36 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                     const uint32_t ph = (uint32_t)((t / kVSt) & 1);
                     bool v_ready = false, k_next_ready = false;
                     const long long t1 = t + 1;
-                    // V of this tile (normally landed long before P) and, over
-                    // bf16 pools, which of its key halves stayed bf16: read
-                    // before waiting for P, off the P -> PV path
-                    int bfh = 0;
+                    int bfh = 0;   // bf16 pools: key halves of this V tile that stayed bf16
                     for (int sl = 0; ok && sl < 2; ++sl) {
                         if (j >= ns[sl]) continue;
+                        if (!wait_or_fail(&bar[B_PFULL + sl], (uint32_t)(cnt[sl] & 1))) break;
                         if (!v_ready) {
                             if (!wait_or_fail(&bar[B_VFULL + st], ph)) break;
                             v_ready = true;
                             if constexpr (kConvV) bfh = v_fmt[2 * st] | (v_fmt[2 * st + 1] << 1);
                         }
-                        if (!wait_or_fail(&bar[B_PFULL + sl], (uint32_t)(cnt[sl] & 1))) break;
                         if (j == 0 && !wait_or_fail(&bar[B_OFREE + sl], (uint32_t)((its[sl] & 1) ^ 1)))
                             break;
                         tc_fence_after();
                         const uint64_t dv0 = smem_desc_sw128(smem_u32(sV + st * C::kTileBytes),
                                                              C::kHalfBytes, 1024);
-                        if (!bfh) {
+                        if (kConvV && bfh) {
+                            // rare: a key half stayed bf16 (out of line)
+                            if (!pv_with_bf16_halves(bar + B_SPLITREQ + sl, bar + B_SPLITDONE + sl,
+                                                     split_fmt + sl, bfh, &nsplit[sl],
+                                                     tmem + C::col_o(sl), tmem + C::col_s(sl), dv0,
+                                                     idPV, idPVb, j > 0)) {
+                                ok = false;
+                                break;
+                            }
+                        } else {
 #pragma unroll
                             for (int kk = 0; kk < kBN / 16; ++kk)
                                 mma_ts(tmem + C::col_o(sl),
                                        tmem + C::col_s(sl) + (kk >> 2) * 64 + (kk & 3) * 8,
                                        dv0 + (uint64_t)(kk * 2048 >> 4), idPV,
                                        (j > 0 || kk > 0) ? 1u : 0u);
-                        } else {
-                            // a bf16 half: P as hi and lo, two bf16 MMAs per step
-                            for (int kk = 0; kk < kBN / 16; ++kk) {
-                                const uint32_t pa = tmem + C::col_s(sl) + (kk >> 2) * 64 + (kk & 3) * 8;
-                                const uint64_t dv = dv0 + (uint64_t)(kk * 2048 >> 4);
-                                const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-                                if ((bfh >> (kk >> 2)) & 1) {
-                                    mma_ts(tmem + C::col_o(sl), pa, dv, idPVb, acc);
-                                    mma_ts(tmem + C::col_o(sl), pa + 32, dv, idPVb, 1u);
-                                } else {
-                                    mma_ts(tmem + C::col_o(sl), pa, dv, idPV, acc);
-                                }
-                            }
                         }
                         // O_X is read only by the epilogue, after the item's last
                         // PV; a rescale before that is ordered by S_FULL, whose
@@ -908,6 +949,39 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
         long long cnt = 0;   // tiles this slot processed (barrier phases)
         long long t0 = 0;    // KV tiles of earlier items (V ring phases)
         int items_done = 0;  // items this slot finished (O_DONE phases)
+        // Wait for a phase of `b`, meanwhile serving the MMA warp's requests
+        // (bf16 pools, rare): a key half whose V stayed bf16 (it holds a value
+        // f16 cannot) needs the last tile's f16 P rewritten as two bf16 terms
+        // hi and lo (an f16 value's 11 significant bits split exactly into
+        // 8 + 3).  The request comes after this slot's P full and before the
+        // MMA warp issues that tile's PV and the next QK, which is when these
+        // warps wait here.  Bounded like every wait.
+        uint32_t split_ph = 0;
+        auto wait_serving = [&](uint64_t *b, uint32_t par) -> bool {
+            if constexpr (!kConvV) {
+                return mbar_wait_warp(b, par);
+            } else {
+                uint64_t start = 0;
+                for (;;) {
+                    // a suspending wait: the warp takes no issue slots while
+                    // it waits (a pending request shows when it returns
+                    // without the phase)
+                    if (__all_sync(0xffffffffu, mbar_try_wait(b, par))) return true;
+                    if (__all_sync(0xffffffffu, mbar_test(&bar[B_SPLITREQ + slot], split_ph))) {
+                        tc_fence_after();
+                        split_p_halves(colS, split_fmt[slot]);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[B_SPLITDONE + slot]);
+                        split_ph ^= 1;
+                        continue;
+                    }
+                    const uint64_t now = globaltimer_ns();
+                    if (!start) start = now;
+                    else if (now - start > kWaitLimitNs) return false;
+                }
+            }
+        };
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const long long ik = item_at(k);
@@ -923,25 +997,13 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
             const int pos = valid ? it.L - it.n + tl : -1;  // last key this row sees
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < ntS; ++j, ++cnt) {
-                if (!mbar_wait_warp(&bar[B_SFULL + slot], (uint32_t)(cnt & 1))) {
+                if (!wait_serving(&bar[B_SFULL + slot], (uint32_t)(cnt & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int key0 = j * kBN;
                 const bool full_tile = key0 + kBN - 1 <= pos;
-                // bf16 pools: which key halves of this tile's V stayed bf16
-                // (V_j has normally landed and been converted by S_j)
-                int vfmt = 0;
-                if constexpr (kConvV) {
-                    const long long tv = t0 + j;
-                    const int vst = (int)(tv % kVSt);
-                    if (!mbar_wait_warp(&bar[B_VFULL + vst], (uint32_t)((tv / kVSt) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    vfmt = v_fmt[2 * vst] | (v_fmt[2 * vst + 1] << 1);
-                }
                 if constexpr (!F8) {
                     // One TMEM pass, 64 columns at a time: the half's row max (scale
                     // > 0 keeps the argmax), then P = exp2(s*c - m_ref) in packed
@@ -1026,12 +1088,6 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                     }
                     tmem_wait_st();
                     l += (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-                    // A key half whose V stayed bf16 (it holds a value f16
-                    // cannot): its f16 P, rewritten as two bf16 terms hi and
-                    // lo (an f16 value's 11 significant bits split exactly
-                    // into 8 + 3), hi in columns 64hh .. 64hh+31, lo in
-                    // 64hh+32 .. 64hh+63, for two bf16 PV MMAs.
-                    if (kConvV && vfmt) split_p_halves(colS, vfmt);
                 } else {
                     // FP8 pools: two passes over the scores (row max, then P).
                     // The one-pass form above measured slower here when scores
@@ -1139,7 +1195,7 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
             }
             if (!ok) break;
             // ---- epilogue: O / l for this row (O_DONE: once per item and slot)
-            if (!mbar_wait_warp(&bar[B_ODONE + slot], (uint32_t)(items_done & 1))) {
+            if (!wait_serving(&bar[B_ODONE + slot], (uint32_t)(items_done & 1))) {
                 ok = false;
                 break;
             }
