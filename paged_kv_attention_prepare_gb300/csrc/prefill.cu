@@ -160,25 +160,28 @@ __device__ __forceinline__ uint32_t instr_desc(int M, int N, int b_mn_major) {
     return d;
 }
 
+// The MMA and commit wrappers are executed by the whole (converged) MMA warp
+// with warp-uniform operands; one lane, chosen by elect.sync, issues.
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "{\n.reg .pred p, e;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
         "l"(a), "l"(b), "r"(id), "r"(acc)
         : "memory");
 }
 
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "{\n.reg .pred p, e;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
         "r"(a), "l"(b), "r"(id), "r"(acc)
         : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+        "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
             smem_u32(bar))
         : "memory");
 }
@@ -502,14 +505,16 @@ __device__ __noinline__ void split_p_halves(uint32_t colS, int halves) {
 // (bits of `bfh`): ask the slot's softmax warps to rewrite those halves' f16
 // P as bf16 pairs and wait for them, then issue PV with one f16 MMA per 16
 // keys of an f16 half and two bf16 MMAs (hi, lo) per 16 keys of a bf16 half.
-// False when the wait ran out.
+// Called by the whole MMA warp; false when the wait ran out.
 __device__ __noinline__ bool pv_with_bf16_halves(uint64_t *req, uint64_t *done, volatile int *fmt,
                                                  int bfh, uint32_t *nsplit, uint32_t col_o,
                                                  uint32_t col_s, uint64_t dv0, uint32_t idPV,
                                                  uint32_t idPVb, bool accumulate) {
-    *fmt = bfh;
-    mbar_arrive(req);
-    if (!mbar_wait(done, *nsplit & 1u)) return false;
+    if ((threadIdx.x & 31) == 0) {
+        *fmt = bfh;
+        mbar_arrive(req);
+    }
+    if (!mbar_wait_warp(done, *nsplit & 1u)) return false;
     ++*nsplit;
     tc_fence_after();
     for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -750,10 +755,12 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
             if (ik < 0 || !walk.find(ik, lane, it)) break;
             int ns[2] = {slot_tiles(p, it, 0), slot_tiles(p, it, 1)};
             const int nt = max(ns[0], ns[1]);
-            if (lane == 0) {
+            {
+                // The whole warp runs this loop, converged, on warp-uniform
+                // values; the MMA and commit wrappers issue from one lane.
                 const uint32_t q0 = smem_u32(sQ);
                 auto wait_or_fail = [&](uint64_t *b, uint32_t par) {
-                    if (ok && !mbar_wait(b, par)) ok = false;
+                    if (ok && !mbar_wait_warp(b, par)) ok = false;
                     return ok;
                 };
                 auto issue_qk = [&](int slot, int kst) {
@@ -841,20 +848,14 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                     if (*abort_flag) ok = false;
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            // keep the per-slot counters in step on every lane
-            for (int sl = 0; sl < 2; ++sl) {
-                cnt[sl] = __shfl_sync(0xffffffffu, cnt[sl], 0);
+            for (int sl = 0; sl < 2; ++sl)
                 if (ns[sl] > 0) ++its[sl];
-            }
             t0 += nt;
         }
         if (!ok && lane == 0) fail();
-        if (lane == 0) {
-            // Every MMA issued must be complete before TMEM is released.
-            mma_commit(&bar[B_DRAIN]);
-            mbar_wait(&bar[B_DRAIN], 0);
-        }
+        // Every MMA issued must be complete before TMEM is released.
+        mma_commit(&bar[B_DRAIN]);
+        mbar_wait_warp(&bar[B_DRAIN], 0);
     } else if (warp >= 2 + kSoftmaxWarps) {
         // =================== converters (warps 10, 11) ===================
         if constexpr (kConvV) {
@@ -1045,7 +1046,9 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                         }
                         if (hh == 1 && __any_sync(0xffffffffu, need)) {
                             // the first half's P was written against the old reference
+                            // (its store completes first)
                             const float alpha = need ? fast_exp2(m_ref - mx) : 1.f;
+                            tmem_wait_st();
                             uint32_t w[32];
                             tmem_ld32(colS, w);
                             tmem_wait_ld();
