@@ -748,6 +748,8 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
         long long cnt[2] = {0, 0};  // tiles processed per slot (barrier phases)
         int its[2] = {0, 0};        // items processed per slot
         uint32_t nsplit[2] = {0, 0};   // P rewrites requested per slot
+        int vst = 0;                   // V stage of the next tile (0 .. kVSt-1) and
+        uint32_t vph = 0;              // its mbarrier phase, advanced per tile
         int items = 0;
         bool ok = true;
         for (int k = 0; ok; ++k, ++items) {
@@ -790,8 +792,12 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                 }
                 for (int j = 0; ok && j < nt; ++j) {
                     const long long t = t0 + j;
-                    const int st = (int)(t % kVSt);   // V stage of tile t
-                    const uint32_t ph = (uint32_t)((t / kVSt) & 1);
+                    const int st = vst;            // V stage of tile t (t % kVSt)
+                    const uint32_t ph = vph;       // (t / kVSt) & 1
+                    if (++vst == kVSt) {
+                        vst = 0;
+                        vph ^= 1u;
+                    }
                     bool v_ready = false, k_next_ready = false;
                     const long long t1 = t + 1;
                     int bfh = 0;   // bf16 pools: key halves of this V tile that stayed bf16
