@@ -809,8 +809,10 @@ def run_ours(args):
         roofline_prefill = {"bound": "tensor", "achieved": achieved, "peak": tf_peak,
                             "unit": "TFLOP/s", "frac": achieved / tf_peak,
                             "traffic": recorded_traffic(args.workload, "paged_prefill_kernel"),
-                            "kernel": "paged_prefill_kernel (tcgen05), prefill-class requests "
-                                      "alone", "flops_per_launch": flops,
+                            "kernel": "pa_attention on the prefill-class requests alone: "
+                                      "paged_prefill_kernel (tcgen05), after widen_v_kernel "
+                                      "over bf16 pools at head_dim 128",
+                            "flops_per_launch": flops,
                             "avg_launch_us": pre_s * 1e6,
                             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, "
                                            "burst; fp16 runs at the same dense rate)"}

@@ -335,12 +335,18 @@ pa_status pa_zero_blocks(void *key_cache, void *value_cache, const int32_t *bloc
 
 /*
  * pa_attention_workspace_size -- bytes of workspace that let pa_attention
- * split every request's context into its preferred number of partitions.
- * Any smaller workspace (including 0) is still correct: the kernel then uses
- * longer partitions so the partial results fit (less parallelism for long
- * contexts), and without the first 256 bytes (the item counters) both
- * kernels take their work items in a fixed order instead of as their CTAs
- * free up.  Arguments are host-known bounds of the step.
+ * split every request's context into its preferred number of partitions
+ * and, over bf16 pools at head_dim 128, convert the V of the requests with
+ * more than 16 query tokens to f16 once (for up to 64 MiB of it) instead of
+ * once per 256-row tile inside the tensor-core kernel.  The workspace is
+ * laid out as 256 bytes of item counters, the split-K partials, then that
+ * copy.  Any smaller workspace (including 0) is still correct and gives the
+ * same prefill rows bit for bit: requests the copy has no room for are
+ * converted in the kernel, the split-K kernel uses longer partitions so the
+ * partial results fit (less parallelism for long contexts), and without
+ * the first 256 bytes both kernels take their work items in a fixed order
+ * instead of as their CTAs free up.  Arguments are host-known bounds of the
+ * step.
  */
 size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens,
                                    int32_t max_query_len, int32_t max_seq_len,

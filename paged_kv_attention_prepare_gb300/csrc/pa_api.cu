@@ -346,8 +346,11 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens, int32_t
                                    int32_t max_seq_len, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_dim) {
     if (num_reqs <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
-    return kCtrlBytes + decode_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len,
-                                              num_q_heads, num_kv_heads, head_dim);
+    const size_t dec = decode_workspace_size(num_reqs, num_tokens, max_query_len, max_seq_len,
+                                             num_q_heads, num_kv_heads, head_dim);
+    return kCtrlBytes + (dec + 255) / 256 * 256 +
+           prefill_widen_size(num_reqs, num_tokens, max_query_len, max_seq_len, num_kv_heads,
+                              head_dim);
 }
 
 pa_status pa_attention(const void *q, const void *key_cache, const void *value_cache,
@@ -420,10 +423,22 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
     a.ctrl = nullptr;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
+    a.pf_ws = nullptr;
+    a.pf_bytes = 0;
     if (workspace && workspace_bytes >= kCtrlBytes) {
         a.ctrl = static_cast<unsigned int *>(workspace);
         a.ws = static_cast<unsigned char *>(workspace) + kCtrlBytes;
         a.ws_bytes = workspace_bytes - kCtrlBytes;
+        // Past what the decode partials can use, the rest goes to the
+        // prefill kernel (a widened copy of bf16 V).
+        const size_t dec = (decode_workspace_size(num_reqs, num_tokens, max_query_len,
+                                                  max_seq_len, num_q_heads, num_kv_heads,
+                                                  head_dim) + 255) / 256 * 256;
+        if (a.ws_bytes > dec) {
+            a.pf_ws = static_cast<unsigned char *>(a.ws) + dec;
+            a.pf_bytes = a.ws_bytes - dec;
+            a.ws_bytes = dec;
+        }
     }
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (a.ctrl) PA_TRY_CUDA(cudaMemsetAsync(a.ctrl, 0, kCtrlWords * sizeof(unsigned int), st));

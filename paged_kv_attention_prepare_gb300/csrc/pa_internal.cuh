@@ -83,6 +83,8 @@ struct AttnArgs {
     void *out;
     void *ws;              // decode partials (after the control block)
     size_t ws_bytes;
+    void *pf_ws;           // the workspace past the decode partials (NULL: none)
+    size_t pf_bytes;
     unsigned int *ctrl;    // control block at the workspace's start (NULL: none)
     uint32_t flags;        // PA_ATTN_* bits
 };
@@ -100,6 +102,11 @@ size_t decode_workspace_size(int32_t R, int32_t T, int32_t max_q, int32_t max_se
 // Requests with at most `tau` query tokens run on the split-K kernel, longer
 // ones on the tensor-core kernel (tau == INT_MAX: everything split-K).
 int prefill_tau(const AttnArgs &a);
+// Workspace for the prefill kernel's widened copy of bf16 V (past the decode
+// partials); 0 when no request can take the prefill kernel or head_dim is
+// not 128.
+size_t prefill_widen_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq, int32_t Hkv,
+                          int32_t D);
 pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream);
 pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream);
 

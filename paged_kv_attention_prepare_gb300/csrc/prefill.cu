@@ -81,6 +81,7 @@ struct Params {
     CUtensorMap tmQ;
     CUtensorMap tmK;
     CUtensorMap tmV;
+    CUtensorMap tmVw;   // bf16 pools: the prefill requests' V widened to f16 (below)
     void *out;
     const int32_t *bt;
     const int32_t *qsl;
@@ -92,6 +93,13 @@ struct Params {
     const float *k_scale, *v_scale;   // FP8 pools (device scalars; NULL = 1)
     unsigned int *item_counter;       // zeroed before launch: items are taken in order
                                       // as CTAs free up (NULL: fixed snake order)
+    // bf16 pools: V of the prefill requests widened to f16 once per call by
+    // widen_v_kernel, token-major like a pool (NULL: not widened).  w_off[r]
+    // is request r's first token there, or -1; w_flag[page * Hkv + head] is
+    // 1 where a value of that page f16 cannot hold (the tile then comes from
+    // the pool and is converted in the kernel, with the bf16 route).
+    const int32_t *w_off;
+    const uint8_t *w_flag;
     unsigned int *status;
 };
 
@@ -562,6 +570,9 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
     // bf16 pools: per V stage and key half, 1 when the half stayed bf16
     volatile int *v_fmt = reinterpret_cast<volatile int *>(tmem_slot + 2 + kQueue);   // [kVSt][2]
     volatile int *split_fmt = v_fmt + 2 * 3;   // [2]: halves of the requested P rewrite
+    // bf16 pools: per V stage, 1 when the tile came widened (no conversion)
+    volatile int *v_src = split_fmt + 2;        // [3]
+    static_assert(B_COUNT * 8 + (2 + kQueue + 2 * 3 + 2 + 3) * 4 <= 512, "control block");
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -666,6 +677,12 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
             const int nt = max(slot_tiles(p, it, 0), ntB);
             const int32_t *row = p.bt + (long long)it.r * p.MB;
             const int ctx_pages = (it.L + kPage - 1) / kPage;
+            // bf16 pools: the request's first token in the widened V, or -1
+            int woff = -1;
+            if constexpr (kConvV) {
+                if (p.w_off && lane == 0) woff = p.w_off[it.r];
+                woff = __shfl_sync(0xffffffffu, woff, 0);
+            }
             if (lane == 0) {
                 if (!mbar_wait(&bar[B_QEMPTY], (items & 1) ^ 1)) ok = false;
                 else {
@@ -687,13 +704,20 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                 const int pg0 = j * kPagesPerTile;
                 const int npg = min(kPagesPerTile, ctx_pages - pg0);
                 int blk = 0;
+                uint32_t wfl = 0;
                 if (lane < npg) {
                     blk = row[pg0 + lane];
+                    if (kConvV && woff >= 0)
+                        wfl = p.w_flag[((long long)(woff / kPage) + pg0 + lane) * p.Hkv + it.g];
                     if (blk < 0 || blk >= p.NB) {
                         flag(p.status, PA_CHECK_BLOCK_ID);
                         blk = 0;
                     }
                 }
+                // V of this tile from the widened copy: one 128-token box
+                // per 64-dim half (counted in full, rows past the request
+                // included: the softmax zeroes keys past the context)
+                const bool vw = kConvV && woff >= 0 && !__any_sync(0xffffffffu, wfl != 0);
                 // K ring: two stages; V ring: kVSt
                 const int kst = (int)(t & 1), vst = (int)(t % kVSt);
                 const uint32_t kph = (uint32_t)((t >> 1) & 1), vph = (uint32_t)((t / kVSt) & 1);
@@ -701,6 +725,7 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                 // upper half; 64: into the staging area)
                 const uint32_t bytes = F8 ? (uint32_t)npg * kPage * D
                                           : (uint32_t)npg * C::kHalves * C::kPageHalfBytes;
+                const uint32_t vbytes = vw ? (uint32_t)C::kTileBytes : bytes;
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv) {
                     const int st = kv ? vst : kst;
@@ -709,12 +734,23 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                     uint64_t *emptyb = &bar[(kv ? B_VEMPTY : B_KEMPTY) + st];
                     unsigned char *dst = (kv ? sV : sK) + st * C::kTileBytes;
                     if (lane == 0) {
-                        if (!mbar_wait(emptyb, (kv ? vph : kph) ^ 1)) ok = false;
-                        else mbar_arrive_expect_tx(fullb, bytes);
+                        if (!mbar_wait(emptyb, (kv ? vph : kph) ^ 1)) {
+                            ok = false;
+                        } else {
+                            if (kConvV && kv) v_src[st] = vw ? 1 : 0;
+                            mbar_arrive_expect_tx(fullb, kv ? vbytes : bytes);
+                        }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
-                    if (lane < npg) {
+                    if (kConvV && kv && vw) {
+                        if (lane == 0) {
+#pragma unroll
+                            for (int h = 0; h < C::kHalves; ++h)
+                                tma_load_3d(dst + h * C::kHalfBytes, &p.tmVw, fullb, h * 64, it.g,
+                                            woff + pg0 * kPage);
+                        }
+                    } else if (lane < npg) {
                         if constexpr (F8) {
                             unsigned char *fdst =
                                 D == 128 ? dst + C::kHalfBytes + lane * kPage * 128
@@ -882,8 +918,9 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                         break;
                     }
                     const int valid = min(kBN, it.L - j * kBN) - 64 * cw;   // keys inside the context
-                    const int f = v_half_to_f16<C::kHalves>(sV + st * C::kTileBytes + cw * 64 * 128,
-                                                            C::kHalfBytes, valid, lane);
+                    const int f = v_src[st] ? 0
+                                            : v_half_to_f16<C::kHalves>(sV + st * C::kTileBytes + cw * 64 * 128,
+                                                                        C::kHalfBytes, valid, lane);
                     if (lane == 0) v_fmt[2 * st + cw] = f;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
@@ -1295,6 +1332,127 @@ pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) 
     return PA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// bf16 pools: V of the prefill requests widened to f16 once per call
+// ---------------------------------------------------------------------------
+// PV runs in f16 (P as f16 keeps 11 significant bits), so a bf16 V tile must
+// be converted before the tensor core reads it.  Converted inside the kernel,
+// every item of a (request, kv head) -- one per pair of 128-row tiles --
+// converts the same tiles again; here each page is converted once into a
+// token-major copy in the workspace, [token][kv head][dim] like a pool, for
+// the requests the prefill kernel takes (more than tau query tokens), in
+// request order while the copy has room.  A page holding a value f16 cannot
+// represent (|v| > 65280, or not finite) is flagged and its tiles take the
+// in-kernel route, which keeps such halves bf16.  Only at head_dim 128: at
+// 64 the softmax, not the conversion, bounds the kernel, and the extra pass
+// measured slower (bf16 chunk, 32/8 heads: 284 -> 290 us; 16/16: 174 -> 186).
+struct WidenParams {
+    const __nv_bfloat16 *vc;   // V pool [NB*bs][Hkv][D]
+    const int32_t *bt, *qsl, *seq_lens;
+    int32_t *w_off;            // [R] out: first token of request r in the copy, or -1
+    uint8_t *w_flag;           // [pages_cap][Hkv] out
+    __half *w_data;            // [pages_cap*16][Hkv][D]
+    int R, MB, NB, Hkv, D, tau, pages_cap;
+};
+constexpr int kWidenThreads = 256;
+constexpr int kWidenMaxReqs = 8192;   // the prefix over requests is kept in shared memory
+constexpr size_t kWidenCapBytes = (size_t)64 << 20;   // widened copy: at most 64 MiB
+
+__global__ void __launch_bounds__(kWidenThreads) widen_v_kernel(const WidenParams w) {
+    extern __shared__ int32_t s_first[];   // [R + 1]: first page of each request in the copy
+    __shared__ int s_scan[33];
+    const int tid = threadIdx.x, lane = tid & 31, nthreads = blockDim.x;
+    auto pages_of = [&](int r) -> int {
+        const int n = w.qsl[r + 1] - w.qsl[r];
+        const int L = w.seq_lens[r];
+        return (n > w.tau && L > 0) ? (L + kPage - 1) / kPage : 0;
+    };
+    const int per = (w.R + nthreads - 1) / nthreads;
+    const int r0 = min(w.R, tid * per), r1 = min(w.R, r0 + per);
+    int local = 0;
+    for (int r = r0; r < r1; ++r) local += pages_of(r);
+    int total = 0;
+    int run = block_exclusive_scan(local, s_scan, total);
+    for (int r = r0; r < r1; ++r) {
+        s_first[r] = run;
+        run += pages_of(r);
+    }
+    if (tid == 0) s_first[w.R] = total;
+    __syncthreads();
+    // A request is widened when all its pages fit (the prefix is monotone,
+    // so the widened requests are a leading run of the prefill requests).
+    if (blockIdx.x == 0)
+        for (int r = tid; r < w.R; r += nthreads) {
+            const bool has = s_first[r + 1] > s_first[r];
+            w.w_off[r] = (has && s_first[r + 1] <= w.pages_cap) ? s_first[r] * kPage : -1;
+        }
+    // One warp per (page of the copy, kv head): 16 rows of D values.
+    const int upr = w.D / 8;   // 16-byte units per row
+    const long long units = (long long)min(total, w.pages_cap) * w.Hkv;
+    const long long nw = (long long)gridDim.x * (nthreads / 32);
+    for (long long u = (long long)blockIdx.x * (nthreads / 32) + (tid >> 5); u < units; u += nw) {
+        const int pgc = (int)(u / w.Hkv), h = (int)(u % w.Hkv);
+        // the request holding copy page pgc: the last r with s_first[r] <= pgc
+        int lo = 0, hi = w.R - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_first[mid] <= pgc) lo = mid;
+            else hi = mid - 1;
+        }
+        const int r = lo;
+        if (s_first[r + 1] > w.pages_cap) continue;   // the request does not fit
+        const int pg = pgc - s_first[r];
+        const int L = w.seq_lens[r];
+        const int blk = w.bt[(long long)r * w.MB + pg];
+        // a bad block id: flagged, so the kernel reads (and checks) the pool
+        uint32_t fl = (blk < 0 || blk >= w.NB) ? 0x8000u : 0u;
+        if (!fl) {
+            for (int x = lane; x < kPage * upr; x += 32) {
+                const int i = x / upr, c = x % upr;
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+                    w.vc + ((long long)(blk * kPage + i) * w.Hkv + h) * w.D + c * 8));
+                if (pg * kPage + i < L) {
+                    // magnitude above 0x477F (65280) sets bit 15 of (m + 0x3880)
+                    fl |= (v.x & 0x7fff7fffu) + 0x38803880u;
+                    fl |= (v.y & 0x7fff7fffu) + 0x38803880u;
+                    fl |= (v.z & 0x7fff7fffu) + 0x38803880u;
+                    fl |= (v.w & 0x7fff7fffu) + 0x38803880u;
+                }
+                uint4 o;
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(&v);
+                uint32_t *dst = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __half2 hv = __floats2half2_rn(__uint_as_float(src[e] << 16),
+                                                   __uint_as_float(src[e] & 0xffff0000u));
+                    dst[e] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                *reinterpret_cast<uint4 *>(w.w_data + ((long long)(pgc * kPage + i) * w.Hkv + h) * w.D +
+                                           c * 8) = o;
+            }
+        }
+        fl = __reduce_or_sync(0xffffffffu, fl & 0x80008000u);
+        if (lane == 0) w.w_flag[(long long)pgc * w.Hkv + h] = fl ? 1 : 0;
+    }
+}
+
+}  // namespace prefill
+
+size_t prefill_widen_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq, int32_t Hkv,
+                          int32_t D) {
+    using namespace prefill;
+    if (max_q <= kTauDefault || R <= 0 || R > kWidenMaxReqs || Hkv <= 0 || D != 128) return 0;
+    const long long reqs = min((long long)R, (long long)T / (kTauDefault + 1));
+    if (reqs <= 0) return 0;
+    const long long per_page = (long long)Hkv * (kPage * D * 2 + 1);
+    long long pages = reqs * (((long long)max_seq + kPage - 1) / kPage);
+    const long long cap = (long long)(kWidenCapBytes / (size_t)per_page);
+    if (pages > cap) pages = cap;
+    auto up = [](long long x) { return (x + 255) / 256 * 256; };
+    return (size_t)(up((long long)R * 4) + up(pages * Hkv) + pages * kPage * Hkv * D * 2);
+}
+
+namespace prefill {
 }  // namespace prefill
 
 int prefill_tau(const AttnArgs &a) {
@@ -1341,6 +1499,46 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     // upper bound on the row tiles
     const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T + 2 * TT - 1) / (2 * TT));
     const bool bf16 = a.dtype == PA_BF16;
+    // bf16 pools: the prefill requests' V widened once, into the workspace's
+    // tail: [R] first tokens, then [pages][Hkv] flags, then the f16 rows.
+    if (bf16 && !f8 && a.D == 128 && a.pf_ws && a.R <= kWidenMaxReqs) {
+        auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+        const size_t off_bytes = up((size_t)a.R * 4);
+        const size_t row_bytes = (size_t)a.Hkv * a.D * 2;   // one token, every kv head
+        long long pages = a.pf_bytes > off_bytes
+                              ? (long long)((a.pf_bytes - off_bytes) / (kPage * row_bytes + a.Hkv))
+                              : 0;
+        if (pages > INT32_MAX / (4 * kPage)) pages = INT32_MAX / (4 * kPage);
+        while (pages > 0 && off_bytes + up((size_t)pages * a.Hkv) + (size_t)pages * kPage * row_bytes >
+                                a.pf_bytes)
+            --pages;
+        if (pages > 0) {
+            unsigned char *base = static_cast<unsigned char *>(a.pf_ws);
+            WidenParams w;
+            w.vc = static_cast<const __nv_bfloat16 *>(a.vc);
+            w.bt = a.bt;
+            w.qsl = a.qsl;
+            w.seq_lens = a.seq_lens;
+            w.w_off = reinterpret_cast<int32_t *>(base);
+            w.w_flag = base + off_bytes;
+            w.w_data = reinterpret_cast<__half *>(base + off_bytes + up((size_t)pages * a.Hkv));
+            w.R = a.R;
+            w.MB = a.MB;
+            w.NB = a.NB;
+            w.Hkv = a.Hkv;
+            w.D = a.D;
+            w.tau = tau;
+            w.pages_cap = (int)pages;
+            if (!encode_sw128(&prm.tmVw, w.w_data, a.D, a.Hkv, (uint64_t)pages * kPage, 1, kBN))
+                return PA_ERR_CUDA;
+            widen_v_kernel<<<2 * num_sms(), kWidenThreads, (size_t)(a.R + 1) * sizeof(int32_t),
+                             stream>>>(w);
+            PA_TRY_CUDA(cudaGetLastError());
+            note_launch();
+            prm.w_off = w.w_off;
+            prm.w_flag = w.w_flag;
+        }
+    }
     if (f8 && a.D == 128)
         return bf16 ? launch_typed<__nv_bfloat16, 128, true>(prm, items, stream)
                     : launch_typed<__half, 128, true>(prm, items, stream);
