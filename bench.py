@@ -145,6 +145,7 @@ KERNEL_SOURCES = {
     "paged_decode_kernel": ("decode.cu", "decode_fp16.cu", "pa_internal.cuh"),
     "paged_prefill_kernel": ("prefill.cu", "pa_internal.cuh"),
     "cache_write_kernel": ("cache_write.cu", "pa_internal.cuh"),
+    "prepare_write_kernel": ("prep_write.cu", "pa_internal.cuh"),
 }
 
 
@@ -810,8 +811,10 @@ def run_ours(args):
                             "unit": "TFLOP/s", "frac": achieved / tf_peak,
                             "traffic": recorded_traffic(args.workload, "paged_prefill_kernel"),
                             "kernel": "pa_attention on the prefill-class requests alone: "
-                                      "paged_prefill_kernel (tcgen05), after widen_v_kernel "
-                                      "over bf16 pools at head_dim 128",
+                                      "paged_prefill_kernel (tcgen05)" +
+                                      (", after widen_v_kernel (V to f16 once per call)"
+                                       if (w.dtype == "bf16" and w.head_dim == 128
+                                           and w.kv_cache_dtype != "fp8_e4m3") else ""),
                             "flops_per_launch": flops,
                             "avg_launch_us": pre_s * 1e6,
                             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, "

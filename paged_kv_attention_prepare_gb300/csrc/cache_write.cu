@@ -7,7 +7,8 @@
 // loaded together (the rows' addresses do not depend on the slot), up to four
 // K and four V units per lane in flight, in the widest unit the addresses
 // allow (16 bytes for the usual aligned rows); then the stores.  The grid
-// covers every token in one wave up to eight 256-thread CTAs per SM.
+// covers every token in one wave up to five 256-thread CTAs per SM (the
+// registers' limit at 48 a thread), more tokens per warp beyond that.
 // Sources are read through the read-only path; a negative slot skips the
 // token; a slot past the pool is flagged and skipped.
 #include <cuda_fp8.h>
@@ -17,11 +18,13 @@
 namespace pa {
 
 constexpr int kWriteThreads = 256;
+constexpr int kWriteCtasPerSm = 5;    // 40 warps an SM: registers capped at 48 a thread
+constexpr int kWriteF8CtasPerSm = 4;  // FP8: 32 warps an SM, 64 registers (48 spill)
 constexpr int kWriteWarps = kWriteThreads / 32;
 constexpr int kWriteUnroll = 4;   // units of each row in flight per lane
 
 template <typename V>
-__global__ void __launch_bounds__(kWriteThreads)
+__global__ void __launch_bounds__(kWriteThreads, kWriteCtasPerSm)
 cache_write_kernel(const V *__restrict__ key, const V *__restrict__ value, int64_t stride_v,
                    V *__restrict__ kc, V *__restrict__ vc, const int32_t *__restrict__ slots,
                    int32_t T, int32_t row_v, int64_t num_slots, unsigned int *status) {
@@ -56,10 +59,11 @@ cache_write_kernel(const V *__restrict__ key, const V *__restrict__ value, int64
     }
 }
 
-// CTAs for T tokens, one warp each, up to eight CTAs per SM.
-static int write_blocks(int32_t T) {
+// CTAs for T tokens, one warp each, up to one wave of them (ctas_per_sm
+// resident on each SM).
+static int write_blocks(int32_t T, int ctas_per_sm = kWriteCtasPerSm) {
     long long blocks = ((long long)T + kWriteWarps - 1) / kWriteWarps;
-    const long long cap = 8LL * num_sms();
+    const long long cap = (long long)ctas_per_sm * num_sms();
     if (blocks > cap) blocks = cap;
     return blocks < 1 ? 1 : (int)blocks;
 }
@@ -109,7 +113,7 @@ pa_status launch_cache_write(const void *key, const void *value, int64_t stride_
 // bytes of bf16/fp16 in, 8 bytes out) per unit, up to four units of K and
 // four of V in flight.
 template <typename T>
-__global__ void __launch_bounds__(kWriteThreads)
+__global__ void __launch_bounds__(kWriteThreads, kWriteF8CtasPerSm)
 cache_write_fp8_kernel(const T *__restrict__ key, const T *__restrict__ value, int64_t stride,
                        uint8_t *__restrict__ kc, uint8_t *__restrict__ vc,
                        const int32_t *__restrict__ slots, int32_t T_, int32_t row,
@@ -161,7 +165,7 @@ pa_status launch_cache_write_fp8(const void *key, const void *value, int64_t str
         return PA_ERR_UNSUPPORTED;
     unsigned int *st = status_word();
     if (!st) return PA_ERR_CUDA;
-    const int blocks = write_blocks(T);
+    const int blocks = write_blocks(T, kWriteF8CtasPerSm);
     if (src == PA_BF16)
         cache_write_fp8_kernel<__nv_bfloat16><<<blocks, kWriteThreads, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(key), static_cast<const __nv_bfloat16 *>(value),

@@ -19,7 +19,8 @@
 
 namespace pa {
 
-constexpr int kFusedThreads = 512;
+constexpr int kFusedThreads = 256;
+constexpr int kFusedCtasPerSm = 4;   // 32 warps an SM, 64 registers a thread
 constexpr int kUnroll = 4;   // 16-byte units of each row in flight per lane
 
 struct WriteArgs {
@@ -33,13 +34,33 @@ struct WriteArgs {
 // kMode 0: 16-bit pools (a row is row * 2 / 16 16-byte vectors); 1: FP8
 // pools, bf16 source; 2: FP8 pools, fp16 source.
 template <int kMode>
-__global__ void __launch_bounds__(kFusedThreads)
+__global__ void __launch_bounds__(kFusedThreads, kFusedCtasPerSm)
 prepare_write_kernel(const PrepArgs a, const WriteArgs w, unsigned int *status) {
     extern __shared__ int32_t s_start[];  // [R + 1]: first flat token of each request
     __shared__ int32_t s_scan[33];
     const int tid = threadIdx.x, lane = tid & 31;
     const int nthreads = blockDim.x;
     const int R = a.R;
+
+    // The warp's first token's K and V row units are loaded before the scan:
+    // their addresses depend only on the token, so the copy's first memory
+    // round trip overlaps the scan's.
+    using Src = uint4;
+    using Dst = typename std::conditional<kMode == 0, uint4, uint2>::type;
+    const int nu = w.row / 8;   // 16-byte source units per row (and pool units)
+    Src kx[kUnroll], vx[kUnroll];
+    auto load_first = [&](long long t) {
+        const Src *ksrc = static_cast<const Src *>(w.key) + t * (w.stride / 8);
+        const Src *vsrc = static_cast<const Src *>(w.value) + t * (w.stride / 8);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (lane + 32 * u < nu) {
+                kx[u] = __ldg(ksrc + lane + 32 * u);
+                vx[u] = __ldg(vsrc + lane + 32 * u);
+            }
+    };
+    const long long t_first = (long long)blockIdx.x * (nthreads / 32) + (tid >> 5);
+    if (t_first < a.T) load_first(t_first);
 
     // ---- the scan of num_scheduled_tokens, as in the index build
     const int per = (R + nthreads - 1) / nthreads;
@@ -76,7 +97,7 @@ prepare_write_kernel(const PrepArgs a, const WriteArgs w, unsigned int *status) 
     const float ks = (kMode != 0 && w.k_scale) ? *w.k_scale : 1.f;
     const float vs = (kMode != 0 && w.v_scale) ? *w.v_scale : 1.f;
     const long long nwarps = (long long)gridDim.x * (nthreads / 32);
-    for (long long t = (long long)blockIdx.x * (nthreads / 32) + (tid >> 5); t < a.T; t += nwarps) {
+    for (long long t = t_first; t < a.T; t += nwarps) {
         if (t >= total || R == 0) {
             if (lane == 0) {
                 a.req[t] = -1;
@@ -85,20 +106,11 @@ prepare_write_kernel(const PrepArgs a, const WriteArgs w, unsigned int *status) 
             }
             continue;
         }
-        // The token's first row units are loaded before its slot is known
-        // (their addresses do not depend on it), so the two latencies overlap.
-        using Src = uint4;
-        using Dst = typename std::conditional<kMode == 0, uint4, uint2>::type;
-        const int nu = w.row / 8;   // 16-byte source units per row (and pool units)
+        // A later token's first row units are loaded before its slot is
+        // known (their addresses do not depend on it): the latencies overlap.
+        if (t != t_first) load_first(t);
         const Src *ksrc = static_cast<const Src *>(w.key) + t * (w.stride / 8);
         const Src *vsrc = static_cast<const Src *>(w.value) + t * (w.stride / 8);
-        Src kx[kUnroll], vx[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (lane + 32 * u < nu) {
-                kx[u] = __ldg(ksrc + lane + 32 * u);
-                vx[u] = __ldg(vsrc + lane + 32 * u);
-            }
         // The request holding t: the last one whose start is <= t (every
         // lane searches, so the result needs no broadcast).
         int lo = 0, hi = R - 1;
@@ -174,7 +186,7 @@ pa_status launch_prepare_write(const PrepArgs &a, const void *key, const void *v
                                          (int)smem));
     const int warps = kFusedThreads / 32;
     long long blocks = ((long long)a.T + warps - 1) / warps;
-    const long long cap = 4LL * num_sms();   // four 512-thread CTAs fill an SM
+    const long long cap = (long long)kFusedCtasPerSm * num_sms();   // one wave
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     unsigned int *st = status_word();
