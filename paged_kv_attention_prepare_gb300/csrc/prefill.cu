@@ -1038,7 +1038,12 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
             }
             const int tl = (it.mt * 2 + slot) * p.TT + row / p.G;   // token in the request
             const bool valid = row < p.TT * p.G && tl < it.n;
-            const int pos = valid ? it.L - it.n + tl : -1;  // last key this row sees
+            // The last key this row sees.  A row that is never written out (the
+            // empty rows of a tile whose G does not divide 128, or tokens past
+            // the request) sees every key: with -1 it would take the masking
+            // path on every tile and hold the slot's P back (28/4 heads:
+            // 345 -> 275 us on a 5000-token chunk).  Its values stay in its own row.
+            const int pos = valid ? it.L - it.n + tl : INT_MAX / 2;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < ntS; ++j, ++cnt) {
                 if (!wait_serving(&bar[B_SFULL + slot], (uint32_t)(cnt & 1))) {
