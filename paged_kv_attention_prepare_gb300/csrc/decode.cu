@@ -82,6 +82,8 @@ struct Params {
     const float *k_scale; // FP8 pools: cached value = element * scale (device scalars)
     const float *v_scale;
     unsigned int *status;
+    int launch_pdl;       // host side: the split-K grid as a programmatic dependent of the grid before
+    int launch_part;      // host side: 0 split-K grid and merge pass, 1 the grid only, 2 the merge only
 };
 
 // Marker for an FP8 E4M3 cache element.
@@ -1201,6 +1203,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const __grid_co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = (blockIdx.x % groups) * kHeads + warp / WPH;
     const int sub = warp % WPH;
+    // A grid launched after this one as a programmatic dependent (the rest of
+    // the tensor-core kernel's items) may be scheduled now: it reads nothing
+    // this pass writes.
+    if (threadIdx.x == 0) grid_launch_dependents();
     grid_dependency_wait();   // every write of the split-K kernel is visible past here
     if (r >= p.R) return;
     const int4 meta = reinterpret_cast<const int4 *>(p.req_meta)[r];
@@ -1318,7 +1324,11 @@ static pa_status launch_merge(const Params &prm, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // Right behind the split-K grid: a programmatic dependent (its CTAs wait
+    // in griddepcontrol.wait for that grid).  Launched later on its own (the
+    // merge-only part), an ordinary launch: it starts once everything before
+    // it in the stream has finished.
+    cfg.numAttrs = prm.launch_part == 2 ? 0 : 1;
     PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, merge_kernel<T, D, RPI, WPH, B>, prm));
     note_launch();
     return PA_OK;
@@ -1343,8 +1353,25 @@ pa_status launch_split_k(Params &prm, long long max_items, cudaStream_t stream) 
     long long grid = (long long)per_sm * num_sms();
     if (max_items < grid) grid = max_items;
     if (grid < 1) grid = 1;
-    paged_decode_kernel<TQ, TC, D, RPI, kGroups><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
-    PA_TRY_CUDA(cudaGetLastError());
+    if (prm.launch_pdl) {
+        // Beside the tensor-core kernel's first grid: this grid may start
+        // while it runs (it reads nothing that grid writes), its CTAs taking
+        // the SMs that grid leaves free, then the rest as its CTAs exit.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = S::kBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, paged_decode_kernel<TQ, TC, D, RPI, kGroups>, prm));
+    } else {
+        paged_decode_kernel<TQ, TC, D, RPI, kGroups><<<(int)grid, kThreads, S::kBytes, stream>>>(prm);
+        PA_TRY_CUDA(cudaGetLastError());
+    }
     note_launch();
     return PA_OK;
 }
@@ -1352,10 +1379,12 @@ pa_status launch_split_k(Params &prm, long long max_items, cudaStream_t stream) 
 template <typename TQ, typename TC, int D, int RPI>
 pa_status launch_typed(Params &prm, long long max_items, long long merge_splits, bool groups,
                        cudaStream_t stream) {
-    const pa_status st = groups ? launch_split_k<TQ, TC, D, RPI, true>(prm, max_items, stream)
-                                : launch_split_k<TQ, TC, D, RPI, false>(prm, max_items, stream);
-    if (st != PA_OK) return st;
-    if (merge_splits > 0 && prm.R > 0) {
+    if (prm.launch_part != 2) {
+        const pa_status st = groups ? launch_split_k<TQ, TC, D, RPI, true>(prm, max_items, stream)
+                                    : launch_split_k<TQ, TC, D, RPI, false>(prm, max_items, stream);
+        if (st != PA_OK) return st;
+    }
+    if (merge_splits > 0 && prm.R > 0 && prm.launch_part != 1) {
         switch (merge_warps_per_head(merge_splits, prm.R, prm.Hq)) {
             case 1:   // at most 8 partitions: a batch of 8 rows, more warps resident
                 return merge_splits <= 8 ? launch_merge<TQ, D, RPI, 1, 8>(prm, stream)
@@ -1472,6 +1501,8 @@ pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream) {
     prm.qscale = a.scale * 1.4426950408889634f;
     prm.status = status_word();
     if (!prm.status) return PA_ERR_CUDA;
+    prm.launch_pdl = a.pdl ? 1 : 0;
+    prm.launch_part = a.decode_part;
     prm.item_counter = a.ctrl ? a.ctrl + kCtrlDecodeCounter : nullptr;
     const int rpi = rows_per_item(prm.G, a.max_q < tau ? a.max_q : tau);
 

@@ -443,6 +443,11 @@ pa_status pa_attention_ex(const void *q, const void *key_cache, const void *valu
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (a.ctrl) PA_TRY_CUDA(cudaMemsetAsync(a.ctrl, 0, kCtrlWords * sizeof(unsigned int), st));
     const int tau = prefill_tau(a);
+    a.pdl = false;
+    a.decode_part = 0;
+    // Both request classes possible: the two kernels side by side.
+    if (a.ctrl && tau != INT_MAX && max_query_len > tau && num_reqs > 1)
+        return launch_attention_overlapped(a, tau, st);
     const pa_status r = launch_decode(a, tau, st);
     if (r != PA_OK) return r;
     return launch_prefill(a, tau, st);

@@ -87,6 +87,8 @@ struct AttnArgs {
     size_t pf_bytes;
     unsigned int *ctrl;    // control block at the workspace's start (NULL: none)
     uint32_t flags;        // PA_ATTN_* bits
+    bool pdl;              // launch the split-K kernel as a programmatic dependent
+    int decode_part;       // launch_decode: 0 split-K grid + merge, 1 the grid only, 2 the merge only
 };
 
 // Bytes at the start of a caller's workspace kept for per-call counters.
@@ -109,6 +111,12 @@ size_t prefill_widen_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq, 
                           int32_t D);
 pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream);
 pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream);
+// A batch that may hold both request classes: the tensor-core kernel's first
+// grid on a third of the SMs, the split-K kernel beside it on the rest, a
+// second tensor-core grid that takes the remaining prefill items as SMs free
+// up, then the merge pass.  Same results as launch_decode then
+// launch_prefill.
+pa_status launch_attention_overlapped(const AttnArgs &a, int tau, cudaStream_t stream);
 
 // Encode a 3-D TMA map over one pool viewed as [NB*bs][Hkv][D] elements of
 // `elt` bytes, with a box of min(128 bytes, a row) x 1 kv head x `box_rows`

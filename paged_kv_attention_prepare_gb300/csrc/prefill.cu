@@ -575,6 +575,10 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
     static_assert(B_COUNT * 8 + (2 + kQueue + 2 * 3 + 2 + 3) * 4 <= 512, "control block");
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // A grid launched after this one as a programmatic dependent (the
+    // split-K kernel beside this grid) may be scheduled at once: it reads
+    // nothing this kernel writes.
+    if (tid == 0) grid_launch_dependents();
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -1316,7 +1320,8 @@ bool encode_sw128(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, u
 }
 
 template <typename T, int D, bool F8>
-pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) {
+pa_status launch_typed(const Params &prm, long long items, long long max_ctas, bool pdl,
+                       cudaStream_t stream) {
     using C = Cfg<D>;
     constexpr int kSmem = (F8 && D == 64) ? C::kSmemF8Land : C::smem(Conv<T, F8>::kV ? 3 : 2);
     static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -1328,13 +1333,45 @@ pa_status launch_typed(const Params &prm, long long items, cudaStream_t stream) 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
         if (dev < 64) configured[dev] = true;
     }
-    long long grid = num_sms();
+    long long grid = max_ctas;
     if (items < grid) grid = items;
     if (grid < 1) return PA_OK;
-    paged_prefill_kernel<T, D, F8><<<(int)grid, threads_for(Conv<T, F8>::kAny), kSmem, stream>>>(prm);
-    PA_TRY_CUDA(cudaGetLastError());
+    if (pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(threads_for(Conv<T, F8>::kAny));
+        cfg.dynamicSmemBytes = kSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        PA_TRY_CUDA(cudaLaunchKernelEx(&cfg, paged_prefill_kernel<T, D, F8>, prm));
+    } else {
+        paged_prefill_kernel<T, D, F8><<<(int)grid, threads_for(Conv<T, F8>::kAny), kSmem, stream>>>(prm);
+        PA_TRY_CUDA(cudaGetLastError());
+    }
     note_launch();
     return PA_OK;
+}
+
+// One launch of the instantiation for these pools and head size.
+pa_status launch_kind(const AttnArgs &a, const Params &prm, long long items, long long max_ctas,
+                      bool pdl, cudaStream_t stream) {
+    const bool f8 = a.cache_dtype == PA_FP8_E4M3;
+    const bool bf16 = a.dtype == PA_BF16;
+    if (f8 && a.D == 128)
+        return bf16 ? launch_typed<__nv_bfloat16, 128, true>(prm, items, max_ctas, pdl, stream)
+                    : launch_typed<__half, 128, true>(prm, items, max_ctas, pdl, stream);
+    if (f8)
+        return bf16 ? launch_typed<__nv_bfloat16, 64, true>(prm, items, max_ctas, pdl, stream)
+                    : launch_typed<__half, 64, true>(prm, items, max_ctas, pdl, stream);
+    if (a.D == 128)
+        return bf16 ? launch_typed<__nv_bfloat16, 128, false>(prm, items, max_ctas, pdl, stream)
+                    : launch_typed<__half, 128, false>(prm, items, max_ctas, pdl, stream);
+    return bf16 ? launch_typed<__nv_bfloat16, 64, false>(prm, items, max_ctas, pdl, stream)
+                : launch_typed<__half, 64, false>(prm, items, max_ctas, pdl, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -1457,9 +1494,6 @@ size_t prefill_widen_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq, 
     return (size_t)(up((long long)R * 4) + up(pages * Hkv) + pages * kPage * Hkv * D * 2);
 }
 
-namespace prefill {
-}  // namespace prefill
-
 int prefill_tau(const AttnArgs &a) {
     const int G = a.Hq / a.Hkv;
     // The tensor-core kernel takes the row max of unscaled scores: scale > 0.
@@ -1467,10 +1501,13 @@ int prefill_tau(const AttnArgs &a) {
     return prefill::kTauDefault;
 }
 
-pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
-    using namespace prefill;
-    if (tau == INT_MAX || a.max_q <= tau) return PA_OK;
-    Params prm;
+namespace prefill {
+
+// The kernel's parameters for this call (tensor maps, the widened V when
+// bf16 pools at head_dim 128 leave room for it in the workspace: its pass is
+// launched here) and an upper bound on the work items.
+static pa_status build(const AttnArgs &a, int tau, cudaStream_t stream, Params &prm,
+                       long long &items) {
     memset(&prm, 0, sizeof prm);
     const int G = a.Hq / a.Hkv;
     const uint64_t slots = (uint64_t)a.NB * a.bs;
@@ -1502,7 +1539,7 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
     prm.status = status_word();
     if (!prm.status) return PA_ERR_CUDA;
     // upper bound on the row tiles
-    const long long items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T + 2 * TT - 1) / (2 * TT));
+    items = (long long)a.Hkv * ((long long)a.R + ((long long)a.T + 2 * TT - 1) / (2 * TT));
     const bool bf16 = a.dtype == PA_BF16;
     // bf16 pools: the prefill requests' V widened once, into the workspace's
     // tail: [R] first tokens, then [pages][Hkv] flags, then the f16 rows.
@@ -1544,17 +1581,53 @@ pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
             prm.w_flag = w.w_flag;
         }
     }
-    if (f8 && a.D == 128)
-        return bf16 ? launch_typed<__nv_bfloat16, 128, true>(prm, items, stream)
-                    : launch_typed<__half, 128, true>(prm, items, stream);
-    if (f8)
-        return bf16 ? launch_typed<__nv_bfloat16, 64, true>(prm, items, stream)
-                    : launch_typed<__half, 64, true>(prm, items, stream);
-    if (a.D == 128)
-        return bf16 ? launch_typed<__nv_bfloat16, 128, false>(prm, items, stream)
-                    : launch_typed<__half, 128, false>(prm, items, stream);
-    return bf16 ? launch_typed<__nv_bfloat16, 64, false>(prm, items, stream)
-                : launch_typed<__half, 64, false>(prm, items, stream);
+    return PA_OK;
+}
+
+}  // namespace prefill
+
+pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream) {
+    using namespace prefill;
+    if (tau == INT_MAX || a.max_q <= tau) return PA_OK;
+    Params prm;
+    long long items = 0;
+    const pa_status st = build(a, tau, stream, prm, items);
+    if (st != PA_OK) return st;
+    return launch_kind(a, prm, items, num_sms(), false, stream);
+}
+
+// HBM-bound split-K work and tensor-bound prefill work side by side.  The
+// split-K kernel keeps ~96% of its bandwidth on 120 of the 152 SMs and ~80%
+// on 100, so the tensor-core kernel's first grid takes a third of the SMs
+// from the start; the split-K grid (a programmatic dependent: it may start
+// at once) fills the rest, and its CTAs that do not fit wait for SMs to free
+// up.  A second tensor-core grid, a programmatic dependent of the split-K
+// grid, takes the remaining prefill items from the same counter as SMs free
+// up.  Items go to CTAs as they free up in both grids, so every item is
+// computed once, by one CTA, with the same result as in a single grid.  The
+// merge pass comes last as an ordinary launch: it starts once every grid
+// before it has finished, so no CTA of it sits on an SM waiting.
+pa_status launch_attention_overlapped(const AttnArgs &a, int tau, cudaStream_t stream) {
+    using namespace prefill;
+    Params prm;
+    long long items = 0;
+    pa_status st = build(a, tau, stream, prm, items);
+    if (st != PA_OK) return st;
+    const long long first = num_sms() / 3 > 0 ? num_sms() / 3 : 1;
+    st = launch_kind(a, prm, items, first, false, stream);
+    if (st != PA_OK) return st;
+    AttnArgs b = a;
+    b.pdl = true;
+    b.decode_part = 1;
+    st = launch_decode(b, tau, stream);
+    if (st != PA_OK) return st;
+    if (items > first) {
+        st = launch_kind(a, prm, items - first, num_sms(), true, stream);
+        if (st != PA_OK) return st;
+    }
+    b.pdl = false;
+    b.decode_part = 2;
+    return launch_decode(b, tau, stream);
 }
 
 }  // namespace pa
