@@ -112,7 +112,7 @@ size_t prefill_widen_size(int32_t R, int32_t T, int32_t max_q, int32_t max_seq, 
 pa_status launch_decode(const AttnArgs &a, int tau, cudaStream_t stream);
 pa_status launch_prefill(const AttnArgs &a, int tau, cudaStream_t stream);
 // A batch that may hold both request classes: the tensor-core kernel's first
-// grid on a third of the SMs, the split-K kernel beside it on the rest, a
+// grid on two fifths of the SMs, the split-K kernel beside it on the rest, a
 // second tensor-core grid that takes the remaining prefill items as SMs free
 // up, then the merge pass.  Same results as launch_decode then
 // launch_prefill.
