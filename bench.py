@@ -149,6 +149,14 @@ KERNEL_SOURCES = {
 }
 
 
+# The prefill-class requests of a workload timed alone form a batch of their
+# own; for the mixed step that batch is the `chunk` workload's shape (one
+# 5000-token chunk at 2048, 32/8, D 128), whose ncu summary gives its traffic.
+# (Inside the mixed step's own launches, under ncu, the kernels run one after
+# another, so the first tensor-core grid would take every item itself.)
+PREFILL_ALONE = {"mixed": "chunk"}
+
+
 def kernel_source_hash(kernel: str = "paged_decode_kernel") -> str:
     """Hash of a kernel's sources with comments and blank space removed: a
     comment edit does not change the kernel the profile measured."""
@@ -809,7 +817,8 @@ def run_ours(args):
         achieved = flops / pre_s / 1e12
         roofline_prefill = {"bound": "tensor", "achieved": achieved, "peak": tf_peak,
                             "unit": "TFLOP/s", "frac": achieved / tf_peak,
-                            "traffic": recorded_traffic(args.workload, "paged_prefill_kernel"),
+                            "traffic": recorded_traffic(PREFILL_ALONE.get(args.workload, args.workload),
+                                                        "paged_prefill_kernel"),
                             "kernel": "pa_attention on the prefill-class requests alone: "
                                       "paged_prefill_kernel (tcgen05)" +
                                       (", after widen_v_kernel (V to f16 once per call)"

@@ -1400,7 +1400,8 @@ constexpr int kWidenThreads = 256;
 constexpr int kWidenMaxReqs = 8192;   // the prefix over requests is kept in shared memory
 constexpr size_t kWidenCapBytes = (size_t)64 << 20;   // widened copy: at most 64 MiB
 
-__global__ void __launch_bounds__(kWidenThreads) widen_v_kernel(const WidenParams w) {
+template <int D>
+__global__ void __launch_bounds__(kWidenThreads, 4) widen_v_kernel(const WidenParams w) {
     extern __shared__ int32_t s_first[];   // [R + 1]: first page of each request in the copy
     __shared__ int s_scan[33];
     const int tid = threadIdx.x, lane = tid & 31, nthreads = blockDim.x;
@@ -1428,8 +1429,11 @@ __global__ void __launch_bounds__(kWidenThreads) widen_v_kernel(const WidenParam
             const bool has = s_first[r + 1] > s_first[r];
             w.w_off[r] = (has && s_first[r + 1] <= w.pages_cap) ? s_first[r] * kPage : -1;
         }
-    // One warp per (page of the copy, kv head): 16 rows of D values.
-    const int upr = w.D / 8;   // 16-byte units per row
+    // One warp per (page of the copy, kv head): 16 rows of D values, every
+    // 16-byte unit of them loaded before any is converted (one memory round
+    // trip per page, not one per unit).
+    constexpr int upr = D / 8;                   // 16-byte units per row
+    constexpr int kPer = kPage * upr / 32;       // units per lane
     const long long units = (long long)min(total, w.pages_cap) * w.Hkv;
     const long long nw = (long long)gridDim.x * (nthreads / 32);
     for (long long u = (long long)blockIdx.x * (nthreads / 32) + (tid >> 5); u < units; u += nw) {
@@ -1449,10 +1453,17 @@ __global__ void __launch_bounds__(kWidenThreads) widen_v_kernel(const WidenParam
         // a bad block id: flagged, so the kernel reads (and checks) the pool
         uint32_t fl = (blk < 0 || blk >= w.NB) ? 0x8000u : 0u;
         if (!fl) {
-            for (int x = lane; x < kPage * upr; x += 32) {
-                const int i = x / upr, c = x % upr;
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
-                    w.vc + ((long long)(blk * kPage + i) * w.Hkv + h) * w.D + c * 8));
+            uint4 vin[kPer];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int x = lane + 32 * k, i = x / upr, c = x % upr;
+                vin[k] = __ldg(reinterpret_cast<const uint4 *>(
+                    w.vc + ((long long)(blk * kPage + i) * w.Hkv + h) * D + c * 8));
+            }
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int x = lane + 32 * k, i = x / upr, c = x % upr;
+                const uint4 v = vin[k];
                 if (pg * kPage + i < L) {
                     // magnitude above 0x477F (65280) sets bit 15 of (m + 0x3880)
                     fl |= (v.x & 0x7fff7fffu) + 0x38803880u;
@@ -1469,7 +1480,7 @@ __global__ void __launch_bounds__(kWidenThreads) widen_v_kernel(const WidenParam
                                                    __uint_as_float(src[e] & 0xffff0000u));
                     dst[e] = *reinterpret_cast<uint32_t *>(&hv);
                 }
-                *reinterpret_cast<uint4 *>(w.w_data + ((long long)(pgc * kPage + i) * w.Hkv + h) * w.D +
+                *reinterpret_cast<uint4 *>(w.w_data + ((long long)(pgc * kPage + i) * w.Hkv + h) * D +
                                            c * 8) = o;
             }
         }
@@ -1573,8 +1584,8 @@ static pa_status build(const AttnArgs &a, int tau, cudaStream_t stream, Params &
             w.pages_cap = (int)pages;
             if (!encode_sw128(&prm.tmVw, w.w_data, a.D, a.Hkv, (uint64_t)pages * kPage, 1, kBN))
                 return PA_ERR_CUDA;
-            widen_v_kernel<<<2 * num_sms(), kWidenThreads, (size_t)(a.R + 1) * sizeof(int32_t),
-                             stream>>>(w);
+            widen_v_kernel<128><<<4 * num_sms(), kWidenThreads, (size_t)(a.R + 1) * sizeof(int32_t),
+                                  stream>>>(w);
             PA_TRY_CUDA(cudaGetLastError());
             note_launch();
             prm.w_off = w.w_off;

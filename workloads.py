@@ -181,6 +181,14 @@ def mixed_step(seed: int = 2, hq: int = 32, hkv: int = 8) -> Workload:
                  hq, hkv, 128, "bf16")
 
 
+def chunk(seed: int = 5) -> Workload:
+    """The mixed step's prompt chunk alone: one 5000-token chunk at 2048
+    computed; 32 q / 8 kv heads, D 128, bf16 (a batch of the tensor-core
+    kernel only: one grid over every SM)."""
+    rng = np.random.default_rng(seed)
+    return _make("chunk-5000@2048-gqa32/8-d128", [5000], [2048], rng, 32, 8, 128, "bf16")
+
+
 def chunk_fp8_d64(seed: int = 5) -> Workload:
     """One 5000-token prompt chunk at 2048 computed over FP8 (E4M3) pools at
     head_dim 64; 32 q / 8 kv heads, bf16 q."""
@@ -242,6 +250,7 @@ NAMED = {
     # tokens (126 of 128 rows)
     "mixed_gqa28_4": lambda seed=2: mixed_step(seed, 28, 4),
     "chunk_fp8_d64": lambda seed=5: chunk_fp8_d64(seed),
+    "chunk": lambda seed=5: chunk(seed),
 }
 
 
