@@ -838,17 +838,18 @@ paged_prefill_kernel(const __grid_constant__ Params p) {
                         vst = 0;
                         vph ^= 1u;
                     }
-                    bool v_ready = false, k_next_ready = false;
                     const long long t1 = t + 1;
+                    // This tile's V is waited for before the tile's first P (it
+                    // is normally in long before it), so the PV issues as soon
+                    // as P is; the next tile's K only before the first QK that
+                    // reads it (over FP8 pools it may still be being widened).
+                    if (!wait_or_fail(&bar[B_VFULL + st], ph)) break;
                     int bfh = 0;   // bf16 pools: key halves of this V tile that stayed bf16
+                    if constexpr (kConvV) bfh = v_fmt[2 * st] | (v_fmt[2 * st + 1] << 1);
+                    bool k_next_ready = false;
                     for (int sl = 0; ok && sl < 2; ++sl) {
                         if (j >= ns[sl]) continue;
                         if (!wait_or_fail(&bar[B_PFULL + sl], (uint32_t)(cnt[sl] & 1))) break;
-                        if (!v_ready) {
-                            if (!wait_or_fail(&bar[B_VFULL + st], ph)) break;
-                            v_ready = true;
-                            if constexpr (kConvV) bfh = v_fmt[2 * st] | (v_fmt[2 * st + 1] << 1);
-                        }
                         if (j == 0 && !wait_or_fail(&bar[B_OFREE + sl], (uint32_t)((its[sl] & 1) ^ 1)))
                             break;
                         tc_fence_after();
