@@ -367,15 +367,20 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t num_tokens,
  * g = h / (num_q_heads / num_kv_heads):
  *     out[t][h] = sum_{j <= p} softmax_j(scale * q[t][h] . K_r[j][g]) V_r[j][g]
  * where K_r[j] is the cache entry at block_table[r][j / block_size],
- * offset j % block_size.  Accumulation is fp32; the softmax weights enter
- * the weighted sum of V as f16, or for bf16 as two bf16 terms (the weight
- * rounded, then the remainder rounded: 16 significant bits); the output is
- * rounded once to the element type.
+ * offset j % block_size.  Accumulation is fp32 and the output is rounded
+ * once to the element type.  The softmax weights enter the weighted sum of
+ * V with at least 11 significant bits.  On the split-K kernel they are f16
+ * over fp16 and FP8 pools, and two bf16 terms over bf16 pools (the weight
+ * rounded, then the remainder rounded: 16 significant bits).  On the
+ * tensor-core kernel they are f16, with V converted to f16 first: exactly,
+ * apart from values below f16's normal range, which round to its subnormals
+ * (an absolute error of at most 2^-25).  A 64-key half of a V tile holding a
+ * value that f16 cannot represent keeps bf16 V, and its weights enter as two
+ * bf16 terms, exactly.
  *
  * Requests with more than 16 query tokens run on the tensor-core (tcgen05)
  * kernel when num_q_heads / num_kv_heads <= 128 and scale > 0; every other
- * request runs on the split-K kernel.  Both
- * compute the definition above in the same precision.
+ * request runs on the split-K kernel.
  *
  * Arguments:
  *   q             device [num_tokens][num_q_heads][head_dim], contiguous
