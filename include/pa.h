@@ -21,8 +21,9 @@
  *
  * Conventions shared by every call:
  *   - Ownership: the caller allocates and owns every buffer.  The library
- *     allocates nothing per call; its only device state is one status word
- *     per device (a file-scope device variable).
+ *     allocates nothing per call.  Its device state is file-scope device
+ *     variables: one status word per device, and the fixed scratch array
+ *     that only pa_attention_noalloc uses (below).
  *   - Pointers named "device" are CUDA device pointers (any memory a kernel
  *     can dereference); sizes and scalars are host values.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream).  The
